@@ -1,0 +1,18 @@
+"""mxfa -- MXFP8 block-scaled FlashAttention (forward + backward) for GB300.
+
+The compute path is the C-ABI library ``libmxfa.so`` (hand-written CUDA for
+sm_103a); :mod:`.mxfa` is a thin ctypes binding over it whose functions carry
+the C names (``mxfa_quantize``, ``mxfa_fwd``, ``mxfa_bwd``, ...).  PyTorch is
+used only for device memory and streams.  There is no CPU fallback: every
+call fails loudly when the library is missing.
+"""
+from . import inputs  # noqa: F401  (seeded synthetic workloads; no arithmetic)
+
+
+def __getattr__(name):
+    if name.startswith("mxfa_") or name in ("lib", "MxfaError", "status_string",
+                                            "Mx", "quantize", "attention_fwd",
+                                            "attention_bwd", "rmsnorm_quant"):
+        from . import mxfa as _m
+        return getattr(_m, name)
+    raise AttributeError(name)
