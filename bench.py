@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark: one MXFP8 block-scaled attention training step on one GB300.
+
+Workload (the LLM-shaped causal self-attention): B=2, H=16, S=8192, D=128,
+Q/K/V/dO bf16 ~ N(0,1) from seed 1.  One step is the whole hot path:
+quantize Q, K (1x32 along D) and V (32x1 along keys) with packed scales ->
+forward -> quantize Q, K, dO (32x32) and V (1x32) -> backward with FP32 dQ
+reduction.  value = algorithmic PFLOP/s of the step (forward 4*D and backward
+10*D FLOPs per unmasked (query, key) pair, S^2/2 pairs per causal head).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxfa|reference]
+
+One JSON line on rank 0.  Under torchrun (N > 1) every rank runs the same
+per-GPU workload (replicas; no collective on the data path) and value is the
+sum of all ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, H, S, D = 2, 16, 8192, 128
+CAUSAL = True
+SEED = 1
+METRIC = "MXFP8 attn fwd+bwd PFLOP/s (1 GB300)"
+NOMINAL_FP8_TFLOPS = 4500.0
+
+
+def attn_flops(b, h, s, d, causal, per_pair):
+    pairs = b * h * (s * s / 2 if causal else s * s)
+    return per_pair * d * pairs
+
+
+FWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 4)
+BWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 10)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="mxfa", choices=["mxfa", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-components", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class GpuStep:
+    """Preallocated buffers and the hot path as a sequence of C-ABI calls."""
+
+    def __init__(self, torch, mx, dev, qb, kb, vb, dob):
+        self.torch, self.mx, self.dev = torch, mx, dev
+        to = lambda b: torch.from_numpy(b.view("int16")).view(torch.bfloat16).reshape(B * S, H, D)
+        self.host_in = [to(b).pin_memory() for b in (qb, kb, vb, dob)]
+        self.q, self.k, self.v, self.do = [t.to(dev) for t in self.host_in]
+        self.seqs = mx.Seqs.dense(B, S)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        pk = lambda blk: torch.empty(self.seqs.ptiles * H * (16 if blk == 2 else 512), **u8)
+        self.mx_out = {}
+        for name, blk in (("qR", 0), ("kR", 0), ("vC", 1), ("qS", 2), ("kS", 2), ("doS", 2), ("vR", 0)):
+            self.mx_out[name] = mx.Mx(torch.empty((B * S, H, D), **u8), None, pk(blk), blk)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.o = torch.empty((B * S, H, D), **bf)
+        self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty((B * S, H, D), **bf) for _ in range(3))
+        self.ws = torch.empty(mx.mxfa_bwd_workspace_size(B * S, H, D, 0), **u8)
+        self.host_out = [torch.empty((B * S, H, D), dtype=torch.bfloat16).pin_memory()
+                         for _ in range(4)]
+        self.scale = 1.0 / math.sqrt(D)
+        self.launches_per_step = 7 + 1 + 3  # 7 quantizations, forward, backward (pre, main, post)
+
+    def quant(self, x, name):
+        m = self.mx_out[name]
+        out = self.mx.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+        s = self.seqs
+        self.mx.mxfa_quantize(x, s.total, H, D, m.blk, None, s.nseq, s.max_len, s.ptiles, out)
+
+    def fwd(self):
+        m = self.mx_out
+        self.mx.mxfa_fwd(m["qR"].mx_in(), m["kR"].mx_in(), m["vC"].mx_in(), B, S, H, D, self.scale,
+                         CAUSAL, self.o, self.lse)
+
+    def bwd(self, dq_mode=0, dq_static=1.0):
+        m = self.mx_out
+        self.mx.mxfa_bwd(m["qS"].mx_in(), m["kS"].mx_in(), m["vR"].mx_in(), m["doS"].mx_in(), self.o,
+                         self.do, self.lse, B, S, H, D, self.scale, CAUSAL, dq_mode, dq_static,
+                         self.dq, self.dk, self.dv, self.ws, self.ws.numel())
+
+    def step(self):
+        self.quant(self.q, "qR")
+        self.quant(self.k, "kR")
+        self.quant(self.v, "vC")
+        self.fwd()
+        self.quant(self.q, "qS")
+        self.quant(self.k, "kS")
+        self.quant(self.do, "doS")
+        self.quant(self.v, "vR")
+        self.bwd()
+
+    def step_e2e(self):
+        for dst, src in zip((self.q, self.k, self.v, self.do), self.host_in):
+            dst.copy_(src, non_blocking=True)
+        self.step()
+        for dst, src in zip(self.host_out, (self.o, self.dq, self.dk, self.dv)):
+            dst.copy_(src, non_blocking=True)
+
+
+def time_loop(torch, fn, iters, warmup, flush=None):
+    """Mean per-call device time (ms) with CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+    tot = 0.0
+    for _ in range(iters):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / iters
+
+
+def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
+    """Per-kernel figures on the same workload, plus the other workloads' rows."""
+    from mxfp8_block_scaled_fa_gb300 import inputs
+    dev = st.dev
+    res = {}
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    fp8_peak = 2.0 * bf16_peak
+    st.step()
+    t_fwd = time_loop(torch, st.fwd, iters, warmup)
+    t_bwd = time_loop(torch, st.bwd, iters, warmup)
+    t_bwd16 = time_loop(torch, lambda: st.bwd(1, 1.0), iters, warmup)
+    st.bwd()
+    t_q = time_loop(torch, lambda: st.quant(st.q, "qR"), iters, warmup, flush)
+    t_qs = time_loop(torch, lambda: st.quant(st.q, "qS"), iters, warmup, flush)
+    t_qc = time_loop(torch, lambda: st.quant(st.v, "vC"), iters, warmup, flush)
+    n = B * S * H * D
+    res["fwd"] = {"ms": t_fwd, "pflops": FWD_FLOPS / t_fwd / 1e12,
+                  "frac_of_4.5": FWD_FLOPS / t_fwd / 1e9 / NOMINAL_FP8_TFLOPS}
+    res["bwd_fp32_dq"] = {"ms": t_bwd, "pflops": BWD_FLOPS / t_bwd / 1e12,
+                          "frac_of_4.5": BWD_FLOPS / t_bwd / 1e9 / NOMINAL_FP8_TFLOPS}
+    res["bwd_fp16_dq"] = {"ms": t_bwd16, "pflops": BWD_FLOPS / t_bwd16 / 1e12,
+                          "frac_of_4.5": BWD_FLOPS / t_bwd16 / 1e9 / NOMINAL_FP8_TFLOPS}
+    for key, t, sfb in (("quantize_row", t_q, 1 / 32), ("quantize_col", t_qc, 1 / 32),
+                        ("quantize_sq", t_qs, 1 / 1024)):
+        gbs = n * (2 + 1 + sfb) / t / 1e6
+        res[key] = {"ms": t, "GB_s": gbs, "frac_of_hbm": gbs / hbm_peak}
+    # fused RMSNorm + Quantize (row + column layouts) on X[32768, 2048]
+    x, g, _ = inputs.fused_inputs()
+    xd = torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(dev)
+    gd = torch.from_numpy(g).to(dev)
+    outs = mx.rmsnorm_quant(xd, gd, 1e-6, 8192, 16, outputs=("row", "col"))
+    structs = {k: mx.MxOut(v.data.data_ptr(), v.sf_compact.data_ptr(), v.sf_packed.data_ptr())
+               for k, v in outs.items()}
+    rms = lambda: mx.mxfa_rmsnorm_quant(xd, gd, 32768, 2048, 1e-6, 8192, 16, structs["row"],
+                                         structs["col"], None)
+    t_rms = time_loop(torch, rms, iters, warmup, flush)
+    nb = 32768 * 2048 * (2 + 2 * (1 + 1 / 32))
+    res["rmsnorm_quant_row_col"] = {"ms": t_rms, "GB_s": nb / t_rms / 1e6,
+                                    "frac_of_hbm": nb / t_rms / 1e6 / hbm_peak}
+    del xd, outs
+    # jagged cross-attention, 64 sequences (varlen forward + backward)
+    qb, kb, vb, dob, cu_q, cu_k = inputs.jagged_attn()
+    lq, lk = cu_q[1:] - cu_q[:-1], cu_k[1:] - cu_k[:-1]
+    sq, sk = mx.Seqs.varlen(lq, dev), mx.Seqs.varlen(lk, dev)
+    tq = lambda b: torch.from_numpy(b.view("int16")).view(torch.bfloat16).to(dev)
+    Hj = 8
+    qR, kR, vC = mx.quantize(tq(qb), 0, sq), mx.quantize(tq(kb), 0, sk), mx.quantize(tq(vb), 1, sk)
+    qS, kS, vR = mx.quantize(tq(qb), 2, sq), mx.quantize(tq(kb), 2, sk), mx.quantize(tq(vb), 0, sk)
+    do_t = tq(dob)
+    doS = mx.quantize(do_t, 2, sq)
+    o, lse = mx.attention_fwd(qR, kR, vC, sq, sk, 1 / math.sqrt(D), False)
+    out = (o, lse)
+    t_jf = time_loop(torch, lambda: mx.attention_fwd(qR, kR, vC, sq, sk, 1 / math.sqrt(D), False,
+                                                     out=out), iters, warmup)
+    ws = torch.empty(mx.mxfa_bwd_workspace_size(sq.total, Hj, D, 0), dtype=torch.uint8, device=dev)
+    grads = tuple(torch.empty_like(t) for t in (o, o, o))
+    grads = (grads[0], torch.empty((sk.total, Hj, D), dtype=torch.bfloat16, device=dev),
+             torch.empty((sk.total, Hj, D), dtype=torch.bfloat16, device=dev))
+    t_jb = time_loop(torch, lambda: mx.attention_bwd(qS, kS, vR, doS, o, do_t, lse, sq, sk,
+                                                     1 / math.sqrt(D), False, ws=ws, out=grads),
+                     iters, warmup)
+    pairs = float(np.sum(lq.astype(np.float64) * lk)) * Hj
+    res["jagged_fwd"] = {"ms": t_jf, "pflops": 4 * D * pairs / t_jf / 1e12}
+    res["jagged_bwd"] = {"ms": t_jb, "pflops": 10 * D * pairs / t_jb / 1e12}
+    step_q = (4 * t_q + 2 * t_qs + t_qc) / 7 * 7
+    res["step_share"] = {"fwd": t_fwd, "bwd": t_bwd, "quantize_x7": step_q}
+    del flush_buf
+    torch.cuda.synchronize()
+    return res
+
+
+import numpy as np  # noqa: E402  (used by components)
+
+
+# ------------------------------------------------------------ CPU oracle legs
+def oracle_sample(qb, kb, vb, dob, s_len, n_heads):
+    """Causal s_len-token prefix of n_heads (batch, head) pairs as one oracle call."""
+    from mxfp8_block_scaled_fa_gb300 import inputs
+    pairs = [(i // H, i % H) for i in range(min(n_heads, B * H))]
+    take = lambda x: np.stack([inputs.bf16_bits_to_f32(x[b, :s_len, h, :]) for b, h in pairs],
+                              axis=1).astype(np.float64)
+    return take(qb), take(kb), take(vb), take(dob), len(pairs)
+
+
+def run_oracle_step(oracle, q, k, v, do, scale):
+    o, lse = oracle.method_fwd(q, k, v, None, None, scale, True, True, 128, 8.0, True)
+    o_bf = np.asarray(o, np.float32).astype(np.float64)
+    oracle.method_bwd(q, k, v, do, o_bf, lse, None, None, scale, True, True, True)
+
+
+def cpu_baseline(qb, kb, vb, dob, s_len=4096):
+    import oracle
+    cores = oracle.num_threads()
+    q, k, v, do, n = oracle_sample(qb, kb, vb, dob, s_len, cores)
+    t0 = time.perf_counter()
+    run_oracle_step(oracle, q, k, v, do, 1.0 / math.sqrt(D))
+    dt = time.perf_counter() - t0
+    flops = 14 * D * (s_len * s_len / 2) * n
+    return {"value": flops / dt / 1e15, "unit": "PFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fwd+bwd (quantize, forward, backward) of the causal {s_len}-token prefix of "
+                      f"{n} (batch, head) pairs of the workload, heads in parallel, {dt:.1f} s",
+            "seconds": dt}
+
+
+def reference_arm(args):
+    """The CPU oracle as the reference implementation, on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from mxfp8_block_scaled_fa_gb300 import inputs
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=SEED)
+    cores = oracle.num_threads()
+    s_len = 2048
+    q, k, v, do, n = oracle_sample(qb, kb, vb, dob, s_len, cores)
+    scale = 1.0 / math.sqrt(D)
+    for _ in range(args.warmup):
+        run_oracle_step(oracle, q, k, v, do, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(oracle, q, k, v, do, scale)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 14 * D * (s_len * s_len / 2) * n
+    val = flops / dt / 1e15
+    sample = (f"per step: quantize + forward + backward of the causal {s_len}-token prefix of {n} "
+              f"(batch, head) pairs of the workload")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "PFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llm-causal B2 H16 S8192 D128 fwd+bwd", "B": B, "H": H,
+                       "seq_len": S, "D": D, "causal": CAUSAL, "seed": SEED},
+            "cpu_baseline": {"value": val, "unit": "PFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "PFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    import torch
+    import torch.distributed as dist
+    from mxfp8_block_scaled_fa_gb300 import build, inputs
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    bf16_peak, hbm_peak, peak_src = load_peaks()
+    fp8_peak = 2.0 * bf16_peak
+
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=SEED)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(qb, kb, vb, dob)
+    st = GpuStep(torch, mxfa, dev, qb, kb, vb, dob)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        st.step()
+    assert mxfa.device_status() == 0, "device status after warm-up"
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        st.step()
+    e1.record()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    # end to end through the same C-ABI calls, host buffers in and out
+    for _ in range(2):
+        st.step_e2e()
+    barrier()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(args.steps):
+        st.step_e2e()
+    a1.record()
+    barrier()
+    ms_e2e = a0.elapsed_time(a1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    assert mxfa.device_status() == 0, "device status after timing"
+    comp = None
+    if not args.no_components:
+        comp = components(torch, mxfa, st, args.steps, args.warmup, bf16_peak, hbm_peak)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    flops = (FWD_FLOPS + BWD_FLOPS) * world
+    value = flops / (ms * 1e-3) / 1e15
+    bytes_io = B * S * H * D * 2 * 4
+    line = {"metric": METRIC, "value": value, "unit": "PFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "llm-causal B2 H16 S8192 D128 fwd+bwd (fp32 dQ)", "B": B,
+                       "H": H, "seq_len": S, "D": D, "causal": CAUSAL, "seed": SEED,
+                       "flops_per_step": FWD_FLOPS + BWD_FLOPS,
+                       "l2": "inputs 268 MB (bf16 Q, K, V, dO) > 129 MB L2; no flush",
+                       "parallelism": f"replicas x{world}"},
+            "frac_of_nominal_4.5": value / world * 1e3 / NOMINAL_FP8_TFLOPS,
+            "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e15, "unit": "PFLOP/s",
+                    "ms_per_step": ms_e2e, "h2d_bytes_per_step": bytes_io,
+                    "d2h_bytes_per_step": bytes_io},
+            "gpu_launches": st.launches_per_step * args.steps,
+            "clocks": clk}
+    if comp is not None:
+        sh = comp["step_share"]
+        dom = "bwd" if sh["bwd"] >= sh["fwd"] else "fwd"
+        t_dom = sh[dom]
+        fl = BWD_FLOPS if dom == "bwd" else FWD_FLOPS
+        achieved = fl / (t_dom * 1e-3) / 1e12
+        line["roofline"] = {"bound": "tensor", "kernel": "attn_bwd_kernel (mxfa_bwd call incl. "
+                            "pre/post)" if dom == "bwd" else "attn_fwd_kernel",
+                            "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                            "frac": achieved / fp8_peak, "traffic": None,
+                            "peak_source": f"{peak_src} bf16 burst {bf16_peak} x 2 (fp8/bf16 "
+                                           f"nominal ratio)"}
+        line["components"] = comp
+    if cpu is not None:
+        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,215 @@
+/*
+ * mxfa.h -- C ABI of libmxfa: MXFP8 block-scaled FlashAttention (forward and
+ * backward) for NVIDIA GB300 (sm_103a), with its quantizers and the fused
+ * RMSNorm+Quantize producer.
+ *
+ * Sources for what each call computes (web pages on one subject):
+ *  [MX]   "Low-Precision FlashAttention-4: End-to-End Block-Scaled Attention
+ *         on Blackwell" (kongchang.com), section "Why MXFP8" -- OCP MX: 32
+ *         elements share one power-of-two (E8M0) scale, E4M3 payload.
+ *  [TMEM] "MXFP8 FlashAttention-4 Hits 2.85 Petaflops in Meta's Production
+ *         Training" (andresseo.expert), section "Inside the TMEM Bargain and
+ *         Zero-Gather Jagged Pipeline" -- online P / dS quantization, square
+ *         32x32 blocks for Q, K, dO in the backward pass, dQ reduction in
+ *         FP16 with static scaling, split addressing for jagged inputs,
+ *         fused RMSNorm / GEMM producers.
+ *  [KDIM] "Meta's MXFP8 FlashAttention-4 kernel, tackling TMEM scale-factor
+ *         constraints, hits up to 1.6x over BF16" (theclarity.today),
+ *         paragraphs 1-3 -- scales along the MMA K dimension (D for Q and K,
+ *         N for V); scales padded and permuted to 128-aligned layouts for TMA.
+ *  [ITEMS] "Meta's FlashAttention-4 Achieves 2.85 PF/s with MXFP8 on Blackwell
+ *         GPUs" (brifing.si), items 5 (jagged), 6 (backward), 7 (fused
+ *         producers).
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises (except mxfa_get_device_status).
+ *    Work is enqueued on the caller's stream (a cudaStream_t; 0 = legacy).
+ *  - Attention tensors are token-major: x[token][head][d] with d contiguous
+ *    (dense [B][S][H][D] is the varlen layout with B sequences of length S).
+ *    D must be 128.
+ *  - Payload pointers, scale pointers and bf16 outputs must be 16-byte
+ *    aligned (else MXFA_ERR_MISALIGNED).
+ *  - Arguments are checked before any launch; launch failures are reported
+ *    as MXFA_ERR_CUDA.  Device-side failures (a bounded wait that expired,
+ *    an index check that skipped an access) are recorded in a status word
+ *    read by mxfa_get_device_status.  Nothing aborts the process.
+ *
+ * Scale-factor layouts
+ *  compact (one E8M0 byte per block, logical order):
+ *    ROW  [tokens][H*D/32]            1x32 along d
+ *    COL  [sum ceil(len/32)][H*D]     32x1 along the tokens of a sequence
+ *    SQ   [sum ceil(len/32)][H*D/32]  32x32 within a head
+ *  packed (what the attention kernels read; rows padded per sequence to a
+ *  multiple of 128 with value 0x7F, i.e. 2^0):
+ *    tiles = sum over sequences of ceil(len/128); tile t of head h is entry
+ *    (t * H + h).
+ *    ROW  512-byte atom per entry: byte (r%32)*16 + (r/32)*4 + k for token r
+ *         of the tile and d-block k  (the tensor core's 128x4 scale layout)
+ *    COL  512-byte atom per entry: byte (d%32)*16 + (d/32)*4 + k for column d
+ *         and 32-token block k of the tile
+ *    SQ   16 bytes per entry: byte 4*k + c for token block k and d-block c
+ */
+#ifndef MXFA_H
+#define MXFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mxfa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MXFA_OK = 0,
+  MXFA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum        */
+  MXFA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. D!=128) */
+  MXFA_ERR_MISALIGNED = 3,    /* pointer not 16-byte aligned             */
+  MXFA_ERR_WORKSPACE_TOO_SMALL = 4,
+  MXFA_ERR_CUDA = 5,          /* a CUDA call or kernel launch failed     */
+  MXFA_ERR_TIMEOUT = 6,       /* a kernel's bounded wait expired         */
+  MXFA_ERR_DEVICE_INDEX = 7   /* a kernel's index check skipped an access */
+} mxfa_status;
+
+typedef enum {
+  MXFA_BLK_ROW = 0, /* 1x32 along d (MMA K = D: Q, K forward; V backward)    */
+  MXFA_BLK_COL = 1, /* 32x1 along tokens of a sequence (MMA K = N: V forward) */
+  MXFA_BLK_SQ = 2   /* 32x32, transpose-invariant (Q, K, dO backward)         */
+} mxfa_block;
+
+/* An MXFP8 operand as the attention kernels read it: E4M3 payload in the
+ * source layout (compact, never padded) and E8M0 scales in the packed
+ * layout of its block kind. */
+typedef struct {
+  const uint8_t* data;
+  const uint8_t* sf;
+} mxfa_mx;
+
+/* Outputs of a quantizing call; sf_compact and sf_packed may be NULL. */
+typedef struct {
+  uint8_t* data;
+  uint8_t* sf_compact;
+  uint8_t* sf_packed;
+} mxfa_mx_out;
+
+/* The forward kernel moves its running row maximum only when it grows by
+ * more than this many log2 units (O and l keep the stale maximum exactly). */
+#define MXFA_FWD_RESCALE_THRESHOLD 8.0f
+
+const char* mxfa_status_string(mxfa_status s);
+int mxfa_version(void);
+
+/* Number of packed tiles: sum over sequences of ceil(len/128).  cu_seqlens
+ * here is a HOST array of nseq+1 offsets; NULL means nseq sequences of
+ * seqlen tokens.  Returns -1 on bad input. */
+int64_t mxfa_packed_tiles(const int32_t* cu_seqlens_host, int nseq, int seqlen);
+/* Bytes of a packed scale tensor for `tiles` packed tiles and H heads. */
+size_t mxfa_sf_packed_bytes(mxfa_block blk, int64_t tiles, int H);
+
+/* mxfa_quantize -- bf16 -> E4M3 payload + E8M0 scales ([MX]; orientation
+ * per [KDIM] and [TMEM]).
+ *  x          bf16 [tokens][H][D], D = 128
+ *  blk        block kind
+ *  cu_seqlens DEVICE int32[nseq+1] sequence offsets, or NULL for nseq
+ *             sequences of max_seqlen tokens each (tokens = nseq*max_seqlen)
+ *  max_seqlen longest sequence (sizes the grid)
+ *  packed_tiles  mxfa_packed_tiles() of the same sequences (bounds the
+ *             packed output; ignored when out->sf_packed is NULL)
+ *  out        payload [tokens][H][D] and the compact and/or packed scales
+ * Scale: floor(log2 amax) - 8 clamped to [0, 254]; payload RNE, saturating
+ * at 448; a block holding Inf/NaN gets scale 0xFF and payload 0x7F. */
+mxfa_status mxfa_quantize(const void* x, int64_t tokens, int H, int D, mxfa_block blk,
+                          const int32_t* cu_seqlens, int nseq, int max_seqlen,
+                          int64_t packed_tiles, const mxfa_mx_out* out, mxfa_stream_t stream);
+
+/* mxfa_sf_pack -- compact scales -> packed scales for the same block kind,
+ * values unchanged, padding rows 0x7F ([KDIM] paragraph 3, [ITEMS] item 5:
+ * only the scale factors are scattered and padded; payload stays compact).
+ * Arguments as mxfa_quantize. */
+mxfa_status mxfa_sf_pack(const uint8_t* sf_compact, int64_t tokens, int H, int D, mxfa_block blk,
+                         const int32_t* cu_seqlens, int nseq, int max_seqlen,
+                         int64_t packed_tiles, uint8_t* sf_packed, mxfa_stream_t stream);
+
+/* mxfa_fwd -- dense forward ([KDIM] paragraphs 1-2, [TMEM]).
+ *  q, k       ROW-quantized payload [B][S][H][128] + packed ROW scales
+ *  v          COL-quantized payload + packed COL scales
+ *  causal     mask key > query
+ *  o          bf16 [B][S][H][128] (output)
+ *  lse        fp32 [B][H][S] natural-log log-sum-exp (output)
+ * P is quantized per 32 keys in registers; the row sum is taken before. */
+mxfa_status mxfa_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H,
+                     int D, float softmax_scale, int causal, void* o, float* lse,
+                     mxfa_stream_t stream);
+
+/* mxfa_varlen_fwd -- jagged forward ([TMEM] split addressing, [ITEMS] 5).
+ *  cu_seqlens_q/k  DEVICE int32[nseq+1]; q/o/lse follow cu_seqlens_q,
+ *                  k/v follow cu_seqlens_k; every key length >= 1
+ *  ptiles_q/k      mxfa_packed_tiles() of the query / key sequences
+ *  lse             fp32 [H][total_q]
+ *  causal          top-left aligned (key index > query index masked) */
+mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, int64_t total_q, int64_t total_k,
+                            int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
+                            int causal, void* o, float* lse, mxfa_stream_t stream);
+
+/* Workspace of the backward pass: Delta (fp32 [H][total_q]) followed by the
+ * dQ accumulator ([total_q][H][128], fp32 when dq_mode = 0, fp16 when 1). */
+size_t mxfa_bwd_workspace_size(int64_t total_q, int H, int D, int dq_mode);
+
+/* mxfa_bwd -- dense backward, five GEMMs with recompute ([TMEM], [ITEMS] 6).
+ *  q, k, dO   SQ-quantized payload + packed SQ scales (32x32 blocks serve
+ *             both GEMM orientations)
+ *  v          ROW-quantized payload + packed ROW scales
+ *  o, dout    bf16 O and dO [B][S][H][128];  lse fp32 [B][H][S] from mxfa_fwd
+ *  dq_mode    0: dQ reduced in fp32;  1: fp16 with static scale
+ *             dq_static_scale (a power of two; partials are multiplied by it
+ *             before the fp16 reduction and divided after)
+ *  dq, dk, dv bf16 outputs [B][S][H][128]
+ *  ws         caller-owned workspace of mxfa_bwd_workspace_size() bytes
+ * P is recomputed from the square-block Q, K and lse, quantized 1x32 along
+ * queries for dV; dS = P (dP - Delta) is quantized in 32x32 blocks. */
+mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dout_mx,
+                     const void* o, const void* dout, const float* lse, int B, int S, int H, int D,
+                     float softmax_scale, int causal, int dq_mode, float dq_static_scale, void* dq,
+                     void* dk, void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
+
+/* mxfa_varlen_bwd -- jagged backward; arguments as mxfa_varlen_fwd and
+ * mxfa_bwd (lse [H][total_q]). */
+mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                            const mxfa_mx* dout_mx, const void* o, const void* dout, const float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, int64_t total_q, int64_t total_k,
+                            int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
+                            int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
+                            void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
+
+/* mxfa_rmsnorm_quant -- fused RMSNorm + MX quantization in one pass
+ * ([TMEM] "fused producers", [ITEMS] item 7: FP8 out with dual scale layouts).
+ *  x      bf16 [T][C], C in {256, 512, 1024, 2048}
+ *  gamma  fp32 [C]
+ *  y = (x * r) * gamma, r = 1/sqrt(mean(x^2) + eps), fp32, each operation
+ *  correctly rounded; the sum of squares runs in a fixed order: lane l of a
+ *  warp owns columns 8l + 256k + j, adds their squares k-outer, j-inner, then
+ *  a butterfly over lane distances 16, 8, 4, 2, 1.
+ *  seg_len  column and square blocks are anchored every seg_len rows
+ *           (a multiple of 32; a multiple of 128 dividing T when packed
+ *           scales are requested)
+ *  H        head split of C for the packed layouts (C = H * 128)
+ *  row/col/sq  outputs for 1x32, 32x1 and 32x32 blocks; each may be NULL
+ *           (at least one must be given). */
+mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int64_t C, float eps,
+                               int seg_len, int H, const mxfa_mx_out* row, const mxfa_mx_out* col,
+                               const mxfa_mx_out* sq, mxfa_stream_t stream);
+
+/* Synchronise `stream`, then return and clear the device status words:
+ * MXFA_OK, MXFA_ERR_TIMEOUT or MXFA_ERR_DEVICE_INDEX (bit flags also in
+ * *flags when flags is not NULL: 1 timeout, 2 index). */
+mxfa_status mxfa_get_device_status(mxfa_stream_t stream, unsigned* flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXFA_H */

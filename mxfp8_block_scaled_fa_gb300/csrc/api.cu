@@ -1,0 +1,355 @@
+// api.cu -- the C ABI (include/mxfa.h): argument checks, TMA descriptors and
+// kernel launches.  No allocation, no synchronisation on the hot path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mxfa.h"
+#include "mxfa_internal.h"
+
+using namespace mxfa;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// u8 tensor [tokens][H][128] as a 3-D map, box 128 x 1 x box_rows, 128B swizzle.
+bool make_map_u8(CUtensorMap* m, const void* ptr, int64_t tokens, int H, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, cuuint64_t(H), cuuint64_t(tokens)};
+  cuuint64_t strides[2] = {128, cuuint64_t(H) * 128};
+  cuuint32_t box[3] = {128, 1, cuuint32_t(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mxfa_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MXFA_OK;
+  if (e == cudaErrorInvalidValue) return MXFA_ERR_INVALID_ARG;
+  return MXFA_ERR_CUDA;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shared checks of a sequence description.
+mxfa_status check_seqs(const int32_t* cu, int nseq, int maxlen, int64_t tokens) {
+  if (nseq <= 0 || maxlen < 0 || tokens < 0) return MXFA_ERR_INVALID_ARG;
+  if (!cu && int64_t(nseq) * maxlen != tokens) return MXFA_ERR_INVALID_ARG;
+  if (tokens >= (int64_t(1) << 31)) return MXFA_ERR_UNSUPPORTED;
+  return MXFA_OK;
+}
+
+mxfa_status check_mx(const mxfa_mx* x) {
+  if (!x || !x->data || !x->sf) return MXFA_ERR_INVALID_ARG;
+  if (!aligned16(x->data) || !aligned16(x->sf)) return MXFA_ERR_MISALIGNED;
+  return MXFA_OK;
+}
+
+mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seqs sq, Seqs sk,
+                       int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
+                       float scale, int causal, void* o, float* lse, bool dense, mxfa_stream_t stream) {
+  mxfa_status s;
+  if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v))) return s;
+  if (!o || !lse || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return MXFA_ERR_INVALID_ARG;
+  if (!aligned16(o)) return MXFA_ERR_MISALIGNED;
+  if (ptq <= 0 || ptk <= 0) return MXFA_ERR_INVALID_ARG;
+  if (total_q == 0) return MXFA_OK;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map_u8(&a.tm_q, q->data, total_q, H, 128) || !make_map_u8(&a.tm_k, k->data, total_k, H, 128) ||
+      !make_map_u8(&a.tm_v, v->data, total_k, H, 128))
+    return MXFA_ERR_CUDA;
+  a.sfq = q->sf;
+  a.sfk = k->sf;
+  a.sfv = v->sf;
+  a.sq = sq;
+  a.sk = sk;
+  a.total_q = total_q;
+  a.ptiles_q = ptq;
+  a.ptiles_k = ptk;
+  a.H = H;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal ? 1 : 0;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.dense_lse = dense ? 1 : 0;
+  a.lse_hstride = dense ? sq.seqlen : total_q;
+  return from_cuda(launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                       const void* o, const void* dout, const float* lse, Seqs sq, Seqs sk,
+                       int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
+                       float scale, int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
+                       void* dv, void* ws, size_t ws_bytes, bool dense, mxfa_stream_t stream) {
+  mxfa_status s;
+  if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v)) || (s = check_mx(dmx))) return s;
+  if (!o || !dout || !lse || !dq || !dk || !dv || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return MXFA_ERR_INVALID_ARG;
+  if (dq_mode != 0 && dq_mode != 1) return MXFA_ERR_INVALID_ARG;
+  if (dq_mode == 1) {
+    int e;
+    if (!(dq_static_scale > 0.0f) || !std::isfinite(dq_static_scale) ||
+        std::frexp(dq_static_scale, &e) != 0.5f)
+      return MXFA_ERR_INVALID_ARG;  // must be a power of two
+  }
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(ws))
+    return MXFA_ERR_MISALIGNED;
+  if (ptq <= 0 || ptk <= 0) return MXFA_ERR_INVALID_ARG;
+  if (!ws) return MXFA_ERR_INVALID_ARG;
+  if (ws_bytes < mxfa_bwd_workspace_size(total_q, H, D, dq_mode)) return MXFA_ERR_WORKSPACE_TOO_SMALL;
+  if (total_q == 0 || total_k == 0) return MXFA_OK;
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map_u8(&a.tm_q, q->data, total_q, H, 64) || !make_map_u8(&a.tm_do, dmx->data, total_q, H, 64) ||
+      !make_map_u8(&a.tm_k, k->data, total_k, H, 128) || !make_map_u8(&a.tm_v, v->data, total_k, H, 128))
+    return MXFA_ERR_CUDA;
+  a.sfq = q->sf;
+  a.sfk = k->sf;
+  a.sfv = v->sf;
+  a.sfdo = dmx->sf;
+  a.o = static_cast<const uint16_t*>(o);
+  a.dout = static_cast<const uint16_t*>(dout);
+  a.lse = lse;
+  a.sq = sq;
+  a.sk = sk;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.ptiles_q = ptq;
+  a.ptiles_k = ptk;
+  a.H = H;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.dq_mode = dq_mode;
+  a.dq_static_scale = dq_mode == 1 ? dq_static_scale : 1.0f;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.delta = static_cast<float*>(ws);
+  const size_t delta_bytes = ((size_t(total_q) * H * 4) + 255) & ~size_t(255);
+  a.dq_acc = static_cast<uint8_t*>(ws) + delta_bytes;
+  a.dense_lse = dense ? 1 : 0;
+  a.lse_hstride = dense ? sq.seqlen : total_q;
+  return from_cuda(launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mxfa_status_string(mxfa_status s) {
+  switch (s) {
+    case MXFA_OK: return "ok";
+    case MXFA_ERR_INVALID_ARG: return "invalid argument";
+    case MXFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MXFA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MXFA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MXFA_ERR_CUDA: return "CUDA error";
+    case MXFA_ERR_TIMEOUT: return "device wait timed out";
+    case MXFA_ERR_DEVICE_INDEX: return "device index check failed";
+  }
+  return "unknown status";
+}
+
+int mxfa_version(void) { return 1; }
+
+int64_t mxfa_packed_tiles(const int32_t* cu, int nseq, int seqlen) {
+  if (nseq < 0) return -1;
+  if (!cu) return seqlen < 0 ? -1 : int64_t(nseq) * ceil_div(seqlen, 128);
+  int64_t t = 0;
+  for (int i = 0; i < nseq; i++) {
+    int64_t len = int64_t(cu[i + 1]) - cu[i];
+    if (len < 0) return -1;
+    t += ceil_div(len, 128);
+  }
+  return t;
+}
+
+size_t mxfa_sf_packed_bytes(mxfa_block blk, int64_t tiles, int H) {
+  if (tiles < 0 || H <= 0) return 0;
+  return size_t(tiles) * size_t(H) * (blk == MXFA_BLK_SQ ? 16u : 512u);
+}
+
+mxfa_status mxfa_quantize(const void* x, int64_t tokens, int H, int D, mxfa_block blk,
+                          const int32_t* cu, int nseq, int max_seqlen, int64_t packed_tiles,
+                          const mxfa_mx_out* out, mxfa_stream_t stream) {
+  if (!x || !out || !out->data || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (blk < MXFA_BLK_ROW || blk > MXFA_BLK_SQ) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  mxfa_status s = check_seqs(cu, nseq, max_seqlen, tokens);
+  if (s) return s;
+  if (!aligned16(x) || !aligned16(out->data)) return MXFA_ERR_MISALIGNED;
+  if (out->sf_packed && packed_tiles <= 0) return MXFA_ERR_INVALID_ARG;
+  QuantArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.tokens = tokens;
+  a.H = H;
+  a.D = D;
+  a.mode = int(blk);
+  a.seq = Seqs{cu, nseq, max_seqlen};
+  a.packed_tiles = packed_tiles;
+  a.data = out->data;
+  a.sf_compact = out->sf_compact;
+  a.sf_packed = out->sf_packed;
+  if (tokens == 0) return MXFA_OK;
+  return from_cuda(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_sf_pack(const uint8_t* sf_compact, int64_t tokens, int H, int D, mxfa_block blk,
+                         const int32_t* cu, int nseq, int max_seqlen, int64_t packed_tiles,
+                         uint8_t* sf_packed, mxfa_stream_t stream) {
+  if (!sf_compact || !sf_packed || H <= 0 || packed_tiles <= 0) return MXFA_ERR_INVALID_ARG;
+  if (blk < MXFA_BLK_ROW || blk > MXFA_BLK_SQ) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  mxfa_status s = check_seqs(cu, nseq, max_seqlen, tokens);
+  if (s) return s;
+  PackArgs a;
+  a.sf_compact = sf_compact;
+  a.tokens = tokens;
+  a.H = H;
+  a.D = D;
+  a.mode = int(blk);
+  a.seq = Seqs{cu, nseq, max_seqlen};
+  a.packed_tiles = packed_tiles;
+  a.sf_packed = sf_packed;
+  if (tokens == 0) return MXFA_OK;
+  return from_cuda(launch_sf_pack(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H, int D,
+                     float softmax_scale, int causal, void* o, float* lse, mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  return fwd_common(q, k, v, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total, pt, pt, H, D,
+                    softmax_scale, causal, o, lse, true, stream);
+}
+
+mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const int32_t* cu_q,
+                            const int32_t* cu_k, int nseq, int max_sq, int max_sk, int64_t total_q,
+                            int64_t total_k, int64_t ptq, int64_t ptk, int H, int D, float softmax_scale,
+                            int causal, void* o, float* lse, mxfa_stream_t stream) {
+  if (!cu_q || !cu_k) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  if (max_sk <= 0) return MXFA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk}, total_q, total_k, ptq,
+                    ptk, H, D, softmax_scale, causal, o, lse, false, stream);
+}
+
+size_t mxfa_bwd_workspace_size(int64_t total_q, int H, int D, int dq_mode) {
+  if (total_q < 0 || H <= 0 || D <= 0) return 0;
+  const size_t delta_bytes = ((size_t(total_q) * H * 4) + 255) & ~size_t(255);
+  return delta_bytes + size_t(total_q) * H * D * (dq_mode == 1 ? 2u : 4u);
+}
+
+mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                     const void* o, const void* dout, const float* lse, int B, int S, int H, int D,
+                     float softmax_scale, int causal, int dq_mode, float dq_static_scale, void* dq,
+                     void* dk, void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total,
+                    pt, pt, H, D, softmax_scale, causal, dq_mode, dq_static_scale, dq, dk, dv, ws,
+                    ws_bytes, true, stream);
+}
+
+mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                            const void* o, const void* dout, const float* lse, const int32_t* cu_q,
+                            const int32_t* cu_k, int nseq, int max_sq, int max_sk, int64_t total_q,
+                            int64_t total_k, int64_t ptq, int64_t ptk, int H, int D, float softmax_scale,
+                            int causal, int dq_mode, float dq_static_scale, void* dq, void* dk, void* dv,
+                            void* ws, size_t ws_bytes, mxfa_stream_t stream) {
+  if (!cu_q || !cu_k) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk},
+                    total_q, total_k, ptq, ptk, H, D, softmax_scale, causal, dq_mode, dq_static_scale,
+                    dq, dk, dv, ws, ws_bytes, false, stream);
+}
+
+mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int64_t C, float eps,
+                               int seg_len, int H, const mxfa_mx_out* row, const mxfa_mx_out* col,
+                               const mxfa_mx_out* sq, mxfa_stream_t stream) {
+  if (!x || !gamma || T < 0 || seg_len <= 0 || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (!row && !col && !sq) return MXFA_ERR_INVALID_ARG;
+  if (C != 256 && C != 512 && C != 1024 && C != 2048) return MXFA_ERR_UNSUPPORTED;
+  if (C % H != 0 || C / H != 128) return MXFA_ERR_UNSUPPORTED;
+  if (seg_len % 32 != 0) return MXFA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MXFA_ERR_INVALID_ARG;
+  const mxfa_mx_out* outs[3] = {row, col, sq};
+  bool packed = false;
+  for (const mxfa_mx_out* m : outs) {
+    if (!m) continue;
+    if (!m->data) return MXFA_ERR_INVALID_ARG;
+    if (!aligned16(m->data)) return MXFA_ERR_MISALIGNED;
+    if (m->sf_packed) packed = true;
+  }
+  if (packed && (seg_len % 128 != 0 || T % seg_len != 0)) return MXFA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(gamma)) return MXFA_ERR_MISALIGNED;
+  RmsArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const uint16_t*>(x);
+  a.gamma = gamma;
+  a.T = T;
+  a.C = int(C);
+  a.eps = eps;
+  a.seg_len = seg_len;
+  a.H = H;
+  a.D = 128;
+  if (row) { a.row_data = row->data; a.row_sfc = row->sf_compact; a.row_sfp = row->sf_packed; }
+  if (col) { a.col_data = col->data; a.col_sfc = col->sf_compact; a.col_sfp = col->sf_packed; }
+  if (sq) { a.sq_data = sq->data; a.sq_sfc = sq->sf_compact; a.sq_sfp = sq->sf_packed; }
+  if (T == 0) return MXFA_OK;
+  return from_cuda(launch_rmsnorm_quant(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_get_device_status(mxfa_stream_t stream, unsigned* flags) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MXFA_ERR_CUDA;
+  unsigned f = read_status_quant(st) | read_status_fwd(st) | read_status_bwd(st);
+  if (flags) *flags = f;
+  if (f & 1u) return MXFA_ERR_TIMEOUT;
+  if (f & 2u) return MXFA_ERR_DEVICE_INDEX;
+  return MXFA_OK;
+}
+
+}  // extern "C"

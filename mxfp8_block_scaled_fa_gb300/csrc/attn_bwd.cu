@@ -1,0 +1,574 @@
+// attn_bwd.cu -- MXFP8 block-scaled FlashAttention backward for sm_103a.
+//
+// What it computes ("MXFP8 FlashAttention-4 Hits 2.85 Petaflops in Meta's
+// Production Training", section "Inside the TMEM Bargain and Zero-Gather
+// Jagged Pipeline"; "Meta's FlashAttention-4 Achieves 2.85 PF/s with MXFP8 on
+// Blackwell GPUs", item 6; "Low-Precision FlashAttention-4 ...", section
+// "Hardware Adaptation for Blackwell" for the recompute):
+//   five GEMMs with recompute -- S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
+//   dK += dS^T Q, dQ^T = K^T dS^T -- on MXFP8 operands.  Q, K and dO carry
+//   32x32 square scales, so one E4M3 payload serves both GEMM orientations;
+//   V carries 1x32 scales along D.  P = exp(S tau - lse) is quantized in 1x32
+//   blocks along queries (the dV contraction), dS = P (dP - Delta) once per
+//   32x32 block with a warp-wide absolute-maximum reduction.  dQ partials are
+//   reduced into a global accumulator in FP32, or in FP16 after multiplying by
+//   a static power-of-two scale.
+//
+// Structure: one CTA = one 128-key tile of one head, looping over 64-query
+// tiles (16 warps, 1 CTA per SM):
+//   warp 0       TMA producer: K, V (+ V scale atom) once; Q_i, dO_i ring
+//   warp 1       TMEM owner + MMA issuer (scale atoms enter TMEM by tcgen05.cp)
+//   warps 2-3    scale-atom builder: per-tile Q / dO atoms in both
+//                orientations from the packed square scales; lse, Delta
+//   warps 4-11   P / dS: thread = key row, warpgroup 0 queries 0-31,
+//                warpgroup 1 queries 32-63 of the tile
+//   warps 12-15  dQ drain: TMEM dQ^T -> shared -> bulk reduce-add
+// TMEM columns: dV [0,128) dK [128,256) S^T [256,320) dP^T [320,384)
+//               dQ^T [384,448) scale slots [448,512).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mx_ptx.cuh"
+#include "mx_seq.cuh"
+#include "mxfa_internal.h"
+
+namespace mxfa {
+
+static __device__ unsigned g_status_bwd;
+
+namespace bwd {
+constexpr int KT = 128;                 // keys per CTA
+constexpr int QT = 64;                  // queries per inner tile
+constexpr int NSQ = 2;                  // Q / dO ring stages
+constexpr int KV_BYTES = KT * 128;      // 16 KB
+constexpr int QD_BYTES = QT * 128;      // 8 KB
+constexpr int PS_BYTES = KT * QT;       // 8 KB (128 rows x 64 B)
+
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KV_BYTES;
+constexpr int OFF_Q = OFF_V + KV_BYTES;                 // NSQ stages
+constexpr int OFF_DO = OFF_Q + NSQ * QD_BYTES;          // NSQ stages
+constexpr int OFF_PT = OFF_DO + NSQ * QD_BYTES;         // 2 buffers, SW64
+constexpr int OFF_DST = OFF_PT + 2 * PS_BYTES;          // 2 buffers, SW64
+constexpr int OFF_DQS = OFF_DST + 2 * PS_BYTES;         // dQ staging, 64 x 512 B
+constexpr int OFF_ATOM = OFF_DQS + QT * 512;
+// scale atoms (512 B each)
+constexpr int A_SFK = 0, A_SFV = 1, A_SFKT = 2;
+constexpr int A_SFQ = 3, A_SFDO = 5, A_SFDOT = 7, A_SFQT = 9;    // x2 (tile parity)
+constexpr int A_SFPT = 11, A_SFDST = 13, A_SFDS = 15;            // x2
+constexpr int NATOM = 17;
+constexpr int OFF_LD = OFF_ATOM + NATOM * 512;          // lse*log2e, Delta: 2 x 2 x 64 floats
+constexpr int OFF_BAR = OFF_LD + 2 * 2 * QT * 4;
+enum {
+  B_KVFULL = 0, B_KCONST, B_QDOFULL, B_QDOEMPTY = B_QDOFULL + NSQ, B_SFINFULL = B_QDOEMPTY + NSQ,
+  B_SFINEMPTY = B_SFINFULL + 2, B_SDPFULL = B_SFINEMPTY + 2, B_SDPFREE, B_PFULL,
+  B_PDSEMPTY = B_PFULL + 2, B_DQFULL = B_PDSEMPTY + 2, B_DQEMPTY, B_KVDONE, B_TEAR, NBAR
+};
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+
+constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384;
+constexpr uint32_t COL_SFK = 448, COL_SFV = 452, COL_SFKT = 456, COL_SFQ = 460, COL_SFDO = 464,
+                   COL_SFPT = 468, COL_SFDOT = 476, COL_SFDST = 484, COL_SFQT = 492,
+                   COL_SFDS = 500;  // the last five are x2 (tile parity), 4 columns each
+constexpr int NTHREADS = 512;
+}  // namespace bwd
+
+// ------------------------------------------------------------ pre / post
+// Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] (fp32 from bf16), one warp per row.
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                      const uint16_t* __restrict__ dout,
+                                                      float* __restrict__ delta, int64_t rows,
+                                                      int H, int64_t total) {
+  const int64_t r = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint2 ov = *reinterpret_cast<const uint2*>(o + r * 128 + lane * 4);
+  const uint2 dv = *reinterpret_cast<const uint2*>(dout + r * 128 + lane * 4);
+  auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+  auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+  float s = lo(ov.x) * lo(dv.x) + hi(ov.x) * hi(dv.x) + lo(ov.y) * lo(dv.y) + hi(ov.y) * hi(dv.y);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  if (lane == 0) {
+    const int64_t t = r / H;
+    const int h = int(r % H);
+    delta[int64_t(h) * total + t] = s;
+  }
+}
+
+// dQ = bf16(acc / static_scale); acc is fp32 (mode 0) or fp16 (mode 1).
+__global__ void __launch_bounds__(256) bwd_post_kernel(const void* __restrict__ acc,
+                                                       uint16_t* __restrict__ dq, int64_t n,
+                                                       int mode, float inv_static) {
+  const int64_t i = (int64_t(blockIdx.x) * 256 + threadIdx.x) * 8;
+  if (i >= n) return;
+  float v[8];
+  if (mode == 0) {
+    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i);
+    const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __half*>(acc) + i);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+      v[2 * j] = f.x * inv_static;
+      v[2 * j + 1] = f.y * inv_static;
+    }
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    w[j] = *reinterpret_cast<uint32_t*>(&p);
+  }
+  *reinterpret_cast<uint4*>(dq + i) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float bex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ bool bwait_raw(uint32_t bar, uint32_t parity) {
+  unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+// Warp-uniform bounded wait (all lanes agree on the outcome).
+__device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, &g_status_bwd));
+}
+// Byte offset of 16-byte chunk c of row r in a 64-byte-row, 64B-swizzled tile.
+__device__ __forceinline__ uint32_t sw64(int r, int c) {
+  return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// ------------------------------------------------------------------ main
+__global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdArgs a) {
+  using namespace bwd;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item: (sequence g, head h, key tile kt)
+  int g, h, kt;
+  if (a.sk.cu == nullptr) {  // dense: heavy (early, causal) key tiles first
+    const int per = a.H * a.sk.nseq;
+    kt = int(blockIdx.x) / per;
+    const int bh = int(blockIdx.x) % per;
+    g = bh / a.H;
+    h = bh % a.H;
+  } else {
+    kt = blockIdx.x;
+    h = blockIdx.y;
+    g = blockIdx.z;
+  }
+  int64_t sq0, sk0;
+  int lq, lk;
+  seq_info(a.sq, g, sq0, lq);
+  seq_info(a.sk, g, sk0, lk);
+  if (kt * KT >= lk) return;
+  const int nq = (lq + QT - 1) / QT;
+  const int first = a.causal ? min(nq, (kt * KT) / QT) : 0;
+  const int ntile = nq - first;
+  const int64_t tq_base = seq_units_before(a.sq, g, 128);
+  const int64_t tk = seq_units_before(a.sk, g, 128) + kt;
+
+  const uint32_t bar0 = base + OFF_BAR;
+  auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  auto ATOM = [&](int i) { return smem + OFF_ATOM + 512 * i; };
+  auto ATOMA = [&](int i) { return base + OFF_ATOM + 512u * uint32_t(i); };
+  float* ld_stage = reinterpret_cast<float*>(smem + OFF_LD);  // [2 tiles][2: lse2, delta][64]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(BAR(B_KVFULL), 1);
+    mbar_init(BAR(B_KCONST), 64);
+    for (int s = 0; s < NSQ; s++) {
+      mbar_init(BAR(B_QDOFULL + s), 1);
+      mbar_init(BAR(B_QDOEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(BAR(B_SFINFULL + b), 64);
+      mbar_init(BAR(B_SFINEMPTY + b), 1);
+      mbar_init(BAR(B_PFULL + b), 256);
+      mbar_init(BAR(B_PDSEMPTY + b), 1);
+    }
+    mbar_init(BAR(B_SDPFULL), 1);
+    mbar_init(BAR(B_SDPFREE), 256);
+    mbar_init(BAR(B_DQFULL), 1);
+    mbar_init(BAR(B_DQEMPTY), 128);
+    mbar_init(BAR(B_KVDONE), 1);
+    mbar_init(BAR(B_TEAR), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool bad = tk >= a.ptiles_k || tq_base + (lq + 127) / 128 > a.ptiles_q;
+  if (bad && tid == 0) {
+    atomicOr(&g_status_bwd, DEV_BAD_INDEX);
+    *abort_flag = 1;
+  }
+  __syncthreads();
+
+  if (bad) {
+    // nothing issued; fall through to teardown
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      tma_prefetch_desc(&a.tm_do);
+      mbar_arrive_expect_tx(BAR(B_KVFULL), 2 * KV_BYTES + 512);
+      const int krow = int(sk0 + int64_t(kt) * KT);
+      tma_load_3d(base + OFF_K, &a.tm_k, BAR(B_KVFULL), 0, h, krow);
+      tma_load_3d(base + OFF_V, &a.tm_v, BAR(B_KVFULL), 0, h, krow);
+      bulk_load(ATOMA(A_SFV), a.sfv + (tk * a.H + h) * 512, 512, BAR(B_KVFULL));
+      int issued = 0;
+      for (int ii = 0; ii < ntile; ii++) {
+        const int s = ii % NSQ, i = first + ii;
+        if (ii >= NSQ && !mbar_wait(BAR(B_QDOEMPTY + s), ((ii / NSQ) - 1) & 1, abort_flag, &g_status_bwd))
+          break;
+        issued = ii + 1;
+        const uint32_t fb = BAR(B_QDOFULL + s);
+        mbar_arrive_expect_tx(fb, 2 * QD_BYTES);
+        const int qrow = int(sq0 + int64_t(i) * QT);
+        tma_load_3d(base + OFF_Q + s * QD_BYTES, &a.tm_q, fb, 0, h, qrow);
+        tma_load_3d(base + OFF_DO + s * QD_BYTES, &a.tm_do, fb, 0, h, qrow);
+      }
+      for (int ii = max(0, issued - NSQ); ii < issued; ii++)
+        bwait_raw(BAR(B_QDOFULL + ii % NSQ), (ii / NSQ) & 1);
+      bwait_raw(BAR(B_KVFULL), 0);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------ scale-atom builder
+    // Atom word w (bytes 4w..4w+3) holds row r = (w & 3) * 32 + (w >> 2),
+    // k-blocks 0..3 in its bytes.  Square scale entry: byte 4 * tb + db.
+    const int t = tid - 64;
+    const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(a.sfk + (tk * a.H + h) * 16));
+    const uint32_t kw[4] = {k4.x, k4.y, k4.z, k4.w};  // kw[tb] = bytes db 0..3
+    auto col_bytes = [](const uint32_t* wv, int db, int tb_lo, int ntb) {
+      uint32_t v = 0x7F7F7F7Fu;
+      for (int j = 0; j < ntb; j++) {
+        const uint32_t byte = (wv[tb_lo + j] >> (8 * db)) & 0xFFu;
+        v = (v & ~(0xFFu << (8 * j))) | (byte << (8 * j));
+      }
+      return v;
+    };
+    for (int w = t; w < 128; w += 64) {
+      reinterpret_cast<uint32_t*>(ATOM(A_SFK))[w] = kw[w & 3];           // rows = keys
+      reinterpret_cast<uint32_t*>(ATOM(A_SFKT))[w] = col_bytes(kw, w & 3, 0, 4);  // rows = d
+    }
+    fence_async_smem();
+    mbar_arrive(BAR(B_KCONST));
+    const float l2e = 1.4426950408889634f;
+    for (int ii = 0; ii < ntile; ii++) {
+      const int i = first + ii, b = ii & 1;
+      if (ii >= 2 && !mbar_wait(BAR(B_SFINEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag, &g_status_bwd))
+        break;
+      const int64_t ent = ((tq_base + i / 2) * a.H + h) * 16;
+      const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + ent));
+      const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + ent));
+      const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+      const int tb0 = (i & 1) * 2;
+      for (int w = t; w < 128; w += 64) {
+        const int rg = w & 3;  // row group = 32-row block of the atom
+        reinterpret_cast<uint32_t*>(ATOM(A_SFQ + b))[w] = rg < 2 ? qw[tb0 + rg] : 0x7F7F7F7Fu;
+        reinterpret_cast<uint32_t*>(ATOM(A_SFDO + b))[w] = rg < 2 ? dw[tb0 + rg] : 0x7F7F7F7Fu;
+        reinterpret_cast<uint32_t*>(ATOM(A_SFQT + b))[w] = col_bytes(qw, rg, tb0, 2);
+        reinterpret_cast<uint32_t*>(ATOM(A_SFDOT + b))[w] = col_bytes(dw, rg, tb0, 2);
+      }
+      {
+        const int c = t;  // query column of the tile
+        const int q = i * QT + c;
+        float l2 = INFINITY, dl = 0.0f;  // queries past the end: P = 2^-inf = 0
+        if (q < lq) {
+          const float lse = a.dense_lse ? a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + q]
+                                        : a.lse[int64_t(h) * a.lse_hstride + sq0 + q];
+          l2 = lse * l2e;
+          dl = a.delta[int64_t(h) * a.total_q + sq0 + q];
+        }
+        ld_stage[(b * 2 + 0) * QT + c] = l2;
+        ld_stage[(b * 2 + 1) * QT + c] = dl;
+      }
+      fence_async_smem();
+      mbar_arrive(BAR(B_SFINFULL + b));
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto cp_sf = [&](uint32_t col, uint32_t saddr) {
+        const uint64_t d = smem_desc(saddr, 128, 128, 0);
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + col), "l"(d) : "memory");
+      };
+      bool ok = mbar_wait(BAR(B_KVFULL), 0, abort_flag, &g_status_bwd) &&
+                mbar_wait(BAR(B_KCONST), 0, abort_flag, &g_status_bwd);
+      tc_fence_after();
+      if (ok) {
+        cp_sf(COL_SFK, ATOMA(A_SFK));
+        cp_sf(COL_SFV, ATOMA(A_SFV));
+        cp_sf(COL_SFKT, ATOMA(A_SFKT));
+      }
+      // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T for local tile jj
+      auto grads = [&](int jj) -> bool {
+        const int s = jj % NSQ, b = jj & 1;
+        if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_bwd)) return false;
+        if (jj >= 1 && !mbar_wait(BAR(B_DQEMPTY), (jj - 1) & 1, abort_flag, &g_status_bwd)) return false;
+        tc_fence_after();
+        cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
+        cp_sf(COL_SFDOT + 4 * b, ATOMA(A_SFDOT + b));
+        cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
+        cp_sf(COL_SFQT + 4 * b, ATOMA(A_SFQT + b));
+        cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
+        const uint32_t pt = base + OFF_PT + b * PS_BYTES, dst = base + OFF_DST + b * PS_BYTES;
+        const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+          const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
+          mma_mxf8_ss(tmem + COL_DV, smem_desc(pt + 32 * k, 16, 512, 4),
+                      smem_desc(dos + 4096 * k, 8192, 1024, 2), idesc_mxf8(128, 128, 0, 1, k, k),
+                      tmem + COL_SFPT + 4 * b, tmem + COL_SFDOT + 4 * b, acc);
+          mma_mxf8_ss(tmem + COL_DK, smem_desc(dst + 32 * k, 16, 512, 4),
+                      smem_desc(qs + 4096 * k, 8192, 1024, 2), idesc_mxf8(128, 128, 0, 1, k, k),
+                      tmem + COL_SFDST + 4 * b, tmem + COL_SFQT + 4 * b, acc);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss(tmem + COL_DQ, smem_desc(base + OFF_K + 4096 * k, 8192, 1024, 2),
+                      smem_desc(dst + 2048 * k, 8192, 512, 4), idesc_mxf8(128, 64, 1, 1, k, k),
+                      tmem + COL_SFKT, tmem + COL_SFDS + 4 * b, k > 0 ? 1u : 0u);
+        tc_commit(BAR(B_QDOEMPTY + s));
+        tc_commit(BAR(B_SFINEMPTY + b));
+        tc_commit(BAR(B_PDSEMPTY + b));
+        tc_commit(BAR(B_DQFULL));
+        return true;
+      };
+      for (int ii = 0; ok && ii < ntile; ii++) {
+        const int s = ii % NSQ, b = ii & 1;
+        if (!mbar_wait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag, &g_status_bwd) ||
+            !mbar_wait(BAR(B_SFINFULL + b), (ii >> 1) & 1, abort_flag, &g_status_bwd) ||
+            (ii >= 1 && !mbar_wait(BAR(B_SDPFREE), (ii - 1) & 1, abort_flag, &g_status_bwd))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        cp_sf(COL_SFQ, ATOMA(A_SFQ + b));
+        cp_sf(COL_SFDO, ATOMA(A_SFDO + b));
+        const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss(tmem + COL_S, smem_desc(base + OFF_K + 32 * k, 16, 1024, 2),
+                      smem_desc(qs + 32 * k, 16, 1024, 2), idesc_mxf8(128, 64, 0, 0, k, k),
+                      tmem + COL_SFK, tmem + COL_SFQ, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss(tmem + COL_DP, smem_desc(base + OFF_V + 32 * k, 16, 1024, 2),
+                      smem_desc(dos + 32 * k, 16, 1024, 2), idesc_mxf8(128, 64, 0, 0, k, k),
+                      tmem + COL_SFV, tmem + COL_SFDO, k > 0 ? 1u : 0u);
+        tc_commit(BAR(B_SDPFULL));
+        if (ii >= 1 && !grads(ii - 1)) { ok = false; break; }
+      }
+      if (ok && ntile > 0) grads(ntile - 1);
+      tc_commit(BAR(B_KVDONE));
+      tc_commit(BAR(B_TEAR));
+      bwait_raw(BAR(B_TEAR), 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ P / dS
+    const int hq = (warp - 4) >> 2;            // query half of the tile
+    const int r = (warp & 3) * 32 + lane;      // key row = TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const int kpos = kt * KT + r;
+    const bool kvalid = kpos < lk;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    bool ok = true;
+    for (int ii = 0; ii < ntile; ii++) {
+      const int i = first + ii, b = ii & 1;
+      if (!wwait(BAR(B_SDPFULL), ii & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float sv[32], dp[32];
+      tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
+      tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(BAR(B_SDPFREE));
+      if (!wwait(BAR(B_SFINFULL + b), (ii >> 1) & 1, abort_flag)) { ok = false; break; }
+      const float* l2 = ld_stage + (b * 2 + 0) * QT + 32 * hq;
+      const float* dl = ld_stage + (b * 2 + 1) * QT + 32 * hq;
+      const int q0 = i * QT + 32 * hq;
+      float pmax = 0.0f, dsmax = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const bool vis = kvalid && !(a.causal && kpos > q0 + c);
+        // P = 2^(fl(S * scale * log2 e) - lse * log2 e), dS = P * (dP - Delta)
+        const float p = vis ? bex2(__fsub_rn(__fmul_rn(sv[c], sl2), l2[c])) : 0.0f;
+        const float ds = __fmul_rn(p, __fsub_rn(dp[c], dl[c]));
+        sv[c] = p;
+        dp[c] = ds;
+        pmax = fmaxf(pmax, p);
+        dsmax = fmaxf(dsmax, fabsf(ds));
+      }
+      // P^T: one 1x32 block along queries per thread; dS: one 32x32 block per
+      // warp, its maximum by a warp-wide absolute-maximum reduction
+      float wmax;
+      asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(dsmax));
+      const uint32_t sp = e8m0_from_amax(pmax), sd = e8m0_from_amax(wmax);
+      const float ip = e8m0_inv_scale(sp), id = e8m0_inv_scale(sd);
+      uint32_t pw[8], dw[8];
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        pw[c] = pack4_e4m3(sv[4 * c] * ip, sv[4 * c + 1] * ip, sv[4 * c + 2] * ip, sv[4 * c + 3] * ip);
+        dw[c] = pack4_e4m3(dp[4 * c] * id, dp[4 * c + 1] * id, dp[4 * c + 2] * id, dp[4 * c + 3] * id);
+      }
+      if (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      uint8_t* pt = smem + OFF_PT + b * PS_BYTES;
+      uint8_t* dst = smem + OFF_DST + b * PS_BYTES;
+      *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+      *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+      *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq + 1)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+      const int aoff = (r & 31) * 16 + (r >> 5) * 4 + hq;      // row = key, k-block = query half
+      ATOM(A_SFPT + b)[aoff] = uint8_t(sp);
+      ATOM(A_SFDST + b)[aoff] = uint8_t(sd);
+      ATOM(A_SFDS + b)[lane * 16 + hq * 4 + (warp & 3)] = uint8_t(sd);  // row = query, k-block = key block
+      fence_async_smem();
+      mbar_arrive(BAR(B_PFULL + b));
+    }
+    // ---- dV (query half 0) and dK (query half 1): TMEM -> bf16
+    if (__all_sync(0xFFFFFFFFu, ok) && wwait(BAR(B_KVDONE), 0, abort_flag)) {
+      tc_fence_after();
+      const uint32_t col = hq == 0 ? COL_DV : COL_DK;
+      const float mult = hq == 0 ? 1.0f : a.scale;
+      uint16_t* dst = (hq == 0 ? a.dv : a.dk) + ((sk0 + kpos) * a.H + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + col + 32 * c, v);
+        tmem_wait_ld();
+        if (kvalid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; v4++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const float x0 = ntile > 0 ? __uint_as_float(v[8 * v4 + 2 * e]) * mult : 0.0f;
+              const float x1 = ntile > 0 ? __uint_as_float(v[8 * v4 + 2 * e + 1]) * mult : 0.0f;
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(x0, x1);
+              w[e] = *reinterpret_cast<uint32_t*>(&p2);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v4) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ drain
+    const int d = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const bool leader = tid == 12 * 32;
+    const int esz = a.dq_mode == 1 ? 2 : 4;
+    const uint32_t rowb = 128u * esz;
+    const float mult = a.scale * a.dq_static_scale;
+    uint8_t* stg = smem + OFF_DQS;
+    volatile int* vote = reinterpret_cast<volatile int*>(smem + OFF_MISC + 16);  // 4 ints
+    for (int ii = 0; ii < ntile; ii++) {
+      const int i = first + ii;
+      // all four warps reach the named barrier whatever their wait returned,
+      // then leave together if any of them gave up
+      const bool okw = wwait(BAR(B_DQFULL), ii & 1, abort_flag);
+      if (lane == 0) vote[warp & 3] = okw ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!(vote[0] && vote[1] && vote[2] && vote[3])) break;
+      tc_fence_after();
+      float v[64];
+      tmem_ld32(tmem + lane_base + COL_DQ, reinterpret_cast<uint32_t*>(v));
+      tmem_ld32(tmem + lane_base + COL_DQ + 32, reinterpret_cast<uint32_t*>(v) + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(BAR(B_DQEMPTY));
+      if (leader) bulk_wait_read0();  // previous reductions finished reading the staging rows
+      named_bar_sync(1, 128);
+      if (esz == 4) {
+#pragma unroll
+        for (int q = 0; q < 64; q++) reinterpret_cast<float*>(stg + q * rowb)[d] = v[q] * mult;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; q++) reinterpret_cast<__half*>(stg + q * rowb)[d] = __float2half_rn(v[q] * mult);
+      }
+      fence_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+        for (int q = 0; q < 64; q++) {
+          const int qq = i * QT + q;
+          if (qq >= lq) break;
+          uint8_t* gdst = static_cast<uint8_t*>(a.dq_acc) + ((sq0 + qq) * a.H + h) * rowb;
+          if (esz == 4)
+            bulk_reduce_add_f32(gdst, base + OFF_DQS + q * rowb, rowb);
+          else
+            bulk_reduce_add_f16(gdst, base + OFF_DQS + q * rowb, rowb);
+        }
+        bulk_commit();
+      }
+    }
+    if (leader) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bwd::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t rows = a.total_q * a.H;
+  const size_t esz = a.dq_mode == 1 ? 2 : 4;
+  cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, size_t(rows) * 128 * esz, st);
+  if (e != cudaSuccess) return e;
+  bwd_pre_kernel<<<unsigned((rows + 7) / 8), 256, 0, st>>>(a.o, a.dout, a.delta, rows, a.H, a.total_q);
+  dim3 grid;
+  if (a.sk.cu == nullptr) {
+    const int nkt = (a.sk.seqlen + bwd::KT - 1) / bwd::KT;
+    grid = dim3(unsigned(nkt * a.H * a.sk.nseq), 1, 1);
+  } else {
+    grid = dim3(unsigned((a.sk.seqlen + bwd::KT - 1) / bwd::KT), unsigned(a.H), unsigned(a.sk.nseq));
+  }
+  if (grid.x > 0 && grid.y > 0 && grid.z > 0)
+    attn_bwd_kernel<<<grid, bwd::NTHREADS, bwd::SMEM_BYTES, st>>>(a);
+  const int64_t n = rows * 128;
+  bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode,
+                                                               1.0f / a.dq_static_scale);
+  return cudaPeekAtLastError();
+}
+
+unsigned read_status_bwd(cudaStream_t st) {
+  unsigned v = 0, z = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_status_bwd, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+  cudaMemcpyToSymbolAsync(g_status_bwd, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+  cudaStreamSynchronize(st);
+  return v;
+}
+
+}  // namespace mxfa

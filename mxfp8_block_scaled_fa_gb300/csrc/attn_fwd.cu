@@ -1,0 +1,394 @@
+// attn_fwd.cu -- MXFP8 block-scaled FlashAttention forward for sm_103a.
+//
+// What it computes ("Meta's MXFP8 FlashAttention-4 kernel, tackling TMEM
+// scale-factor constraints, hits up to 1.6x over BF16", paragraphs 1-2;
+// "MXFP8 FlashAttention-4 Hits 2.85 Petaflops in Meta's Production Training",
+// section "Inside the TMEM Bargain and Zero-Gather Jagged Pipeline"):
+//   S = Q K^T as a block-scaled MMA (E4M3 x E4M3, E8M0 scales per 32 of D),
+//   FP32 online softmax in base 2, P converted to MXFP8 in registers in
+//   32-key blocks whose scale comes from the block maxima of the scores
+//   (bit extraction, no log or division), O += P V as a block-scaled MMA with
+//   P read from tensor memory and V scaled per 32 keys.
+//
+// Structure (one CTA = one 128-query tile of one head, 1 CTA per SM):
+//   warp 0      TMA producer: Q once; K, V tiles + their scale atoms into a
+//               3-stage shared-memory ring (mbarrier complete_tx)
+//   warp 1      TMEM owner and MMA issuer: scale atoms enter TMEM through
+//               tcgen05.cp (in issue order with the MMAs); S(j) into one of
+//               two TMEM S buffers, then O += P(j-1) V(j-1)
+//   warps 4..7  softmax: thread i owns query row i (TMEM lane i); writes
+//               P(j) over the first 32 columns of S(j) and its scales to a
+//               shared atom; rescales O in TMEM when the running max moves;
+//               final O / l and LSE
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,384) scales [384,..).
+// The running max moves only when it grows by more than kRescaleThr (log2
+// units); P~ then stays below 2^kRescaleThr, which the E8M0 block scale
+// absorbs, and O and l carry the stale max exactly.
+#include <cuda_bf16.h>
+
+#include "mx_ptx.cuh"
+#include "mx_seq.cuh"
+#include "mxfa_internal.h"
+
+namespace mxfa {
+
+static __device__ unsigned g_status_fwd;
+
+namespace fwd {
+constexpr int NS = 3;  // K/V pipeline stages
+constexpr int TILE = 128;
+constexpr int TILE_BYTES = TILE * 128;  // 128 rows x 128 E4M3
+constexpr float kRescaleThr = 8.0f;
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE_BYTES;
+constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+constexpr int OFF_SF = OFF_V + NS * TILE_BYTES;
+constexpr int OFF_SFQ = OFF_SF;
+constexpr int OFF_SFK = OFF_SFQ + 512;
+constexpr int OFF_SFV = OFF_SFK + NS * 512;
+constexpr int OFF_SFP = OFF_SFV + NS * 512;
+constexpr int OFF_BAR = OFF_SFP + 2 * 512;
+// barriers: q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done, teardown
+constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+
+constexpr uint32_t COL_S0 = 0, COL_O = 256, COL_SFQ = 384, COL_SFK = 388, COL_SFV = 396,
+                   COL_SFP = 404;
+constexpr int NTHREADS = 256;
+}  // namespace fwd
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool mbar_wait_raw(uint32_t bar, uint32_t parity) {
+  unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using namespace fwd;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item
+  int g, h, qt;
+  if (a.sq.cu == nullptr) {  // dense: heavy (late) query tiles first
+    const int nqt = (a.sq.seqlen + TILE - 1) / TILE;
+    const int per = a.H * a.sq.nseq;
+    qt = nqt - 1 - int(blockIdx.x) / per;
+    const int bh = int(blockIdx.x) % per;
+    g = bh / a.H;
+    h = bh % a.H;
+  } else {
+    qt = blockIdx.x;
+    h = blockIdx.y;
+    g = blockIdx.z;
+  }
+  int64_t sq0, sk0;
+  int lq, lk;
+  seq_info(a.sq, g, sq0, lq);
+  seq_info(a.sk, g, sk0, lk);
+  if (qt * TILE >= lq) return;  // empty tile of a short sequence (before any setup)
+  int nkv = (lk + TILE - 1) / TILE;
+  if (a.causal) nkv = min(nkv, qt + 1);
+  const int64_t tq_g = seq_units_before(a.sq, g, TILE) + qt;
+  const int64_t tk_g0 = seq_units_before(a.sk, g, TILE);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  const uint32_t bar0 = smem_u32(bars);
+  auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  const int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS,
+            B_PFULL = 3 + 2 * NS, B_ODONE = 5 + 2 * NS, B_TEAR = 6 + 2 * NS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(BAR(B_QFULL), 1);
+    for (int s = 0; s < NS; s++) {
+      mbar_init(BAR(B_KVFULL + s), 1);
+      mbar_init(BAR(B_KVEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(BAR(B_SFULL + b), 1);
+      mbar_init(BAR(B_PFULL + b), 128);
+    }
+    mbar_init(BAR(B_ODONE), 1);
+    mbar_init(BAR(B_TEAR), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool bad_tiles = (tq_g >= a.ptiles_q) || (tk_g0 + nkv > a.ptiles_k);
+  if (bad_tiles && tid == 0) {
+    atomicOr(&g_status_fwd, DEV_BAD_INDEX);
+    *abort_flag = 1;
+  }
+  __syncthreads();
+
+  if (warp == 0 && !bad_tiles) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      mbar_arrive_expect_tx(BAR(B_QFULL), TILE_BYTES + 512);
+      tma_load_3d(base + OFF_Q, &a.tm_q, BAR(B_QFULL), 0, h, int(sq0 + int64_t(qt) * TILE));
+      bulk_load(base + OFF_SFQ, a.sfq + (tq_g * a.H + h) * 512, 512, BAR(B_QFULL));
+      int issued = 0;
+      for (int j = 0; j < nkv; j++) {
+        const int s = j % NS, u = j / NS;
+        if (j >= NS && !mbar_wait(BAR(B_KVEMPTY + s), (u - 1) & 1, abort_flag, &g_status_fwd)) break;
+        issued = j + 1;
+        const uint32_t fb = BAR(B_KVFULL + s);
+        mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 1024);
+        const int krow = int(sk0 + int64_t(j) * TILE);
+        tma_load_3d(base + OFF_K + s * TILE_BYTES, &a.tm_k, fb, 0, h, krow);
+        tma_load_3d(base + OFF_V + s * TILE_BYTES, &a.tm_v, fb, 0, h, krow);
+        const int64_t atom = ((tk_g0 + j) * a.H + h) * 512;
+        bulk_load(base + OFF_SFK + s * 512, a.sfk + atom, 512, fb);
+        bulk_load(base + OFF_SFV + s * 512, a.sfv + atom, 512, fb);
+      }
+      // every issued copy has landed before the CTA may exit
+      for (int j = max(0, issued - NS); j < issued; j++) mbar_wait_raw(BAR(B_KVFULL + j % NS), (j / NS) & 1);
+      mbar_wait_raw(BAR(B_QFULL), 0);
+    }
+  } else if (warp == 1 && !bad_tiles) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS[4] = {idesc_mxf8(128, 128, 0, 0, 0, 0), idesc_mxf8(128, 128, 0, 0, 1, 1),
+                               idesc_mxf8(128, 128, 0, 0, 2, 2), idesc_mxf8(128, 128, 0, 0, 3, 3)};
+      const uint32_t idP[4] = {idesc_mxf8(128, 128, 0, 1, 0, 0), idesc_mxf8(128, 128, 0, 1, 1, 1),
+                               idesc_mxf8(128, 128, 0, 1, 2, 2), idesc_mxf8(128, 128, 0, 1, 3, 3)};
+      bool ok = mbar_wait(BAR(B_QFULL), 0, abort_flag, &g_status_fwd);
+      tc_fence_after();
+      auto cp_sf = [&](uint32_t col, uint32_t saddr) {
+        const uint64_t d = smem_desc(saddr, 128, 128, 0);
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + col), "l"(d) : "memory");
+      };
+      auto issue_pv = [&](int jj) -> bool {
+        const int s = jj % NS, b = jj & 1;
+        if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_fwd)) return false;
+        tc_fence_after();
+        cp_sf(COL_SFP + 4 * b, base + OFF_SFP + b * 512);
+        cp_sf(COL_SFV + 4 * b, base + OFF_SFV + s * 512);
+        const uint32_t vb = base + OFF_V + s * TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ts(tmem + COL_O, tmem + COL_S0 + 128 * b + 8 * k,
+                      smem_desc(vb + 4096 * k, 8192, 1024, 2), idP[k], tmem + COL_SFP + 4 * b,
+                      tmem + COL_SFV + 4 * b, (jj > 0 || k > 0) ? 1u : 0u);
+        tc_commit(BAR(B_KVEMPTY + s));
+        tc_commit(BAR(B_ODONE));
+        return true;
+      };
+      if (ok) cp_sf(COL_SFQ, base + OFF_SFQ);
+      for (int j = 0; ok && j < nkv; j++) {
+        const int s = j % NS, b = j & 1;
+        if (!mbar_wait(BAR(B_KVFULL + s), (j / NS) & 1, abort_flag, &g_status_fwd)) { ok = false; break; }
+        tc_fence_after();
+        cp_sf(COL_SFK + 4 * b, base + OFF_SFK + s * 512);
+        const uint32_t kb = base + OFF_K + s * TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss(tmem + COL_S0 + 128 * b, smem_desc(base + OFF_Q + 32 * k, 16, 1024, 2),
+                      smem_desc(kb + 32 * k, 16, 1024, 2), idS[k], tmem + COL_SFQ,
+                      tmem + COL_SFK + 4 * b, k > 0 ? 1u : 0u);
+        tc_commit(BAR(B_SFULL + b));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && nkv > 0) issue_pv(nkv - 1);
+      // all MMAs of this CTA retired before TMEM is released
+      tc_commit(BAR(B_TEAR));
+      mbar_wait_raw(BAR(B_TEAR), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int row = tid - 128;          // query row in the tile = TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const int qpos = qt * TILE + row;   // position in the sequence
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkv; j++) {
+      const int b = j & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + b), (j >> 1) & 1, abort_flag, &g_status_fwd))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+        for (int c = 0; c < 4; c++) tmem_ld32(tmem + lane_base + COL_S0 + 128 * b + 32 * c, su + 32 * c);
+        tmem_wait_ld();
+      }
+      const int kbase = j * TILE;
+      const bool need_mask = (kbase + TILE > lk) || (a.causal && kbase + TILE - 1 > qpos);
+      const int klim = a.causal ? min(lk, qpos + 1) : lk;  // keys < klim are visible
+#pragma unroll
+      for (int i = 0; i < 128; i++) {
+        s[i] = __fmul_rn(s[i], sl2);
+        if (need_mask && kbase + i >= klim) s[i] = -INFINITY;
+      }
+      float bm[4];
+#pragma unroll
+      for (int kb = 0; kb < 4; kb++) {
+        float x = s[32 * kb];
+#pragma unroll
+        for (int i = 1; i < 32; i += 2) {
+          float y;
+          if (i + 1 < 32) {
+            asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(x), "f"(s[32 * kb + i]), "f"(s[32 * kb + i + 1]));
+          } else {
+            y = fmaxf(x, s[32 * kb + i]);
+          }
+          x = y;
+        }
+        bm[kb] = x;
+      }
+      const float mt = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+      const float mn = fmaxf(m, mt);
+      const float mu = (m == -INFINITY || __fsub_rn(mn, m) > kRescaleThr) ? mn : m;
+      const float mref = mu == -INFINITY ? 0.0f : mu;
+      const float alpha = ex2(__fsub_rn(m, mref));
+      const bool rescale = (m != -INFINITY) && (mu > m);
+      float rs = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 128; i++) {
+        s[i] = ex2(__fsub_rn(s[i], mref));
+        rs += s[i];
+      }
+      l = l * alpha + rs;
+      // P -> E4M3 with one E8M0 scale per 32 keys; the block maximum of P is
+      // 2^(block max of s' - m), so no second pass over the elements.
+      uint32_t pw[32];
+      uint32_t sfw = 0;
+#pragma unroll
+      for (int kb = 0; kb < 4; kb++) {
+        const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(bm[kb], mref)));
+        sfw |= sc << (8 * kb);
+        const float inv = e8m0_inv_scale(sc);
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const float* p = s + 32 * kb + 4 * c;
+          pw[8 * kb + c] = pack4_e4m3(p[0] * inv, p[1] * inv, p[2] * inv, p[3] * inv);
+        }
+      }
+      // O must hold PV(j-1) before it is rescaled and before PV(j) is issued
+      if (j >= 1 &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (j - 1) & 1, abort_flag, &g_status_fwd))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xFFFFFFFFu, rescale)) {
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + COL_O + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(tmem + lane_base + COL_O + 32 * c, o);
+          tmem_st16(tmem + lane_base + COL_O + 32 * c + 16, o + 16);
+        }
+      }
+      tmem_st16(tmem + lane_base + COL_S0 + 128 * b, pw);
+      tmem_st16(tmem + lane_base + COL_S0 + 128 * b + 16, pw + 16);
+      *reinterpret_cast<uint32_t*>(smem + OFF_SFP + b * 512 + (row & 31) * 16 + (row >> 5) * 4) = sfw;
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(BAR(B_PFULL + b));
+      m = mu;
+    }
+    // ---- epilogue: O / l -> bf16, LSE
+    if (ok && nkv > 0 &&
+        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (nkv - 1) & 1, abort_flag, &g_status_fwd))) {
+      tc_fence_after();
+      const bool valid = qpos < lq;
+      const float rl = 1.0f / l;
+      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + COL_O + 32 * c, o);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; v4++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[8 * v4 + 2 * e]) * rl,
+                                                        __uint_as_float(o[8 * v4 + 2 * e + 1]) * rl);
+              w[e] = *reinterpret_cast<uint32_t*>(&p2);
+            }
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      if (valid) {
+        const float lse = (m + log2f(l)) * 0.69314718055994530942f;
+        if (a.dense_lse)
+          a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + qpos] = lse;
+        else
+          a.lse[int64_t(h) * a.lse_hstride + sq0 + qpos] = lse;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         fwd::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid;
+  if (a.sq.cu == nullptr) {
+    const int nqt = (a.sq.seqlen + fwd::TILE - 1) / fwd::TILE;
+    grid = dim3(unsigned(nqt * a.H * a.sq.nseq), 1, 1);
+  } else {
+    grid = dim3(unsigned((a.sq.seqlen + fwd::TILE - 1) / fwd::TILE), unsigned(a.H), unsigned(a.sq.nseq));
+  }
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+  attn_fwd_kernel<<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
+  return cudaPeekAtLastError();
+}
+
+unsigned read_status_fwd(cudaStream_t st) {
+  unsigned v = 0, z = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_status_fwd, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+  cudaMemcpyToSymbolAsync(g_status_fwd, &z, sizeof(z), 0, cudaMemcpyHostToDevice, st);
+  cudaStreamSynchronize(st);
+  return v;
+}
+
+}  // namespace mxfa

@@ -1,0 +1,104 @@
+// mxfa_internal.h -- host-side declarations shared by the C-ABI layer and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mxfa {
+
+// Sequence geometry.  When cu == nullptr every sequence has length `seqlen`
+// and sequence g starts at token g * seqlen.
+struct Seqs {
+  const int32_t* cu;  // device, nseq + 1 entries (nullable)
+  int nseq;
+  int seqlen;   // uniform length (cu == nullptr) or maximum length
+};
+
+struct QuantArgs {
+  const uint16_t* x;  // bf16 [tokens][H*D]
+  int64_t tokens;
+  int H, D;
+  int mode;  // 0 ROW, 1 COL, 2 SQ
+  Seqs seq;
+  int64_t packed_tiles;
+  uint8_t* data;
+  uint8_t* sf_compact;  // nullable
+  uint8_t* sf_packed;   // nullable
+};
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
+
+struct PackArgs {
+  const uint8_t* sf_compact;
+  int64_t tokens;
+  int H, D;
+  int mode;
+  Seqs seq;
+  int64_t packed_tiles;
+  uint8_t* sf_packed;
+};
+cudaError_t launch_sf_pack(const PackArgs& a, cudaStream_t s);
+
+struct RmsArgs {
+  const uint16_t* x;
+  const float* gamma;
+  int64_t T;
+  int C;
+  float eps;
+  int seg_len;
+  int H, D;  // head split of C used by the packed layouts (C = H * D)
+  uint8_t *row_data, *row_sfc, *row_sfp;
+  uint8_t *col_data, *col_sfc, *col_sfp;
+  uint8_t *sq_data, *sq_sfc, *sq_sfp;
+};
+cudaError_t launch_rmsnorm_quant(const RmsArgs& a, cudaStream_t s);
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // u8 [tokens][H][128], box 128 x 1 x 128, 128B swizzle
+  const uint8_t* sfq;  // packed ROW atoms
+  const uint8_t* sfk;  // packed ROW atoms
+  const uint8_t* sfv;  // packed COL atoms
+  Seqs sq, sk;
+  int64_t total_q;
+  int64_t ptiles_q, ptiles_k;  // packed tile counts (bounds of sfq / sfk, sfv)
+  int H;
+  float scale_log2;  // softmax scale * log2(e)
+  int causal;
+  uint16_t* o;       // bf16 [tokens][H][128]
+  float* lse;
+  int64_t lse_hstride;  // dense: S, varlen: total_q
+  int dense_lse;        // 1: lse[(b*H + h) * S + s]; 0: lse[h * total_q + token]
+};
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // u8 payloads; q/do boxes 128 x 1 x 64
+  const uint8_t* sfq;   // packed SQ (16 B per tile and head)
+  const uint8_t* sfk;   // packed SQ
+  const uint8_t* sfv;   // packed ROW atoms
+  const uint8_t* sfdo;  // packed SQ
+  const uint16_t* o;    // bf16
+  const uint16_t* dout; // bf16
+  const float* lse;
+  Seqs sq, sk;
+  int64_t total_q, total_k;
+  int64_t ptiles_q, ptiles_k;
+  int H;
+  float scale;        // softmax scale
+  int causal;
+  int dq_mode;        // 0 fp32 accumulation, 1 fp16 with static scale
+  float dq_static_scale;
+  uint16_t *dq, *dk, *dv;  // bf16 outputs
+  float* delta;            // workspace [H][total_q]
+  void* dq_acc;            // workspace [total_q][H][128] fp32 or fp16
+  int64_t lse_hstride;
+  int dense_lse;
+};
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+
+// Read (and clear) the device status words of every kernel module.
+unsigned read_status_quant(cudaStream_t s);
+unsigned read_status_fwd(cudaStream_t s);
+unsigned read_status_bwd(cudaStream_t s);
+
+}  // namespace mxfa

@@ -1,0 +1,321 @@
+"""Thin ctypes binding over libmxfa.so (include/mxfa.h).
+
+The functions named ``mxfa_*`` mirror the C entry points one to one and only
+marshal arguments (torch CUDA tensors -> device pointers, the current torch
+stream -> ``cudaStream_t``).  The helpers below them (``quantize``,
+``attention_fwd`` ...) allocate outputs with torch and call those entry points;
+every arithmetic step runs in the library's CUDA kernels.  Nothing here falls
+back to the CPU: a missing library or a CUDA-less process raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+ROW, COL, SQ = 0, 1, 2
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+           3: "pointer not 16-byte aligned", 4: "workspace too small", 5: "CUDA error",
+           6: "device wait timed out", 7: "device index check failed"}
+
+
+class MxfaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class MxOut(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("sf_compact", ctypes.c_void_p),
+                ("sf_packed", ctypes.c_void_p)]
+
+
+class MxIn(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxfa.so from the package's build folder (raises if absent)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                "libmxfa.so is not built: run mxfp8_block_scaled_fa_gb300.build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        S = ctypes.c_size_t
+        sig = {
+            "mxfa_status_string": (ctypes.c_char_p, [I]),
+            "mxfa_version": (I, []),
+            "mxfa_packed_tiles": (I64, [P, I, I]),
+            "mxfa_sf_packed_bytes": (S, [I, I64, I]),
+            "mxfa_quantize": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
+            "mxfa_sf_pack": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
+            "mxfa_fwd": (I, [P, P, P, I, I, I, I, F, I, P, P, P]),
+            "mxfa_varlen_fwd": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P, P,
+                                    P]),
+            "mxfa_bwd_workspace_size": (S, [I64, I, I, I]),
+            "mxfa_bwd": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P, S, P]),
+            "mxfa_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I,
+                                    F, I, I, F, P, P, P, P, S, P]),
+            "mxfa_rmsnorm_quant": (I, [P, P, I64, I64, F, I, I, P, P, P, P]),
+            "mxfa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise MxfaError(st, where)
+
+
+# ------------------------------------------------------------ C-named calls
+def mxfa_packed_tiles(cu_host: Optional[np.ndarray], nseq: int, seqlen: int) -> int:
+    if cu_host is None:
+        return int(lib().mxfa_packed_tiles(None, nseq, seqlen))
+    cu = np.ascontiguousarray(cu_host, dtype=np.int32)
+    return int(lib().mxfa_packed_tiles(cu.ctypes.data_as(ctypes.c_void_p), nseq, seqlen))
+
+
+def mxfa_quantize(x, tokens, H, D, blk, cu_seqlens, nseq, max_seqlen, packed_tiles, out: MxOut,
+                  stream=None):
+    _check(lib().mxfa_quantize(_p(x), tokens, H, D, blk, _p(cu_seqlens), nseq, max_seqlen,
+                               packed_tiles, ctypes.byref(out), _stream(stream)), "mxfa_quantize")
+
+
+def mxfa_sf_pack(sf_compact, tokens, H, D, blk, cu_seqlens, nseq, max_seqlen, packed_tiles,
+                 sf_packed, stream=None):
+    _check(lib().mxfa_sf_pack(_p(sf_compact), tokens, H, D, blk, _p(cu_seqlens), nseq, max_seqlen,
+                              packed_tiles, _p(sf_packed), _stream(stream)), "mxfa_sf_pack")
+
+
+def mxfa_fwd(q: MxIn, k: MxIn, v: MxIn, B, S, H, D, scale, causal, o, lse, stream=None):
+    _check(lib().mxfa_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), B, S, H, D,
+                          float(scale), int(causal), _p(o), _p(lse), _stream(stream)), "mxfa_fwd")
+
+
+def mxfa_varlen_fwd(q, k, v, cu_q, cu_k, nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H, D,
+                    scale, causal, o, lse, stream=None):
+    _check(lib().mxfa_varlen_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), _p(cu_q),
+                                 _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H, D,
+                                 float(scale), int(causal), _p(o), _p(lse), _stream(stream)),
+           "mxfa_varlen_fwd")
+
+
+def mxfa_bwd_workspace_size(total_q, H, D, dq_mode) -> int:
+    return int(lib().mxfa_bwd_workspace_size(total_q, H, D, dq_mode))
+
+
+def mxfa_bwd(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, dq_mode, dq_static, dq, dk,
+             dv, ws, ws_bytes, stream=None):
+    _check(lib().mxfa_bwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(do_mx),
+                          _p(o), _p(do), _p(lse), B, S, H, D, float(scale), int(causal), dq_mode,
+                          float(dq_static), _p(dq), _p(dk), _p(dv), _p(ws), ws_bytes,
+                          _stream(stream)), "mxfa_bwd")
+
+
+def mxfa_varlen_bwd(q, k, v, do_mx, o, do, lse, cu_q, cu_k, nseq, max_sq, max_sk, total_q,
+                    total_k, ptq, ptk, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
+                    ws_bytes, stream=None):
+    _check(lib().mxfa_varlen_bwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                 ctypes.byref(do_mx), _p(o), _p(do), _p(lse), _p(cu_q), _p(cu_k),
+                                 nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H, D,
+                                 float(scale), int(causal), dq_mode, float(dq_static), _p(dq),
+                                 _p(dk), _p(dv), _p(ws), ws_bytes, _stream(stream)),
+           "mxfa_varlen_bwd")
+
+
+def mxfa_rmsnorm_quant(x, gamma, T, C, eps, seg_len, H, row: Optional[MxOut],
+                       col: Optional[MxOut], sq: Optional[MxOut], stream=None):
+    ref = lambda m: ctypes.byref(m) if m is not None else None
+    _check(lib().mxfa_rmsnorm_quant(_p(x), _p(gamma), T, C, float(eps), seg_len, H, ref(row),
+                                    ref(col), ref(sq), _stream(stream)), "mxfa_rmsnorm_quant")
+
+
+def mxfa_get_device_status(stream=None) -> int:
+    flags = ctypes.c_uint(0)
+    st = lib().mxfa_get_device_status(_stream(stream), ctypes.byref(flags))
+    return st
+
+
+# ----------------------------------------------------------- convenience layer
+@dataclass
+class Seqs:
+    """Host-side description of packed sequences (dense = uniform lengths)."""
+    nseq: int
+    max_len: int
+    total: int
+    cu_host: Optional[np.ndarray]      # int32 [nseq+1] or None (uniform)
+    cu_dev: Optional[torch.Tensor]     # int32 device copy or None
+    ptiles: int                        # sum ceil(len/128)
+    blocks32: int                      # sum ceil(len/32)
+
+    @staticmethod
+    def dense(B: int, S: int) -> "Seqs":
+        return Seqs(B, S, B * S, None, None, B * math.ceil(S / 128), B * math.ceil(S / 32))
+
+    @staticmethod
+    def varlen(lengths: Sequence[int], device) -> "Seqs":
+        lens = np.asarray(lengths, dtype=np.int64)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        cu_dev = torch.from_numpy(cu).to(device)
+        return Seqs(len(lens), int(lens.max()) if len(lens) else 0, int(cu[-1]), cu, cu_dev,
+                    int(np.sum((lens + 127) // 128)), int(np.sum((lens + 31) // 32)))
+
+
+@dataclass
+class Mx:
+    """An MXFP8 tensor produced by the library (payload + scales)."""
+    data: torch.Tensor                 # uint8 [tokens, H, D]
+    sf_compact: Optional[torch.Tensor]
+    sf_packed: Optional[torch.Tensor]
+    blk: int
+
+    def mx_in(self) -> MxIn:
+        return MxIn(self.data.data_ptr(), self.sf_packed.data_ptr())
+
+
+def _sf_shapes(blk, seqs: Seqs, H, D):
+    cols = H * D
+    if blk == ROW:
+        comp = (seqs.total, cols // 32)
+    elif blk == COL:
+        comp = (seqs.blocks32, cols)
+    else:
+        comp = (seqs.blocks32, cols // 32)
+    packed = seqs.ptiles * H * (16 if blk == SQ else 512)
+    return comp, packed
+
+
+def quantize(x: torch.Tensor, blk: int, seqs: Seqs, compact=True, packed=True,
+             stream=None) -> Mx:
+    """bf16 [tokens, H, D] (or [B, S, H, D]) -> Mx via mxfa_quantize."""
+    H, D = x.shape[-2], x.shape[-1]
+    x3 = x.reshape(-1, H, D)
+    dev = x.device
+    data = torch.empty(x3.shape, dtype=torch.uint8, device=dev)
+    comp_shape, pbytes = _sf_shapes(blk, seqs, H, D)
+    sfc = torch.empty(comp_shape, dtype=torch.uint8, device=dev) if compact else None
+    sfp = torch.empty(max(pbytes, 16), dtype=torch.uint8, device=dev) if packed else None
+    out = MxOut(data.data_ptr(), _p(sfc), _p(sfp))
+    mxfa_quantize(x3, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len, seqs.ptiles,
+                  out, stream)
+    return Mx(data, sfc, sfp, blk)
+
+
+def sf_pack(sf_compact: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 128,
+            stream=None) -> torch.Tensor:
+    _, pbytes = _sf_shapes(blk, seqs, H, D)
+    sfp = torch.empty(max(pbytes, 16), dtype=torch.uint8, device=sf_compact.device)
+    mxfa_sf_pack(sf_compact, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len,
+                 seqs.ptiles, sfp, stream)
+    return sfp
+
+
+def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,
+                  causal: bool = False, stream=None, out=None):
+    """Forward on quantized operands -> (O bf16 [tokens, H, D], lse fp32)."""
+    H, D = q.data.shape[-2], q.data.shape[-1]
+    dev = q.data.device
+    o = out[0] if out is not None else torch.empty(q.data.shape, dtype=torch.bfloat16, device=dev)
+    if seqs_q.cu_host is None and seqs_k.cu_host is None:
+        lse = out[1] if out is not None else torch.empty((seqs_q.nseq, H, seqs_q.max_len),
+                                                         dtype=torch.float32, device=dev)
+        mxfa_fwd(q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.nseq, seqs_q.max_len, H, D, scale,
+                 causal, o, lse, stream)
+    else:
+        lse = out[1] if out is not None else torch.empty((H, seqs_q.total), dtype=torch.float32,
+                                                         device=dev)
+        mxfa_varlen_fwd(q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.cu_dev, seqs_k.cu_dev,
+                        seqs_q.nseq, seqs_q.max_len, seqs_k.max_len, seqs_q.total, seqs_k.total,
+                        seqs_q.ptiles, seqs_k.ptiles, H, D, scale, causal, o, lse, stream)
+    return o, lse
+
+
+def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Tensor,
+                  lse: torch.Tensor, seqs_q: Seqs, seqs_k: Seqs, scale: float,
+                  causal: bool = False, dq_mode: int = 0, dq_static: float = 1.0, stream=None,
+                  ws=None, out=None):
+    """Backward on quantized operands -> (dQ, dK, dV) bf16."""
+    H, D = q.data.shape[-2], q.data.shape[-1]
+    dev = q.data.device
+    wsb = mxfa_bwd_workspace_size(seqs_q.total, H, D, dq_mode)
+    if ws is None:
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    if out is None:
+        dq = torch.empty(q.data.shape, dtype=torch.bfloat16, device=dev)
+        dk = torch.empty(k.data.shape, dtype=torch.bfloat16, device=dev)
+        dv = torch.empty(v.data.shape, dtype=torch.bfloat16, device=dev)
+    else:
+        dq, dk, dv = out
+    if seqs_q.cu_host is None and seqs_k.cu_host is None:
+        mxfa_bwd(q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse, seqs_q.nseq,
+                 seqs_q.max_len, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
+                 ws.numel(), stream)
+    else:
+        mxfa_varlen_bwd(q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse,
+                        seqs_q.cu_dev, seqs_k.cu_dev, seqs_q.nseq, seqs_q.max_len,
+                        seqs_k.max_len, seqs_q.total, seqs_k.total, seqs_q.ptiles,
+                        seqs_k.ptiles, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
+                        ws.numel(), stream)
+    return dq, dk, dv
+
+
+def rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float, seg_len: int, H: int,
+                  outputs=("row", "col", "sq"), packed=True, stream=None):
+    """Fused RMSNorm + quantization -> dict name -> Mx (compact + packed scales)."""
+    T, C = x.shape
+    dev = x.device
+    seqs = Seqs.dense(T // seg_len, seg_len) if T % seg_len == 0 else None
+    res, structs = {}, {}
+    for name, blk in (("row", ROW), ("col", COL), ("sq", SQ)):
+        if name not in outputs:
+            continue
+        data = torch.empty((T, C), dtype=torch.uint8, device=dev)
+        nb32 = (T + 31) // 32
+        comp = {ROW: (T, C // 32), COL: (nb32, C), SQ: (nb32, C // 32)}[blk]
+        sfc = torch.empty(comp, dtype=torch.uint8, device=dev)
+        sfp = None
+        if packed:
+            if seqs is None:
+                raise ValueError("packed scales need T to be a multiple of seg_len")
+            sfp = torch.empty(seqs.ptiles * H * (16 if blk == SQ else 512), dtype=torch.uint8,
+                              device=dev)
+        res[name] = Mx(data, sfc, sfp, blk)
+        structs[name] = MxOut(data.data_ptr(), sfc.data_ptr(), _p(sfp))
+    mxfa_rmsnorm_quant(x, gamma, T, C, eps, seg_len, H, structs.get("row"), structs.get("col"),
+                       structs.get("sq"), stream)
+    return res
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the kernels' device status (0 = ok)."""
+    return mxfa_get_device_status(stream)

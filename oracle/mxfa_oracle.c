@@ -238,6 +238,16 @@ static void qdq_block(double* v, int64_t n, int64_t vs) {
     v[i * vs] = mxo_e4m3_decode(mxo_e4m3_encode(ldexp(v[i * vs], -X))) * ldexp(1.0, X);
 }
 
+/* 2^x; with fp32 set, the argument is the fp32 difference of fp32 operands
+ * (callers pass fp32-representable values) and the result is rounded to fp32,
+ * the precision in which the kernel takes its quantization decisions. */
+static double exp2_prec(double x, int fp32) {
+  if (!fp32) return exp2(x);
+  volatile float xf = (float)x;
+  volatile float r = (float)exp2((double)xf);
+  return (double)r;
+}
+
 static double flush_fp32_subnormal(double p) {
   return p < ldexp(1.0, -126) ? 0.0 : p;
 }
@@ -259,21 +269,35 @@ static double flush_fp32_subnormal(double p) {
  *   P~ quantized per 32-key block of the tile (when quant_p), then O += P^ V.
  * End: O /= l;  lse = (m + log2 l) * ln 2 (natural log).
  * causal masks key index > query index within a sequence (equal lengths).
- * lse layout: lse[head][query token]. */
+ * lse layout: lse[head][query token].
+ * score_fp32 = 0 is the fp64 definition.  score_fp32 = 1 takes the values
+ * that decide quantization codes in fp32, the kernel's precision: S rounded
+ * to fp32 (the MMA accumulator), s' = fl(S * fl(scale * log2 e)), the running
+ * maximum test and s' - m in fp32, and P~ rounded to fp32. */
 void mxo_attn_fwd(const double* q, const double* k, const double* v,
                   const int32_t* cu_q, const int32_t* cu_k, int nseq, int H,
                   int D, double scale, int causal, int quant_p, int tile_n,
-                  double lazy_thr, double* o, double* lse, int64_t total_q) {
+                  double lazy_thr, double* o, double* lse, int64_t total_q, int score_fp32) {
   const double log2e = 1.4426950408889634074;
   const double ln2 = 0.69314718055994530942;
-#pragma omp parallel for collapse(2) schedule(dynamic)
-  for (int g = 0; g < nseq; g++) {
-    for (int h = 0; h < H; h++) {
-      int64_t q0 = cu_q[g], lq = cu_q[g + 1] - cu_q[g];
-      int64_t k0 = cu_k[g], lk = cu_k[g + 1] - cu_k[g];
-      double* sp = (double*)malloc(sizeof(double) * (size_t)tile_n);
-      double* acc = (double*)malloc(sizeof(double) * (size_t)D);
-      for (int64_t i = 0; i < lq; i++) {
+  const float sl2f = (float)scale * 1.4426950408889634f;
+  /* rows (query token, head) are independent: one parallel loop over them */
+  int32_t* seq_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1));
+  for (int g = 0; g < nseq; g++)
+    for (int64_t t = cu_q[g]; t < cu_q[g + 1]; t++) seq_of[t] = g;
+#pragma omp parallel
+  {
+    double* sp = (double*)malloc(sizeof(double) * (size_t)tile_n);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t w = 0; w < total_q * H; w++) {
+      {
+        const int64_t tok = w / H;
+        const int h = (int)(w % H);
+        const int g = seq_of[tok];
+        int64_t q0 = cu_q[g];
+        int64_t k0 = cu_k[g], lk = cu_k[g + 1] - cu_k[g];
+        const int64_t i = tok - q0;
         const double* qi = q + ((q0 + i) * H + h) * D;
         double m = -INFINITY, l = 0.0;
         for (int d = 0; d < D; d++) acc[d] = 0.0;
@@ -286,20 +310,26 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
               const double* kj = k + ((k0 + t0 + j) * H + h) * D;
               double s = 0.0;
               for (int d = 0; d < D; d++) s += qi[d] * kj[d];
-              sp[j] = s * scale * log2e;
+              if (score_fp32) { /* S, s' rounded to fp32 like the MMA and kernel */
+                volatile float t = (float)s * sl2f;
+                sp[j] = t;
+              } else {
+                sp[j] = s * scale * log2e;
+              }
               if (sp[j] > mt) mt = sp[j];
             } else {
               sp[j] = -INFINITY;
             }
           }
           double mn = mt > m ? mt : m;
-          double mu = (m == -INFINITY || mn - m > lazy_thr) ? mn : m;
-          double alpha = (m == -INFINITY) ? 0.0 : exp2(m - mu);
+          double growth = score_fp32 ? (double)((float)mn - (float)m) : mn - m;
+          double mu = (m == -INFINITY || growth > lazy_thr) ? mn : m;
+          double alpha = (m == -INFINITY) ? 0.0 : exp2_prec(m - mu, score_fp32);
           for (int d = 0; d < D; d++) acc[d] *= alpha;
           l *= alpha;
           m = mu;
           for (int64_t j = 0; j < tile_n; j++) {
-            sp[j] = sp[j] == -INFINITY ? 0.0 : flush_fp32_subnormal(exp2(sp[j] - m));
+            sp[j] = sp[j] == -INFINITY ? 0.0 : flush_fp32_subnormal(exp2_prec(sp[j] - m, score_fp32));
             l += sp[j];
           }
           if (quant_p)
@@ -314,10 +344,11 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
         for (int d = 0; d < D; d++) oi[d] = acc[d] / l;
         lse[(int64_t)h * total_q + q0 + i] = (m + log2(l)) * ln2;
       }
-      free(sp);
-      free(acc);
     }
+    free(sp);
+    free(acc);
   }
+  free(seq_of);
 }
 
 /* ------------------------------------------------------------------ */
@@ -334,20 +365,26 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  *   dS^: dS quantized in 32x32 blocks, quant_ds
  *   (blocks anchored at the sequence start in both dimensions)
  *   dV_j = sum_i P^_ij dO_i;  dK_j = scale sum_i dS^_ij q_i;
- *   dQ_i = scale sum_j dS^_ij k_j. */
+ *   dQ_i = scale sum_j dS^_ij k_j.
+ * score_fp32 = 1: S, dP, Delta rounded to fp32 and
+ *   P = fl(2^fl(fl(S * fl(scale * log2 e)) - fl(lse * log2 e))),
+ *   dS = fl(P * fl(dP - Delta)), the kernel's fp32 steps (see the forward). */
 void mxo_attn_bwd(const double* q, const double* k, const double* v,
                   const double* dO, const double* o_bf, const double* do_bf,
                   const double* lse, const int32_t* cu_q, const int32_t* cu_k,
                   int nseq, int H, int D, double scale, int causal, int quant_p,
                   int quant_ds, double* dq, double* dk, double* dv,
-                  int64_t total_q) {
-#pragma omp parallel for collapse(2) schedule(dynamic)
+                  int64_t total_q, int score_fp32) {
+  const float sl2f = (float)scale * 1.4426950408889634f;
+  /* heads in turn; inside a head, independent rows / columns / blocks run in
+   * parallel (every element keeps its own summation order) */
   for (int g = 0; g < nseq; g++) {
     for (int h = 0; h < H; h++) {
       int64_t q0 = cu_q[g], lq = cu_q[g + 1] - cu_q[g];
       int64_t k0 = cu_k[g], lk = cu_k[g + 1] - cu_k[g];
       double* P = (double*)calloc((size_t)(lq * lk > 0 ? lq * lk : 1), sizeof(double));
       double* dS = (double*)calloc((size_t)(lq * lk > 0 ? lq * lk : 1), sizeof(double));
+#pragma omp parallel for schedule(dynamic, 8)
       for (int64_t i = 0; i < lq; i++) {
         const double* qi = q + ((q0 + i) * H + h) * D;
         const double* doi = dO + ((q0 + i) * H + h) * D;
@@ -364,16 +401,30 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
             s += qi[d] * kj[d];
             dp += doi[d] * vj[d];
           }
-          double p = flush_fp32_subnormal(exp(s * scale - li));
-          P[i * lk + j] = p;
-          dS[i * lk + j] = p * (dp - delta);
+          if (score_fp32) { /* fp32 S, dP (MMA outputs) and fp32 elementwise steps */
+            volatile float t = (float)s * sl2f;
+            volatile float l2 = (float)li * 1.4426950408889634f;
+            volatile float arg = t - l2;
+            volatile float pf = (float)exp2((double)arg);
+            double p = flush_fp32_subnormal((double)pf);
+            volatile float diff = (float)dp - (float)delta;
+            volatile float dsf = (float)p * diff;
+            P[i * lk + j] = p;
+            dS[i * lk + j] = dsf;
+          } else {
+            double p = flush_fp32_subnormal(exp(s * scale - li));
+            P[i * lk + j] = p;
+            dS[i * lk + j] = p * (dp - delta);
+          }
         }
       }
       if (quant_p) /* 1x32 along queries, for every key column */
+#pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < lk; j++)
           for (int64_t ib = 0; ib < lq; ib += 32)
             qdq_block(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk);
       if (quant_ds) /* 32x32 square blocks */
+#pragma omp parallel for schedule(static)
         for (int64_t ib = 0; ib < lq; ib += 32)
           for (int64_t jb = 0; jb < lk; jb += 32) {
             int64_t ni = lq - ib < 32 ? lq - ib : 32, nj = lk - jb < 32 ? lk - jb : 32;
@@ -390,6 +441,7 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
                 *e = mxo_e4m3_decode(mxo_e4m3_encode(ldexp(*e, -X))) * ldexp(1.0, X);
               }
           }
+#pragma omp parallel for schedule(dynamic, 8)
       for (int64_t j = 0; j < lk; j++) {
         double* dvj = dv + ((k0 + j) * H + h) * D;
         double* dkj = dk + ((k0 + j) * H + h) * D;
@@ -405,6 +457,7 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
         }
         for (int d = 0; d < D; d++) dkj[d] *= scale;
       }
+#pragma omp parallel for schedule(dynamic, 8)
       for (int64_t i = 0; i < lq; i++) {
         double* dqi = dq + ((q0 + i) * H + h) * D;
         for (int d = 0; d < D; d++) dqi[d] = 0.0;

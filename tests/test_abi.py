@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a device (CPU only)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_block_scaled_fa_gb300 import build, mxfa
+    build.build()
+    return mxfa.lib()
+
+
+def declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfa_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_oracle_in_the_product_library(lib):
+    # the product library carries none of the oracle's symbols
+    for n in ("mxo_quantize", "mxo_attn_fwd", "mxo_attn_bwd", "mxo_rmsnorm_quant"):
+        with pytest.raises(AttributeError):
+            getattr(lib, n)
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.mxfa_status_string(s)
+    assert lib.mxfa_version() == 1
+
+
+def test_packed_tiles_and_sizes(lib):
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    assert mxfa.mxfa_packed_tiles(None, 2, 8192) == 128
+    assert mxfa.mxfa_packed_tiles(None, 1, 1) == 1
+    cu = np.array([0, 5, 133, 133 + 256], np.int32)
+    assert mxfa.mxfa_packed_tiles(cu, 3, 0) == 1 + 1 + 2
+    assert lib.mxfa_sf_packed_bytes(0, 10, 4) == 10 * 4 * 512
+    assert lib.mxfa_sf_packed_bytes(2, 10, 4) == 10 * 4 * 16
+    ws = mxfa.mxfa_bwd_workspace_size(1000, 8, 128, 0)
+    assert ws >= 1000 * 8 * 4 + 1000 * 8 * 128 * 4
+    assert mxfa.mxfa_bwd_workspace_size(1000, 8, 128, 1) < ws
+
+
+def _out(data=0x1000, sfc=0x2000, sfp=0x3000):
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    return mxfa.MxOut(data, sfc, sfp)
+
+
+def test_quantize_argument_checks(lib):
+    q = lib.mxfa_quantize
+    o = _out()
+    ref = ctypes.byref
+    assert q(None, 256, 2, 128, 0, None, 1, 256, 2, ref(o), None) == 1       # null x
+    assert q(0x1000, 256, 2, 64, 0, None, 1, 256, 2, ref(o), None) == 2      # D != 128
+    assert q(0x1000, 256, 2, 128, 7, None, 1, 256, 2, ref(o), None) == 1     # bad block kind
+    assert q(0x1001, 256, 2, 128, 0, None, 1, 256, 2, ref(o), None) == 3     # misaligned
+    assert q(0x1000, 255, 2, 128, 0, None, 1, 256, 2, ref(o), None) == 1     # tokens != nseq*len
+    assert q(0x1000, 256, 2, 128, 0, None, 1, 256, 0, ref(o), None) == 1     # packed w/o tiles
+
+
+def test_attention_argument_checks(lib):
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    m = mxfa.MxIn(0x1000, 0x2000)
+    bad = mxfa.MxIn(0x1008, 0x2000)
+    r = ctypes.byref
+    f = lib.mxfa_fwd
+    assert f(r(m), r(m), r(m), 1, 256, 2, 96, 0.1, 0, 0x4000, 0x5000, None) == 2   # D
+    assert f(r(bad), r(m), r(m), 1, 256, 2, 128, 0.1, 0, 0x4000, 0x5000, None) == 3
+    assert f(r(m), r(m), r(m), 0, 256, 2, 128, 0.1, 0, 0x4000, 0x5000, None) == 1   # B
+    assert f(r(m), r(m), r(m), 1, 256, 2, 128, -1.0, 0, 0x4000, 0x5000, None) == 1  # scale
+    assert f(None, r(m), r(m), 1, 256, 2, 128, 0.1, 0, 0x4000, 0x5000, None) == 1
+    b = lib.mxfa_bwd
+    ws = mxfa.mxfa_bwd_workspace_size(256, 2, 128, 0)
+    args = lambda mode, st, wsb: (r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, 1, 256, 2, 128,
+                                  0.1, 0, mode, st, 0x7000, 0x8000, 0x9000, 0xA000, wsb, None)
+    assert b(*args(0, 1.0, ws - 1)) == 4           # workspace too small
+    assert b(*args(2, 1.0, ws)) == 1               # bad dq mode
+    assert b(*args(1, 3.0, ws)) == 1               # static scale not a power of two
+    v = lib.mxfa_varlen_fwd
+    assert v(r(m), r(m), r(m), None, None, 2, 10, 10, 20, 20, 2, 2, 2, 128, 0.1, 0, 0x4000,
+             0x5000, None) == 1                    # varlen needs cu_seqlens
+
+
+def test_rmsnorm_argument_checks(lib):
+    o = _out(sfp=None)
+    r = ctypes.byref
+    f = lib.mxfa_rmsnorm_quant
+    assert f(0x1000, 0x2000, 64, 300, 1e-6, 64, 2, r(o), None, None, None) == 2    # C
+    assert f(0x1000, 0x2000, 64, 256, 1e-6, 48, 2, r(o), None, None, None) == 2    # seg_len
+    assert f(0x1000, 0x2000, 64, 256, 1e-6, 64, 2, None, None, None, None) == 1    # no output
+    assert f(0x1000, 0x2000, 64, 256, 1e-6, 64, 4, r(o), None, None, None) == 2    # C != H*128

@@ -1,0 +1,153 @@
+"""GPU backward (tcgen05 kernel) vs the CPU oracle on the same seeded inputs.
+
+Bar: dQ, dK, dV relative Frobenius <= 3e-2, for FP32 and FP16 (static scale)
+dQ reduction.  Both sides receive the same O (bf16) and lse, produced by the
+oracle's forward, so the backward is tested on its own; one case chains the
+GPU forward into the GPU backward against the oracle's forward + backward.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from mxfp8_block_scaled_fa_gb300 import inputs
+from tests.helpers import f64, host, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+
+THR = 8.0
+G_REL = 3e-2
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import torch
+    from mxfp8_block_scaled_fa_gb300 import build, mxfa
+    build.build()
+    assert torch.cuda.is_available()
+    return mxfa
+
+
+def gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse_dev, sq, sk, scale, causal, dq_mode=0, dq_static=1.0):
+    import torch
+    q = mx.quantize(to_dev(qb), mx.SQ, sq)
+    k = mx.quantize(to_dev(kb), mx.SQ, sk)
+    v = mx.quantize(to_dev(vb), mx.ROW, sk)
+    do_t = to_dev(dob)
+    dmx = mx.quantize(do_t, mx.SQ, sq)
+    H, D = qb.shape[-2], qb.shape[-1]
+    o_t = to_dev(o_bits).reshape(-1, H, D)
+    dq, dk, dv = mx.attention_bwd(q, k, v, dmx, o_t, do_t.reshape(-1, H, D), lse_dev, sq, sk,
+                                  scale, causal, dq_mode, dq_static)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    return [host(t.float()).astype(np.float64) for t in (dq, dk, dv)]
+
+
+def oracle_fwd_out(qf, kf, vf, cu_q, cu_k, scale, causal):
+    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, scale, causal, True, 128, THR, True)
+    o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
+    return o_bits, inputs.bf16_bits_to_f32(o_bits).astype(np.float64), lse
+
+
+def check(got, ref, tag=""):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        e = rel_fro(g.reshape(r.shape), r)
+        assert e <= G_REL, f"{tag} {name} rel {e}"
+
+
+@pytest.mark.parametrize("B,H,S,causal,dq_mode,dq_static", [
+    (1, 2, 256, False, 0, 1.0),     # the tiny workload, fp32 dQ
+    (1, 2, 256, False, 1, 1.0),     # fp16 dQ, static scale 1
+    (1, 2, 256, False, 1, 16.0),    # fp16 dQ, static scale 2^4
+    (1, 2, 384, True, 0, 1.0),
+    (2, 2, 300, True, 0, 1.0),      # ragged tail in both key and query tiles
+    (2, 3, 300, False, 1, 4.0),
+    (1, 1, 33, False, 0, 1.0),
+])
+def test_bwd_dense(mx, B, H, S, causal, dq_mode, dq_static):
+    import torch
+    D = 128
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=200 + S)
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+    o_bits, o_bf, lse = oracle_fwd_out(f(qb), f(kb), f(vb), cu, cu, scale, causal)
+    lse_dense = lse.reshape(H, B, S).transpose(1, 0, 2).astype(np.float32)
+    seqs = mx.Seqs.dense(B, S)
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse_dense.copy()).cuda(), seqs,
+                  seqs, scale, causal, dq_mode, dq_static)
+    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lse, cu, cu, scale, causal, True, True)
+    check(got, ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen(mx, causal):
+    import torch
+    H, D = 2, 128
+    lq = [64, 300, 7, 129, 1, 255]
+    lk = lq if causal else [32, 200, 1, 260, 77, 128]
+    qb, kb, vb, dob, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=31)
+    scale = 1 / math.sqrt(D)
+    o_bits, o_bf, lse = oracle_fwd_out(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal)
+    sq = mx.Seqs.varlen(lq, "cuda")
+    sk = mx.Seqs.varlen(lk, "cuda")
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse.astype(np.float32)).cuda(),
+                  sq, sk, scale, causal)
+    ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale,
+                            causal, True, True)
+    check(got, ref)
+
+
+def test_fwd_then_bwd_on_gpu(mx):
+    # the path as a training step runs it: GPU forward output feeds the GPU backward
+    import torch
+    B, H, S, D = 1, 2, 256, 128
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=0)
+    seqs = mx.Seqs.dense(B, S)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o, lse = mx.attention_fwd(q, k, v, seqs, seqs, scale, causal=True)
+    do_t = to_dev(dob)
+    dq, dk, dv = mx.attention_bwd(mx.quantize(to_dev(qb), mx.SQ, seqs),
+                                  mx.quantize(to_dev(kb), mx.SQ, seqs),
+                                  mx.quantize(to_dev(vb), mx.ROW, seqs),
+                                  mx.quantize(do_t, mx.SQ, seqs), o, do_t.reshape(B * S, H, D),
+                                  lse, seqs, seqs, scale, causal=True)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    o_bits, o_bf, lo = oracle_fwd_out(f(qb), f(kb), f(vb), None, None, scale, True)
+    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lo, None, None, scale, True, True, True)
+    check([host(t.float()).astype(np.float64) for t in (dq, dk, dv)], ref, "chained")
+
+
+def test_bwd_llm_config_sampled_head(mx):
+    # the full LLM-shaped causal backward on the GPU; the oracle recomputes one
+    # (batch, head) pair in full from the same O and lse
+    import torch
+    B, H, S, D = 2, 16, 8192, 128
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=1)
+    b, h = 1, 5
+    sl = lambda x: f64(x[b, :, h:h + 1, :])
+    o_h_bits, o_h_bf, lse_h = oracle_fwd_out(sl(qb), sl(kb), sl(vb), None, None, scale, True)
+    # O and lse for every head: the sampled head from the oracle, others from the GPU forward
+    seqs = mx.Seqs.dense(B, S)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o, lse = mx.attention_fwd(q, k, v, seqs, seqs, scale, causal=True)
+    torch.cuda.synchronize()
+    o_bits = host(o.view(torch.int16)).view(np.uint16).reshape(B, S, H, D).copy()
+    o_bits[b, :, h, :] = o_h_bits.reshape(S, D)
+    lse_h32 = torch.from_numpy(lse_h.reshape(S).astype(np.float32)).cuda()
+    lse.view(B, H, S)[b, h].copy_(lse_h32)
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, scale, True)
+    got = [g.reshape(B, S, H, D)[b, :, h:h + 1, :] for g in got]
+    ref = oracle.method_bwd(sl(qb), sl(kb), sl(vb), sl(dob), o_h_bf, lse_h, None, None, scale, True,
+                            True, True)
+    check(got, ref, "llm")

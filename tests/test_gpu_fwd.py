@@ -1,0 +1,124 @@
+"""GPU forward (tcgen05 kernel) vs the CPU oracle on the same seeded inputs.
+
+Bar: O relative Frobenius <= 1e-2 and max-abs <= 3e-2; LSE max-abs <= 1e-4;
+each max-abs bar plus the rounding of the output format (bf16 O, fp32 lse).
+The oracle runs the method with the kernel's declared schedule: 128-key
+tiles in ascending order, running max moved when it grows by more than 8
+(log2 units), and takes the values that decide P's quantization codes in
+fp32, the kernel's precision.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from mxfp8_block_scaled_fa_gb300 import inputs
+from tests.helpers import f64, host, max_abs, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+
+THR = 8.0
+O_REL, O_ABS, LSE_ABS = 1e-2, 3e-2, 1e-4
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import torch
+    from mxfp8_block_scaled_fa_gb300 import build, mxfa
+    build.build()
+    assert torch.cuda.is_available()
+    return mxfa
+
+
+def gpu_fwd(mx, qb, kb, vb, seqs_q, seqs_k, scale, causal):
+    import torch
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs_q)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs_k)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs_k)
+    o, lse = mx.attention_fwd(q, k, v, seqs_q, seqs_k, scale, causal)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    return host(o.float()).astype(np.float64), host(lse)
+
+
+def _spacing(x, mant_bits):
+    """Distance between adjacent numbers near |x| in a format with mant_bits."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - mant_bits)
+
+
+def check(o, lse, oo, lo):
+    # O is returned in bf16 and lse in fp32: the max-abs bars add the output
+    # format's own rounding (half a bf16 spacing of O, four fp32 spacings of
+    # lse), which only matters where |O| > 8 or |lse| > 100
+    assert rel_fro(o, oo) <= O_REL, rel_fro(o, oo)
+    excess = np.abs(o - oo) - 0.5 * _spacing(oo, 7)
+    assert excess.max() <= O_ABS, (max_abs(o, oo), excess.max())
+    lexcess = np.abs(lse - lo) - 4 * _spacing(lo, 23)
+    assert lexcess.max() <= LSE_ABS, (max_abs(lse, lo), lexcess.max())
+
+
+@pytest.mark.parametrize("B,H,S,causal", [
+    (1, 2, 256, False),     # the tiny workload
+    (1, 2, 384, True),
+    (2, 3, 300, False),     # ragged tail inside a 128-key tile
+    (2, 2, 300, True),
+    (1, 1, 1, False),       # single key
+    (1, 2, 33, True),
+    (3, 2, 640, True),      # several tiles per head, more than the K/V ring
+])
+def test_fwd_dense(mx, B, H, S, causal):
+    D = 128
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb, _ = inputs.dense_attn(B, H, S, D, seed=100 + S)
+    seqs = mx.Seqs.dense(B, S)
+    o, lse = gpu_fwd(mx, qb, kb, vb, seqs, seqs, scale, causal)
+    cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), cu, cu, scale, causal, True, 128, THR, True)
+    check(o.reshape(B * S, H, D), lse.reshape(B, H, S).transpose(1, 0, 2).reshape(H, B * S), oo, lo)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_varlen(mx, causal):
+    H, D = 2, 128
+    lq = [64, 300, 7, 129, 1, 255]
+    lk = lq if causal else [32, 200, 1, 260, 77, 128]
+    qb, kb, vb, _, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=21)
+    sq = mx.Seqs.varlen(lq, "cuda")
+    sk = mx.Seqs.varlen(lk, "cuda")
+    scale = 1 / math.sqrt(D)
+    o, lse = gpu_fwd(mx, qb, kb, vb, sq, sk, scale, causal)
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal, True, 128, THR, True)
+    check(o, lse, oo, lo)
+
+
+@pytest.mark.parametrize("outliers_v", [False, True])
+def test_fwd_outliers_small(mx, outliers_v):
+    # the outlier recipe (1% of Q/K channels x20, 0.1% of elements x200);
+    # outliers_v also puts 0.1% x200 elements into V (non-uniform V scales)
+    B, H, S, D = 1, 4, 512, 128
+    qb, kb, vb, _ = inputs.dense_attn(B, H, S, D, seed=2, outliers=True, outliers_v=outliers_v)
+    seqs = mx.Seqs.dense(B, S)
+    scale = 1 / math.sqrt(D)
+    o, lse = gpu_fwd(mx, qb, kb, vb, seqs, seqs, scale, False)
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, scale, False, True, 128, THR, True)
+    check(o.reshape(B * S, H, D), lse.reshape(H, S), oo, lo)
+
+
+def test_fwd_llm_config_sampled_heads(mx):
+    # full LLM-shaped causal workload on the GPU, as the benchmark launches it;
+    # the oracle recomputes two sampled (batch, head) pairs in full
+    B, H, S, D = 2, 16, 8192, 128
+    scale = 1 / math.sqrt(D)
+    qb, kb, vb, _ = inputs.dense_attn(B, H, S, D, seed=1)
+    seqs = mx.Seqs.dense(B, S)
+    o, lse = gpu_fwd(mx, qb, kb, vb, seqs, seqs, scale, True)
+    o = o.reshape(B, S, H, D)
+    lse = lse.reshape(B, H, S)
+    for b, h in ((0, 3), (1, 14)):
+        sl = lambda x: f64(x[b, :, h:h + 1, :])
+        oo, lo = oracle.method_fwd(sl(qb), sl(kb), sl(vb), None, None, scale, True, True, 128, THR, True)
+        check(o[b, :, h:h + 1, :], lse[b, h:h + 1, :], oo, lo)

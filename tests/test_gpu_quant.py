@@ -1,0 +1,132 @@
+"""GPU quantizers and fused RMSNorm+Quantize vs the CPU oracle: bit-exact
+payload bytes and E8M0 scales (compact, and packed after decoding)."""
+import numpy as np
+import pytest
+
+import oracle
+from mxfp8_block_scaled_fa_gb300 import inputs
+from tests.helpers import f64, host, to_dev, unpack_packed
+
+pytestmark = pytest.mark.gpu
+
+MODES = [(0, "row"), (1, "col"), (2, "sq")]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import torch
+    from mxfp8_block_scaled_fa_gb300 import build, mxfa
+    build.build()
+    assert torch.cuda.is_available()
+    return mxfa
+
+
+def _check_quant(mx, bits3, lens, H, blk):
+    import torch
+    tokens = bits3.shape[0]
+    if lens is None:
+        seqs = mx.Seqs.dense(1, tokens)
+        lens_ = [tokens]
+        cu = None
+    else:
+        seqs = mx.Seqs.varlen(lens, "cuda")
+        lens_ = lens
+        cu = seqs.cu_host
+    m = mx.quantize(to_dev(bits3), blk, seqs)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    q_ref, s_ref = oracle.quantize(f64(bits3).reshape(tokens, -1), blk, cu)
+    np.testing.assert_array_equal(host(m.data).reshape(tokens, -1), q_ref)
+    np.testing.assert_array_equal(host(m.sf_compact), s_ref)
+    comp, pad = unpack_packed(host(m.sf_packed), blk, lens_, H)
+    np.testing.assert_array_equal(comp, s_ref)
+    assert np.all(pad == 0x7F)
+    packed2 = mx.sf_pack(m.sf_compact, blk, seqs, H)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(packed2), host(m.sf_packed))
+
+
+@pytest.mark.parametrize("blk,name", MODES)
+def test_quantize_tiny_dense(mx, blk, name):
+    q, _, _, _ = inputs.dense_attn(1, 2, 256, 128, seed=0)
+    _check_quant(mx, q.reshape(256, 2, 128), None, 2, blk)
+
+
+@pytest.mark.parametrize("blk,name", MODES)
+def test_quantize_ragged_varlen(mx, blk, name):
+    lens = [5, 130, 64, 33, 1, 257]
+    q, _, _, _, _, _ = inputs.varlen_attn(lens, lens, 3, 128, seed=5)
+    _check_quant(mx, q, lens, 3, blk)
+
+
+@pytest.mark.parametrize("blk,name", MODES)
+def test_quantize_adversarial_blocks(mx, blk, name):
+    # zeros, -0, the 448 boundary, E4M3 subnormals, ties, huge / tiny values,
+    # and Inf / NaN blocks, laid out so every block kind meets them
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((128, 2, 128)).astype(np.float32)
+    flat = x.reshape(128, 256)
+    flat[0:32, 0:32] = 0.0
+    flat[1, 5] = -0.0
+    flat[32:64, 32:64] = 1.0
+    flat[40, 40] = 1.75
+    flat[41, 41] = 1.875
+    flat[64, 64:96] = [1.0] + [2.0 ** -17, 2.0 ** -18, 1.5 * 2 ** -17, 3 * 2 ** -19] + [0.0] * 27
+    flat[65, 64:68] = [1.0, 17 * 2.0 ** -9, 19 * 2.0 ** -9, 31 * 2.0 ** -9]
+    flat[96:128, 96:128] *= 2.0 ** 120
+    flat[70, 130] = 1.9921875 * 2.0 ** 127
+    flat[71, 131] = 2.0 ** -130
+    flat[100, 200] = np.inf
+    flat[101, 210] = -np.inf
+    flat[102, 220] = np.nan
+    bits = inputs.f32_to_bf16_bits(x)
+    _check_quant(mx, bits, None, 2, blk)
+
+
+def test_quantize_full_llm_tensor(mx):
+    # one full Q tensor of the LLM-shaped workload (B2 S8192 H16), all kinds
+    import torch
+    B, S, H, D = 2, 8192, 16, 128
+    q = inputs.normal_bf16((B, S, H, D), 1)
+    dev = to_dev(q)
+    seqs = mx.Seqs.dense(B, S)
+    x64 = f64(q).reshape(B * S, H * D)
+    cu = np.array([0, S, 2 * S], np.int32)
+    for blk in (0, 1, 2):
+        m = mx.quantize(dev, blk, seqs)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        q_ref, s_ref = oracle.quantize(x64, blk, cu)
+        np.testing.assert_array_equal(host(m.data).reshape(B * S, -1), q_ref)
+        np.testing.assert_array_equal(host(m.sf_compact), s_ref)
+
+
+@pytest.mark.parametrize("T,C,H,seg", [(256, 2048, 16, 128), (96, 256, 2, 32), (384, 512, 4, 128)])
+def test_rmsnorm_quant_small(mx, T, C, H, seg):
+    import torch
+    x = inputs.normal_bf16((T, C), 7)
+    g = np.random.default_rng(8).uniform(0.5, 1.5, C).astype(np.float32)
+    packed = (T % seg == 0) and (seg % 128 == 0)
+    res = mx.rmsnorm_quant(to_dev(x), torch.from_numpy(g).cuda(), 1e-6, seg, H, packed=packed)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    ref = oracle.rmsnorm_quant(inputs.bf16_bits_to_f32(x), g, 1e-6, 7, seg)
+    for name, blk in (("row", 0), ("col", 1), ("sq", 2)):
+        np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
+        np.testing.assert_array_equal(host(res[name].sf_compact), ref[name][1], err_msg=name)
+        if packed:
+            comp, pad = unpack_packed(host(res[name].sf_packed), blk, [seg] * (T // seg), H)
+            np.testing.assert_array_equal(comp, ref[name][1], err_msg=name)
+
+
+def test_rmsnorm_quant_full_fused_config(mx):
+    # the fused producer workload: X [32768, 2048], gamma U[0.5, 1.5], eps 1e-6
+    import torch
+    x, g, _ = inputs.fused_inputs()
+    res = mx.rmsnorm_quant(to_dev(x), torch.from_numpy(g).cuda(), 1e-6, 8192, 16)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    ref = oracle.rmsnorm_quant(inputs.bf16_bits_to_f32(x), g, 1e-6, 7, 8192)
+    for name in ("row", "col", "sq"):
+        np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
+        np.testing.assert_array_equal(host(res[name].sf_compact), ref[name][1], err_msg=name)

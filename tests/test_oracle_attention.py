@@ -238,3 +238,34 @@ def test_bwd_quantized_close_to_exact():
     for a, b in zip(qu, ex):
         rel = np.linalg.norm(a - b) / np.linalg.norm(b)
         assert 1e-3 < rel < 0.15
+
+
+# ----------------------------------------------- fp32 decision-precision mode
+def test_fp32_mode_rounds_scores_to_fp32():
+    # q.k0 = 2^24 + 1 and q.k1 = 2^24: fp64 keeps the difference of 1 (times
+    # tau * log2 e = 2 with tau = 2 ln 2, so P~ = (1/4, 1) -> O = 1/(1 + 1/4) * v1
+    # = 0.8 for v0 = 0, v1 = 1), fp32 scores round both to 2^24 (P~ = (1, 1) -> O = 0.5).
+    q = np.zeros((1, 1, 4)); q[0, 0, 0] = 2.0 ** 12
+    k = np.zeros((2, 1, 4)); k[0, 0, 0] = 2.0 ** 12; k[1, 0, 0] = 2.0 ** 12 + 2.0 ** -12
+    v = np.zeros((2, 1, 4)); v[1] = 1.0
+    cu = np.array([0, 1], np.int32); ck = np.array([0, 2], np.int32)
+    tau = 2 * math.log(2.0)
+    o64, _ = oracle.attn_fwd(q, k, v, cu, ck, tau, False, True, 128, 0.0, False)
+    o32, _ = oracle.attn_fwd(q, k, v, cu, ck, tau, False, True, 128, 0.0, True)
+    np.testing.assert_allclose(o64, 0.8, rtol=1e-12)
+    np.testing.assert_allclose(o32, 0.5, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_mode_close_to_definition(causal):
+    S, H, D = 300, 2, 64
+    q, k, v, do = (_rand((S, H, D), s) for s in (60, 61, 62, 63))
+    scale = 1 / math.sqrt(D)
+    o64, l64 = oracle.attn_fwd(q, k, v, None, None, scale, causal, False, 128, 8.0, False)
+    o32, l32 = oracle.attn_fwd(q, k, v, None, None, scale, causal, False, 128, 8.0, True)
+    np.testing.assert_allclose(o32, o64, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(l32, l64, rtol=0, atol=2e-6)
+    g64 = oracle.attn_bwd(q, k, v, do, o64, do, l64, None, None, scale, causal, False, False, False)
+    g32 = oracle.attn_bwd(q, k, v, do, o64, do, l64, None, None, scale, causal, False, False, True)
+    for a, b in zip(g32, g64):
+        assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-5
