@@ -204,6 +204,30 @@ mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int
                                int seg_len, int H, const mxfa_mx_out* row, const mxfa_mx_out* col,
                                const mxfa_mx_out* sq, mxfa_stream_t stream);
 
+/* mxfa_bwd_noalloc -- mxfa_bwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call: it is an interface
+ * addition of this library.
+ *  For code that must not call cudaMalloc (allocator or memory-pool hooks,
+ *  runtimes that forbid device allocation after start-up, bindings without a
+ *  device allocator), the workspace comes from a scratch array compiled into
+ *  the library (mxfa_bwd_noalloc_scratch_bytes() = 32 MiB, 256-byte aligned,
+ *  held by every GPU that loads the library until the process exits).  The
+ *  call allocates nothing; inputs and outputs are as for mxfa_bwd.
+ *  The first call on each device looks up the array's device address
+ *  (cudaGetSymbolAddress, with that device current) and caches it: make that
+ *  first call before any stream capture.
+ *  Problems whose workspace (mxfa_bwd_workspace_size) exceeds the array are
+ *  rejected with MXFA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  All calls share the one array and it keeps the last call's contents (the
+ *  backward pass clears what must start at zero); calls that overlap on the
+ *  GPU, e.g. on two streams, race on it. */
+mxfa_status mxfa_bwd_noalloc(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                             const mxfa_mx* dout_mx, const void* o, const void* dout,
+                             const float* lse, int B, int S, int H, int D, float softmax_scale,
+                             int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
+                             void* dv, mxfa_stream_t stream);
+size_t mxfa_bwd_noalloc_scratch_bytes(void);
+
 /* Synchronise `stream`, then return and clear the device status words:
  * MXFA_OK, MXFA_ERR_TIMEOUT or MXFA_ERR_DEVICE_INDEX (bit flags also in
  * *flags when flags is not NULL: 1 timeout, 2 index). */

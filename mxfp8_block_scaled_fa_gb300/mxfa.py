@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
                                     F, I, I, F, P, P, P, P, S, P]),
             "mxfa_rmsnorm_quant": (I, [P, P, I64, I64, F, I, I, P, P, P, P]),
             "mxfa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint)]),
+            "mxfa_bwd_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P]),
+            "mxfa_bwd_noalloc_scratch_bytes": (S, []),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -140,6 +142,15 @@ def mxfa_bwd(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, dq_mode, dq_
                           _p(o), _p(do), _p(lse), B, S, H, D, float(scale), int(causal), dq_mode,
                           float(dq_static), _p(dq), _p(dk), _p(dv), _p(ws), ws_bytes,
                           _stream(stream)), "mxfa_bwd")
+
+
+def mxfa_bwd_noalloc(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, dq_mode, dq_static,
+                     dq, dk, dv, stream=None):
+    """mxfa_bwd without a caller workspace (the library's built-in scratch array)."""
+    _check(lib().mxfa_bwd_noalloc(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                  ctypes.byref(do_mx), _p(o), _p(do), _p(lse), B, S, H, D,
+                                  float(scale), int(causal), dq_mode, float(dq_static), _p(dq),
+                                  _p(dk), _p(dv), _stream(stream)), "mxfa_bwd_noalloc")
 
 
 def mxfa_varlen_bwd(q, k, v, do_mx, o, do, lse, cu_q, cu_k, nseq, max_sq, max_sk, total_q,
