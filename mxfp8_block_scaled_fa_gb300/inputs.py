@@ -37,9 +37,12 @@ CONFIGS = {
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns (uint16), round to nearest even."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (b >> 16) & 1
-    r = ((b + 0x7FFF + lsb) >> 16).astype(np.uint16)
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    # finite patterns are <= 0xFF7FFFFF, so adding at most 0x8000 cannot wrap
+    t = (b >> 16) & 1
+    t += b
+    t += 0x7FFF
+    r = (t >> 16).astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         r[nan] = 0x7FC0
