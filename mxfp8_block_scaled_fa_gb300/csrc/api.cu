@@ -48,6 +48,22 @@ bool make_map_u8(CUtensorMap* m, const void* ptr, int64_t tokens, int H, int box
   return r == CUDA_SUCCESS;
 }
 
+// dQ accumulator [tokens][H][128] (fp32 or fp16) as a 3-D map, box 128 x 1 x 64.
+bool make_map_acc(CUtensorMap* m, const void* ptr, int64_t tokens, int H, bool half) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t esz = half ? 2 : 4;
+  cuuint64_t dims[3] = {128, cuuint64_t(H), cuuint64_t(tokens)};
+  cuuint64_t strides[2] = {128 * esz, cuuint64_t(H) * 128 * esz};
+  cuuint32_t box[3] = {128, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, half ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 mxfa_status from_cuda(cudaError_t e) {
@@ -159,6 +175,7 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   a.delta = static_cast<float*>(ws);
   const size_t delta_bytes = ((size_t(total_q) * H * 4) + 255) & ~size_t(255);
   a.dq_acc = static_cast<uint8_t*>(ws) + delta_bytes;
+  if (!make_map_acc(&a.tm_dqacc, a.dq_acc, total_q, H, dq_mode == 1)) return MXFA_ERR_CUDA;
   a.dense_lse = dense ? 1 : 0;
   a.lse_hstride = dense ? sq.seqlen : total_q;
   return from_cuda(launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)));

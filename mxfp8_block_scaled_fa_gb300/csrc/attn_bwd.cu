@@ -40,6 +40,7 @@ namespace bwd {
 constexpr int KT = 128;                 // keys per CTA
 constexpr int QT = 64;                  // queries per inner tile
 constexpr int NSQ = 2;                  // Q / dO ring stages
+constexpr int NSF = 4;                  // per-tile scale-atom / lse / Delta ring stages
 constexpr int KV_BYTES = KT * 128;      // 16 KB
 constexpr int QD_BYTES = QT * 128;      // 8 KB
 constexpr int PS_BYTES = KT * QT;       // 8 KB (128 rows x 64 B)
@@ -50,18 +51,20 @@ constexpr int OFF_Q = OFF_V + KV_BYTES;                 // NSQ stages
 constexpr int OFF_DO = OFF_Q + NSQ * QD_BYTES;          // NSQ stages
 constexpr int OFF_PT = OFF_DO + NSQ * QD_BYTES;         // 2 buffers, SW64
 constexpr int OFF_DST = OFF_PT + 2 * PS_BYTES;          // 2 buffers, SW64
-constexpr int OFF_DQS = OFF_DST + 2 * PS_BYTES;         // dQ staging, 64 x 512 B
-constexpr int OFF_ATOM = OFF_DQS + QT * 512;
+constexpr int DQS_BYTES = QT * 512;                    // one dQ staging tile (fp32)
+constexpr int OFF_DQS = OFF_DST + 2 * PS_BYTES;         // dQ staging, 2 tiles
+constexpr int OFF_ATOM = OFF_DQS + 2 * DQS_BYTES;
 // scale atoms (512 B each)
 constexpr int A_SFK = 0, A_SFV = 1, A_SFKT = 2;
-constexpr int A_SFQ = 3, A_SFDO = 5, A_SFDOT = 7, A_SFQT = 9;    // x2 (tile parity)
-constexpr int A_SFPT = 11, A_SFDST = 13, A_SFDS = 15;            // x2
-constexpr int NATOM = 17;
-constexpr int OFF_LD = OFF_ATOM + NATOM * 512;          // lse*log2e, Delta: 2 x 2 x 64 floats
-constexpr int OFF_BAR = OFF_LD + 2 * 2 * QT * 4;
+constexpr int A_SFQ = 3, A_SFDO = A_SFQ + NSF, A_SFDOT = A_SFDO + NSF,
+              A_SFQT = A_SFDOT + NSF;                     // x NSF (ring stage)
+constexpr int A_SFPT = A_SFQT + NSF, A_SFDST = A_SFPT + 2, A_SFDS = A_SFDST + 2;  // x2
+constexpr int NATOM = A_SFDS + 2;
+constexpr int OFF_LD = OFF_ATOM + NATOM * 512;          // lse*log2e, Delta: NSF x 2 x 64 floats
+constexpr int OFF_BAR = OFF_LD + NSF * 2 * QT * 4;
 enum {
   B_KVFULL = 0, B_KCONST, B_QDOFULL, B_QDOEMPTY = B_QDOFULL + NSQ, B_SFINFULL = B_QDOEMPTY + NSQ,
-  B_SFINEMPTY = B_SFINFULL + 2, B_SDPFULL = B_SFINEMPTY + 2, B_SDPFREE, B_PFULL,
+  B_SFINEMPTY = B_SFINFULL + NSF, B_SDPFULL = B_SFINEMPTY + NSF, B_SDPFREE, B_PFULL,
   B_PDSEMPTY = B_PFULL + 2, B_DQFULL = B_PDSEMPTY + 2, B_DQEMPTY, B_KVDONE, B_TEAR, NBAR
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
   auto ATOM = [&](int i) { return smem + OFF_ATOM + 512 * i; };
   auto ATOMA = [&](int i) { return base + OFF_ATOM + 512u * uint32_t(i); };
-  float* ld_stage = reinterpret_cast<float*>(smem + OFF_LD);  // [2 tiles][2: lse2, delta][64]
+  float* ld_stage = reinterpret_cast<float*>(smem + OFF_LD);  // [NSF][2: lse2, delta][64]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);
 
@@ -196,9 +199,11 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       mbar_init(BAR(B_QDOFULL + s), 1);
       mbar_init(BAR(B_QDOEMPTY + s), 1);
     }
+    for (int f = 0; f < NSF; f++) {
+      mbar_init(BAR(B_SFINFULL + f), 64);
+      mbar_init(BAR(B_SFINEMPTY + f), 1);
+    }
     for (int b = 0; b < 2; b++) {
-      mbar_init(BAR(B_SFINFULL + b), 64);
-      mbar_init(BAR(B_SFINEMPTY + b), 1);
       mbar_init(BAR(B_PFULL + b), 256);
       mbar_init(BAR(B_PDSEMPTY + b), 1);
     }
@@ -261,37 +266,39 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     // k-blocks 0..3 in its bytes.  Square scale entry: byte 4 * tb + db.
     const int t = tid - 64;
     const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(a.sfk + (tk * a.H + h) * 16));
-    const uint32_t kw[4] = {k4.x, k4.y, k4.z, k4.w};  // kw[tb] = bytes db 0..3
-    auto col_bytes = [](const uint32_t* wv, int db, int tb_lo, int ntb) {
-      uint32_t v = 0x7F7F7F7Fu;
-      for (int j = 0; j < ntb; j++) {
-        const uint32_t byte = (wv[tb_lo + j] >> (8 * db)) & 0xFFu;
-        v = (v & ~(0xFFu << (8 * j))) | (byte << (8 * j));
-      }
-      return v;
+    // word tb of an entry holds the bytes of token block tb for d-blocks 0..3
+    auto pick = [](uint4 e, int tb) {
+      return tb == 0 ? e.x : tb == 1 ? e.y : tb == 2 ? e.z : e.w;
+    };
+    // byte db of token blocks tb0, tb0+1 (and tb0+2, tb0+3 when all4), padding 0x7F
+    auto col_bytes = [&](uint4 e, int db, int tb0, bool all4) {
+      const uint32_t sh = 8u * uint32_t(db);
+      const uint32_t b0 = (pick(e, tb0) >> sh) & 0xFFu, b1 = (pick(e, tb0 + 1) >> sh) & 0xFFu;
+      const uint32_t b2 = all4 ? (e.z >> sh) & 0xFFu : 0x7Fu, b3 = all4 ? (e.w >> sh) & 0xFFu : 0x7Fu;
+      return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
     };
     for (int w = t; w < 128; w += 64) {
-      reinterpret_cast<uint32_t*>(ATOM(A_SFK))[w] = kw[w & 3];           // rows = keys
-      reinterpret_cast<uint32_t*>(ATOM(A_SFKT))[w] = col_bytes(kw, w & 3, 0, 4);  // rows = d
+      reinterpret_cast<uint32_t*>(ATOM(A_SFK))[w] = pick(k4, w & 3);                 // rows = keys
+      reinterpret_cast<uint32_t*>(ATOM(A_SFKT))[w] = col_bytes(k4, w & 3, 0, true);  // rows = d
     }
     fence_async_smem();
     mbar_arrive(BAR(B_KCONST));
     const float l2e = 1.4426950408889634f;
     for (int ii = 0; ii < ntile; ii++) {
-      const int i = first + ii, b = ii & 1;
-      if (ii >= 2 && !mbar_wait(BAR(B_SFINEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag, &g_status_bwd))
+      const int i = first + ii, f = ii % NSF;
+      if (ii >= NSF &&
+          !mbar_wait(BAR(B_SFINEMPTY + f), ((ii / NSF) - 1) & 1, abort_flag, &g_status_bwd))
         break;
       const int64_t ent = ((tq_base + i / 2) * a.H + h) * 16;
       const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + ent));
       const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + ent));
-      const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
       const int tb0 = (i & 1) * 2;
       for (int w = t; w < 128; w += 64) {
         const int rg = w & 3;  // row group = 32-row block of the atom
-        reinterpret_cast<uint32_t*>(ATOM(A_SFQ + b))[w] = rg < 2 ? qw[tb0 + rg] : 0x7F7F7F7Fu;
-        reinterpret_cast<uint32_t*>(ATOM(A_SFDO + b))[w] = rg < 2 ? dw[tb0 + rg] : 0x7F7F7F7Fu;
-        reinterpret_cast<uint32_t*>(ATOM(A_SFQT + b))[w] = col_bytes(qw, rg, tb0, 2);
-        reinterpret_cast<uint32_t*>(ATOM(A_SFDOT + b))[w] = col_bytes(dw, rg, tb0, 2);
+        reinterpret_cast<uint32_t*>(ATOM(A_SFQ + f))[w] = rg < 2 ? pick(q4, tb0 + rg) : 0x7F7F7F7Fu;
+        reinterpret_cast<uint32_t*>(ATOM(A_SFDO + f))[w] = rg < 2 ? pick(d4, tb0 + rg) : 0x7F7F7F7Fu;
+        reinterpret_cast<uint32_t*>(ATOM(A_SFQT + f))[w] = col_bytes(q4, rg, tb0, false);
+        reinterpret_cast<uint32_t*>(ATOM(A_SFDOT + f))[w] = col_bytes(d4, rg, tb0, false);
       }
       {
         const int c = t;  // query column of the tile
@@ -303,11 +310,11 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           l2 = lse * l2e;
           dl = a.delta[int64_t(h) * a.total_q + sq0 + q];
         }
-        ld_stage[(b * 2 + 0) * QT + c] = l2;
-        ld_stage[(b * 2 + 1) * QT + c] = dl;
+        ld_stage[(f * 2 + 0) * QT + c] = l2;
+        ld_stage[(f * 2 + 1) * QT + c] = dl;
       }
       fence_async_smem();
-      mbar_arrive(BAR(B_SFINFULL + b));
+      mbar_arrive(BAR(B_SFINFULL + f));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -326,14 +333,14 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       }
       // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T for local tile jj
       auto grads = [&](int jj) -> bool {
-        const int s = jj % NSQ, b = jj & 1;
+        const int s = jj % NSQ, b = jj & 1, f = jj % NSF;
         if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_bwd)) return false;
         if (jj >= 1 && !mbar_wait(BAR(B_DQEMPTY), (jj - 1) & 1, abort_flag, &g_status_bwd)) return false;
         tc_fence_after();
         cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
-        cp_sf(COL_SFDOT + 4 * b, ATOMA(A_SFDOT + b));
+        cp_sf(COL_SFDOT + 4 * b, ATOMA(A_SFDOT + f));
         cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
-        cp_sf(COL_SFQT + 4 * b, ATOMA(A_SFQT + b));
+        cp_sf(COL_SFQT + 4 * b, ATOMA(A_SFQT + f));
         cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
         const uint32_t pt = base + OFF_PT + b * PS_BYTES, dst = base + OFF_DST + b * PS_BYTES;
         const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
@@ -353,22 +360,22 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
                       smem_desc(dst + 2048 * k, 8192, 512, 4), idesc_mxf8(128, 64, 1, 1, k, k),
                       tmem + COL_SFKT, tmem + COL_SFDS + 4 * b, k > 0 ? 1u : 0u);
         tc_commit(BAR(B_QDOEMPTY + s));
-        tc_commit(BAR(B_SFINEMPTY + b));
+        tc_commit(BAR(B_SFINEMPTY + f));
         tc_commit(BAR(B_PDSEMPTY + b));
         tc_commit(BAR(B_DQFULL));
         return true;
       };
       for (int ii = 0; ok && ii < ntile; ii++) {
-        const int s = ii % NSQ, b = ii & 1;
+        const int s = ii % NSQ, f = ii % NSF;
         if (!mbar_wait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag, &g_status_bwd) ||
-            !mbar_wait(BAR(B_SFINFULL + b), (ii >> 1) & 1, abort_flag, &g_status_bwd) ||
+            !mbar_wait(BAR(B_SFINFULL + f), (ii / NSF) & 1, abort_flag, &g_status_bwd) ||
             (ii >= 1 && !mbar_wait(BAR(B_SDPFREE), (ii - 1) & 1, abort_flag, &g_status_bwd))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        cp_sf(COL_SFQ, ATOMA(A_SFQ + b));
-        cp_sf(COL_SFDO, ATOMA(A_SFDO + b));
+        cp_sf(COL_SFQ, ATOMA(A_SFQ + f));
+        cp_sf(COL_SFDO, ATOMA(A_SFDO + f));
         const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
 #pragma unroll
         for (int k = 0; k < 4; k++)
@@ -407,9 +414,10 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(BAR(B_SDPFREE));
-      if (!wwait(BAR(B_SFINFULL + b), (ii >> 1) & 1, abort_flag)) { ok = false; break; }
-      const float* l2 = ld_stage + (b * 2 + 0) * QT + 32 * hq;
-      const float* dl = ld_stage + (b * 2 + 1) * QT + 32 * hq;
+      const int f = ii % NSF;
+      if (!wwait(BAR(B_SFINFULL + f), (ii / NSF) & 1, abort_flag)) { ok = false; break; }
+      const float* l2 = ld_stage + (f * 2 + 0) * QT + 32 * hq;
+      const float* dl = ld_stage + (f * 2 + 1) * QT + 32 * hq;
       const int q0 = i * QT + 32 * hq;
       float pmax = 0.0f, dsmax = 0.0f;
 #pragma unroll
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     const int esz = a.dq_mode == 1 ? 2 : 4;
     const uint32_t rowb = 128u * esz;
     const float mult = a.scale * a.dq_static_scale;
-    uint8_t* stg = smem + OFF_DQS;
+    uint8_t* stg0 = smem + OFF_DQS;
     volatile int* vote = reinterpret_cast<volatile int*>(smem + OFF_MISC + 16);  // 4 ints
     for (int ii = 0; ii < ntile; ii++) {
       const int i = first + ii;
@@ -501,8 +509,10 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(BAR(B_DQEMPTY));
-      if (leader) bulk_wait_read0();  // previous reductions finished reading the staging rows
+      // the reduction issued two tiles ago has finished reading this staging buffer
+      if (leader) bulk_wait_read1();
       named_bar_sync(1, 128);
+      uint8_t* stg = stg0 + (ii & 1) * DQS_BYTES;
       if (esz == 4) {
 #pragma unroll
         for (int q = 0; q < 64; q++) reinterpret_cast<float*>(stg + q * rowb)[d] = v[q] * mult;
@@ -513,15 +523,10 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       fence_async_smem();
       named_bar_sync(1, 128);
       if (leader) {
-        for (int q = 0; q < 64; q++) {
-          const int qq = i * QT + q;
-          if (qq >= lq) break;
-          uint8_t* gdst = static_cast<uint8_t*>(a.dq_acc) + ((sq0 + qq) * a.H + h) * rowb;
-          if (esz == 4)
-            bulk_reduce_add_f32(gdst, base + OFF_DQS + q * rowb, rowb);
-          else
-            bulk_reduce_add_f16(gdst, base + OFF_DQS + q * rowb, rowb);
-        }
+        // one tiled reduce-add of the 64 x 128 partial; rows past the sequence
+        // hold exact zeros (their dS is zero) and rows past the tensor are clipped
+        tma_reduce_add_3d(&a.tm_dqacc, base + OFF_DQS + (ii & 1) * DQS_BYTES, 0, h,
+                          int(sq0 + int64_t(i) * QT));
         bulk_commit();
       }
     }
