@@ -111,6 +111,18 @@ __device__ __forceinline__ void bulk_reduce_add_f16(void* dst, uint32_t src, uin
       "r"(src), "r"(bytes)
       : "memory");
 }
+// Tiled tensor reduce-add shared -> global (element type from the map).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -273,6 +285,14 @@ __device__ __forceinline__ uint32_t e8m0_from_amax(float amax) {
 // s <= 253 keeps it a normal number.
 __device__ __forceinline__ float e8m0_inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
+}
+// Packed fp32 pair multiply (one f32x2 instruction), round to nearest.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
 }
 // Two fp32 -> E4M3 (round to nearest even, saturate to +-448): lo byte = a.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
