@@ -48,7 +48,12 @@ constexpr int OFF_SFQ = OFF_SF;
 constexpr int OFF_SFK = OFF_SFQ + 512;
 constexpr int OFF_SFV = OFF_SFK + NS * 512;
 constexpr int OFF_SFP = OFF_SFV + NS * 512;
-constexpr int OFF_BAR = OFF_SFP + 2 * 512;
+constexpr int NWG = 2;               // softmax warpgroups sharing each S tile
+constexpr int W = 128 / NWG;         // key columns per warpgroup
+constexpr int NB = W / 32;           // P blocks per thread
+constexpr int OFF_RED = OFF_SFP + 2 * 512;             // row maxima [2][NWG][128], sums [NWG][128]
+constexpr int OFF_VOTE = OFF_RED + 3 * NWG * 128 * 4;  // exit votes [3][NWG*4]
+constexpr int OFF_BAR = OFF_VOTE + 3 * NWG * 4 * 4;
 // barriers: q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done, teardown
 constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -56,7 +61,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
 constexpr uint32_t COL_S0 = 0, COL_O = 256, COL_SFQ = 384, COL_SFK = 388, COL_SFV = 396,
                    COL_SFP = 404;
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 128 + NWG * 128;
 }  // namespace fwd
 
 __device__ __forceinline__ float ex2(float x) {
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(BAR(B_SFULL + b), 1);
-      mbar_init(BAR(B_PFULL + b), 128);
+      mbar_init(BAR(B_PFULL + b), NWG * 128);
     }
     mbar_init(BAR(B_ODONE), 1);
     mbar_init(BAR(B_TEAR), 1);
@@ -220,134 +225,177 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int row = tid - 128;          // query row in the tile = TMEM lane
+    // NWG warpgroups share each 128 x 128 S tile: warpgroup g owns key columns
+    // [g*W, (g+1)*W) of every row (thread = query row = TMEM lane).  They
+    // exchange their partial row maxima once per tile; each keeps its own
+    // partial row sum, writes its own P columns and rescales its own O columns.
+    // Every exit decision is a vote read after a barrier all of them reach, so
+    // they always leave together.
+    const int gw = (warp - 4) >> 2;
+    const int wi = warp - 4;                       // softmax warp index
+    const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    const int qpos = qt * TILE + row;   // position in the sequence
+    const int qpos = qt * TILE + row;
     const float sl2 = a.scale_log2;
+    const int c0 = gw * W;
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);            // [2][NWG][128]
+    volatile int* vote = reinterpret_cast<volatile int*>(smem + OFF_VOTE);  // [2][NWG*4]
     float m = -INFINITY, l = 0.0f;
-    bool ok = true;
+    bool failed = false, ok = true;
     for (int j = 0; j < nkv; j++) {
       const int b = j & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + b), (j >> 1) & 1, abort_flag, &g_status_fwd))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t* su = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-        for (int c = 0; c < 4; c++) tmem_ld32(tmem + lane_base + COL_S0 + 128 * b + 32 * c, su + 32 * c);
-        tmem_wait_ld();
-      }
-      const int kbase = j * TILE;
-      const bool need_mask = (kbase + TILE > lk) || (a.causal && kbase + TILE - 1 > qpos);
+      const bool okw = !failed &&
+          __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + b), (j >> 1) & 1, abort_flag, &g_status_fwd));
+      float s[W];
+      float bm[NB];
+      float pm = -INFINITY;
+      const int kbase = j * TILE + c0;
       const int klim = a.causal ? min(lk, qpos + 1) : lk;  // keys < klim are visible
+      if (okw) {
+        tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 128; i++) {
-        s[i] = __fmul_rn(s[i], sl2);
-        if (need_mask && kbase + i >= klim) s[i] = -INFINITY;
-      }
-      float bm[4];
+        for (int c = 0; c < W / 32; c++)
+          tmem_ld32(tmem + lane_base + COL_S0 + 128 * b + c0 + 32 * c, reinterpret_cast<uint32_t*>(s) + 32 * c);
+        tmem_wait_ld();
+        const bool need_mask = (kbase + W > lk) || (a.causal && kbase + W - 1 > qpos);
 #pragma unroll
-      for (int kb = 0; kb < 4; kb++) {
-        float x = s[32 * kb];
-#pragma unroll
-        for (int i = 1; i < 32; i += 2) {
-          float y;
-          if (i + 1 < 32) {
-            asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(x), "f"(s[32 * kb + i]), "f"(s[32 * kb + i + 1]));
-          } else {
-            y = fmaxf(x, s[32 * kb + i]);
-          }
-          x = y;
+        for (int i = 0; i < W; i += 2) {
+          const float2 t = fmul2(make_float2(s[i], s[i + 1]), make_float2(sl2, sl2));
+          s[i] = t.x;
+          s[i + 1] = t.y;
         }
-        bm[kb] = x;
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < W; i++)
+            if (kbase + i >= klim) s[i] = -INFINITY;
+        }
+#pragma unroll
+        for (int kb = 0; kb < NB; kb++) {
+          float x = s[32 * kb];
+#pragma unroll
+          for (int i = 1; i < 31; i += 2)
+            asm("max.f32 %0, %1, %2, %3;" : "=f"(x) : "f"(x), "f"(s[32 * kb + i]), "f"(s[32 * kb + i + 1]));
+          bm[kb] = fmaxf(x, s[32 * kb + 31]);
+          pm = fmaxf(pm, bm[kb]);
+        }
       }
-      const float mt = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+      red[(b * NWG + gw) * 128 + row] = pm;
+      if (lane == 0) vote[b * (NWG * 4) + wi] = okw ? 1 : 0;
+      named_bar_sync(2, NWG * 128);
+      bool all_ok = true;
+#pragma unroll
+      for (int v = 0; v < NWG * 4; v++) all_ok = all_ok && vote[b * (NWG * 4) + v] != 0;
+      if (!all_ok) { ok = false; break; }
+      float mt = red[(b * NWG + 0) * 128 + row];
+#pragma unroll
+      for (int g2 = 1; g2 < NWG; g2++) mt = fmaxf(mt, red[(b * NWG + g2) * 128 + row]);
       const float mn = fmaxf(m, mt);
       const float mu = (m == -INFINITY || __fsub_rn(mn, m) > kRescaleThr) ? mn : m;
       const float mref = mu == -INFINITY ? 0.0f : mu;
       const float alpha = ex2(__fsub_rn(m, mref));
       const bool rescale = (m != -INFINITY) && (mu > m);
-      float rs = 0.0f;
+      float rs0 = 0.0f, rs1 = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 128; i++) {
+      for (int i = 0; i < W; i += 2) {
         s[i] = ex2(__fsub_rn(s[i], mref));
-        rs += s[i];
+        s[i + 1] = ex2(__fsub_rn(s[i + 1], mref));
+        rs0 += s[i];
+        rs1 += s[i + 1];
       }
-      l = l * alpha + rs;
+      l = l * alpha + (rs0 + rs1);
       // P -> E4M3 with one E8M0 scale per 32 keys; the block maximum of P is
       // 2^(block max of s' - m), so no second pass over the elements.
-      uint32_t pw[32];
+      uint32_t pw[W / 4];
       uint32_t sfw = 0;
 #pragma unroll
-      for (int kb = 0; kb < 4; kb++) {
+      for (int kb = 0; kb < NB; kb++) {
         const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(bm[kb], mref)));
         sfw |= sc << (8 * kb);
         const float inv = e8m0_inv_scale(sc);
 #pragma unroll
         for (int c = 0; c < 8; c++) {
           const float* p = s + 32 * kb + 4 * c;
-          pw[8 * kb + c] = pack4_e4m3(p[0] * inv, p[1] * inv, p[2] * inv, p[3] * inv);
+          const float2 x01 = fmul2(make_float2(p[0], p[1]), make_float2(inv, inv));
+          const float2 x23 = fmul2(make_float2(p[2], p[3]), make_float2(inv, inv));
+          pw[8 * kb + c] = cvt_e4m3x2(x01.x, x01.y) | (cvt_e4m3x2(x23.x, x23.y) << 16);
         }
       }
       // O must hold PV(j-1) before it is rescaled and before PV(j) is issued
       if (j >= 1 &&
           !__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (j - 1) & 1, abort_flag, &g_status_fwd))) {
-        ok = false;
-        break;
+        failed = true;  // leave at the next vote, together with the others
+        m = mu;
+        continue;
       }
       tc_fence_after();
       if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
+        for (int c = 0; c < W / 32; c++) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + COL_O + 32 * c, o);
+          tmem_ld32(tmem + lane_base + COL_O + c0 + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(tmem + lane_base + COL_O + 32 * c, o);
-          tmem_st16(tmem + lane_base + COL_O + 32 * c + 16, o + 16);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 t = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                   make_float2(alpha, alpha));
+            o[i] = __float_as_uint(t.x);
+            o[i + 1] = __float_as_uint(t.y);
+          }
+          tmem_st16(tmem + lane_base + COL_O + c0 + 32 * c, o);
+          tmem_st16(tmem + lane_base + COL_O + c0 + 32 * c + 16, o + 16);
         }
       }
-      tmem_st16(tmem + lane_base + COL_S0 + 128 * b, pw);
-      tmem_st16(tmem + lane_base + COL_S0 + 128 * b + 16, pw + 16);
-      *reinterpret_cast<uint32_t*>(smem + OFF_SFP + b * 512 + (row & 31) * 16 + (row >> 5) * 4) = sfw;
+#pragma unroll
+      for (int c = 0; c < W / 4; c += 16)
+        tmem_st16(tmem + lane_base + COL_S0 + 128 * b + c0 / 4 + c, pw + c);
+      uint8_t* atom = smem + OFF_SFP + b * 512 + (row & 31) * 16 + (row >> 5) * 4 + gw * NB;
+#pragma unroll
+      for (int kb = 0; kb < NB; kb++) atom[kb] = uint8_t(sfw >> (8 * kb));
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(BAR(B_PFULL + b));
       m = mu;
     }
-    // ---- epilogue: O / l -> bf16, LSE
-    if (ok && nkv > 0 &&
-        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (nkv - 1) & 1, abort_flag, &g_status_fwd))) {
-      tc_fence_after();
-      const bool valid = qpos < lq;
-      const float rl = 1.0f / l;
-      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128;
+    // ---- epilogue: O / l -> bf16 (each warpgroup its own columns), LSE
+    const bool okf = ok && !failed && nkv > 0 &&
+        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (nkv - 1) & 1, abort_flag, &g_status_fwd));
+    float* lsum = red + 2 * NWG * 128;  // [NWG][128]
+    lsum[gw * 128 + row] = l;
+    if (lane == 0) vote[2 * (NWG * 4) + wi] = okf ? 1 : 0;
+    named_bar_sync(2, NWG * 128);
+    bool all_ok = true;
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
+    for (int v = 0; v < NWG * 4; v++) all_ok = all_ok && vote[2 * (NWG * 4) + v] != 0;
+    if (all_ok) {
+      tc_fence_after();
+      float lt = lsum[row];
+#pragma unroll
+      for (int g2 = 1; g2 < NWG; g2++) lt += lsum[g2 * 128 + row];
+      const bool valid = qpos < lq;
+      const float rl = 1.0f / lt;
+      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128 + c0;
+#pragma unroll
+      for (int c = 0; c < W / 32; c++) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + COL_O + 32 * c, o);
+        tmem_ld32(tmem + lane_base + COL_O + c0 + 32 * c, o);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; v4++) {
-            uint32_t w[4];
+            uint32_t w4[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
               __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[8 * v4 + 2 * e]) * rl,
                                                         __uint_as_float(o[8 * v4 + 2 * e + 1]) * rl);
-              w[e] = *reinterpret_cast<uint32_t*>(&p2);
+              w4[e] = *reinterpret_cast<uint32_t*>(&p2);
             }
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
       }
-      if (valid) {
-        const float lse = (m + log2f(l)) * 0.69314718055994530942f;
+      if (valid && gw == 0) {
+        const float lse = (m + log2f(lt)) * 0.69314718055994530942f;
         if (a.dense_lse)
           a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + qpos] = lse;
         else
