@@ -139,7 +139,7 @@ class GpuStep:
         self.o = torch.empty((B * S, H, D), **bf)
         self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
         self.dq, self.dk, self.dv = (torch.empty((B * S, H, D), **bf) for _ in range(3))
-        self.ws = torch.empty(mx.mxfa_bwd_workspace_size(B * S, H, D, 0), **u8)
+        self.ws = torch.empty(mx.mxfa_bwd_workspace_size(B * S, B, H, D, 0), **u8)
         self.host_out = [torch.empty((B * S, H, D), dtype=torch.bfloat16).pin_memory()
                          for _ in range(4)]
         self.scale = 1.0 / math.sqrt(D)
@@ -261,7 +261,8 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     out = (o, lse)
     t_jf = time_loop(torch, lambda: mx.attention_fwd(qR, kR, vC, sq, sk, 1 / math.sqrt(D), False,
                                                      out=out), iters, warmup)
-    ws = torch.empty(mx.mxfa_bwd_workspace_size(sq.total, Hj, D, 0), dtype=torch.uint8, device=dev)
+    ws = torch.empty(mx.mxfa_bwd_workspace_size(sq.total, sq.nseq, Hj, D, 0), dtype=torch.uint8,
+                     device=dev)
     grads = tuple(torch.empty_like(t) for t in (o, o, o))
     grads = (grads[0], torch.empty((sk.total, Hj, D), dtype=torch.bfloat16, device=dev),
              torch.empty((sk.total, Hj, D), dtype=torch.bfloat16, device=dev))

@@ -155,9 +155,12 @@ mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
                             int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
                             int causal, void* o, float* lse, mxfa_stream_t stream);
 
-/* Workspace of the backward pass: Delta (fp32 [H][total_q]) followed by the
- * dQ accumulator ([total_q][H][128], fp32 when dq_mode = 0, fp16 when 1). */
-size_t mxfa_bwd_workspace_size(int64_t total_q, int H, int D, int dq_mode);
+/* Workspace of the backward pass for total_q query tokens in nseq sequences:
+ * one 2560-byte record per (64-query tile, head) -- the tile's scale atoms,
+ * lse * log2(e) and Delta = rowsum(dO * O) -- for at most
+ * ceil(total_q / 64) + nseq tiles, followed by the dQ accumulator
+ * ([total_q][H][128], fp32 when dq_mode = 0, fp16 when 1). */
+size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_mode);
 
 /* mxfa_bwd -- dense backward, five GEMMs with recompute ([TMEM], [ITEMS] 6).
  *  q, k, dO   SQ-quantized payload + packed SQ scales (32x32 blocks serve

@@ -74,6 +74,13 @@ mxfa_status from_cuda(cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Backward tile records: 2560 bytes per (64-query tile, head); sum over
+// sequences of ceil(len / 64) is at most ceil(total / 64) + nseq.
+size_t bwd_records_bytes(int64_t total_q, int nseq, int H) {
+  const size_t n = size_t(ceil_div(total_q, 64) + nseq) * size_t(H) * 2560u;
+  return (n + 255) & ~size_t(255);
+}
+
 // Shared checks of a sequence description.
 mxfa_status check_seqs(const int32_t* cu, int nseq, int maxlen, int64_t tokens) {
   if (nseq <= 0 || maxlen < 0 || tokens < 0) return MXFA_ERR_INVALID_ARG;
@@ -144,7 +151,8 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
     return MXFA_ERR_MISALIGNED;
   if (ptq <= 0 || ptk <= 0) return MXFA_ERR_INVALID_ARG;
   if (!ws) return MXFA_ERR_INVALID_ARG;
-  if (ws_bytes < mxfa_bwd_workspace_size(total_q, H, D, dq_mode)) return MXFA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < mxfa_bwd_workspace_size(total_q, sq.nseq, H, D, dq_mode))
+    return MXFA_ERR_WORKSPACE_TOO_SMALL;
   if (total_q == 0 || total_k == 0) return MXFA_OK;
   BwdArgs a;
   memset(&a, 0, sizeof(a));
@@ -172,9 +180,8 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
-  a.delta = static_cast<float*>(ws);
-  const size_t delta_bytes = ((size_t(total_q) * H * 4) + 255) & ~size_t(255);
-  a.dq_acc = static_cast<uint8_t*>(ws) + delta_bytes;
+  a.rec = static_cast<uint8_t*>(ws);
+  a.dq_acc = static_cast<uint8_t*>(ws) + bwd_records_bytes(total_q, sq.nseq, H);
   if (!make_map_acc(&a.tm_dqacc, a.dq_acc, total_q, H, dq_mode == 1)) return MXFA_ERR_CUDA;
   a.dense_lse = dense ? 1 : 0;
   a.lse_hstride = dense ? sq.seqlen : total_q;
@@ -288,10 +295,9 @@ mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
                     ptk, H, D, softmax_scale, causal, o, lse, false, stream);
 }
 
-size_t mxfa_bwd_workspace_size(int64_t total_q, int H, int D, int dq_mode) {
-  if (total_q < 0 || H <= 0 || D <= 0) return 0;
-  const size_t delta_bytes = ((size_t(total_q) * H * 4) + 255) & ~size_t(255);
-  return delta_bytes + size_t(total_q) * H * D * (dq_mode == 1 ? 2u : 4u);
+size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_mode) {
+  if (total_q < 0 || nseq <= 0 || H <= 0 || D <= 0) return 0;
+  return bwd_records_bytes(total_q, nseq, H) + size_t(total_q) * H * D * (dq_mode == 1 ? 2u : 4u);
 }
 
 mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,

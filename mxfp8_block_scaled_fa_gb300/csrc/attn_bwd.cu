@@ -39,8 +39,12 @@ static __device__ unsigned g_status_bwd;
 namespace bwd {
 constexpr int KT = 128;                 // keys per CTA
 constexpr int QT = 64;                  // queries per inner tile
-constexpr int NSQ = 2;                  // Q / dO ring stages
-constexpr int NSF = 4;                  // per-tile scale-atom / lse / Delta ring stages
+constexpr int NSQ = 3;                  // Q / dO / tile-record ring stages
+// Per (64-query tile, head) record written by the preparation kernel:
+// four scale atoms (Q and dO, rows = queries; dO and Q, rows = d) and the
+// tile's lse * log2(e) and Delta.
+constexpr int REC_SFQ = 0, REC_SFDO = 512, REC_SFDOT = 1024, REC_SFQT = 1536, REC_LSE2 = 2048,
+              REC_DELTA = 2304, REC_BYTES = 2560;
 constexpr int KV_BYTES = KT * 128;      // 16 KB
 constexpr int QD_BYTES = QT * 128;      // 8 KB
 constexpr int PS_BYTES = KT * QT;       // 8 KB (128 rows x 64 B)
@@ -53,18 +57,16 @@ constexpr int OFF_PT = OFF_DO + NSQ * QD_BYTES;         // 2 buffers, SW64
 constexpr int OFF_DST = OFF_PT + 2 * PS_BYTES;          // 2 buffers, SW64
 constexpr int DQS_BYTES = QT * 512;                    // one dQ staging tile (fp32)
 constexpr int OFF_DQS = OFF_DST + 2 * PS_BYTES;         // dQ staging, 2 tiles
-constexpr int OFF_ATOM = OFF_DQS + 2 * DQS_BYTES;
+constexpr int OFF_REC = OFF_DQS + 2 * DQS_BYTES;       // NSQ tile records
+constexpr int OFF_ATOM = OFF_REC + NSQ * REC_BYTES;
 // scale atoms (512 B each)
 constexpr int A_SFK = 0, A_SFV = 1, A_SFKT = 2;
-constexpr int A_SFQ = 3, A_SFDO = A_SFQ + NSF, A_SFDOT = A_SFDO + NSF,
-              A_SFQT = A_SFDOT + NSF;                     // x NSF (ring stage)
-constexpr int A_SFPT = A_SFQT + NSF, A_SFDST = A_SFPT + 2, A_SFDS = A_SFDST + 2;  // x2
+constexpr int A_SFPT = 3, A_SFDST = A_SFPT + 2, A_SFDS = A_SFDST + 2;  // x2
 constexpr int NATOM = A_SFDS + 2;
-constexpr int OFF_LD = OFF_ATOM + NATOM * 512;          // lse*log2e, Delta: NSF x 2 x 64 floats
-constexpr int OFF_BAR = OFF_LD + NSF * 2 * QT * 4;
+constexpr int OFF_BAR = OFF_ATOM + NATOM * 512;
 enum {
-  B_KVFULL = 0, B_KCONST, B_QDOFULL, B_QDOEMPTY = B_QDOFULL + NSQ, B_SFINFULL = B_QDOEMPTY + NSQ,
-  B_SFINEMPTY = B_SFINFULL + NSF, B_SDPFULL = B_SFINEMPTY + NSF, B_SDPFREE, B_PFULL,
+  B_KVFULL = 0, B_KCONST, B_QDOFULL, B_QDOEMPTY = B_QDOFULL + NSQ,
+  B_SDPFULL = B_QDOEMPTY + NSQ, B_SDPFREE, B_PFULL,
   B_PDSEMPTY = B_PFULL + 2, B_DQFULL = B_PDSEMPTY + 2, B_DQEMPTY, B_KVDONE, B_TEAR, NBAR
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -78,25 +80,70 @@ constexpr int NTHREADS = 512;
 }  // namespace bwd
 
 // ------------------------------------------------------------ pre / post
-// Delta[h][t] = sum_d dO[t,h,d] * O[t,h,d] (fp32 from bf16), one warp per row.
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
-                                                      const uint16_t* __restrict__ dout,
-                                                      float* __restrict__ delta, int64_t rows,
-                                                      int H, int64_t total) {
-  const int64_t r = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const uint2 ov = *reinterpret_cast<const uint2*>(o + r * 128 + lane * 4);
-  const uint2 dv = *reinterpret_cast<const uint2*>(dout + r * 128 + lane * 4);
-  auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
-  auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-  float s = lo(ov.x) * lo(dv.x) + hi(ov.x) * hi(dv.x) + lo(ov.y) * lo(dv.y) + hi(ov.y) * hi(dv.y);
+// Tile records.  One CTA (256 threads) per (64-query tile of a sequence, head):
+//   Delta[r] = sum_d dO[r,d] * O[r,d] (fp32 from bf16, warp per row),
+//   lse2[r]  = lse[r] * log2(e)  (+inf past the sequence end: P = 2^-inf = 0),
+//   the four scale atoms of the tile built from the packed square scales of
+//   Q and dO: rows = queries (for S^T and dP^T) and rows = d (for dK and dV).
+// Atom word w (bytes 4w..4w+3) holds row (w & 3) * 32 + (w >> 2), k-blocks
+// 0..3 in its bytes; a square-scale entry holds byte 4 * tb + db.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
+  using namespace bwd;
+  const int t = blockIdx.x, h = blockIdx.y, g = blockIdx.z;
+  int64_t s0;
+  int L;
+  seq_info(a.sq, g, s0, L);
+  if (t * QT >= L) return;
+  const int64_t t128 = seq_units_before(a.sq, g, 128) + t / 2;
+  if (t128 >= a.ptiles_q) {
+    atomicOr(&g_status_bwd, DEV_BAD_INDEX);
+    return;
+  }
+  uint8_t* rec = a.rec + ((seq_units_before(a.sq, g, QT) + t) * a.H + h) * REC_BYTES;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* delta = reinterpret_cast<float*>(rec + REC_DELTA);
+  for (int r = warp * 8; r < warp * 8 + 8; r++) {
+    const int q = t * QT + r;
+    float d = 0.0f;
+    if (q < L) {
+      const int64_t off = ((s0 + q) * a.H + h) * 128 + lane * 4;
+      const uint2 ov = *reinterpret_cast<const uint2*>(a.o + off);
+      const uint2 dv = *reinterpret_cast<const uint2*>(a.dout + off);
+      auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+      auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+      d = lo(ov.x) * lo(dv.x) + hi(ov.x) * hi(dv.x) + lo(ov.y) * lo(dv.y) + hi(ov.y) * hi(dv.y);
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-  if (lane == 0) {
-    const int64_t t = r / H;
-    const int h = int(r % H);
-    delta[int64_t(h) * total + t] = s;
+      for (int off2 = 16; off2 >= 1; off2 >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off2);
+    }
+    if (lane == 0) delta[r] = d;
+  }
+  if (tid < QT) {
+    const int q = t * QT + tid;
+    float l2 = INFINITY;
+    if (q < L) {
+      const float lse = a.dense_lse ? a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + q]
+                                    : a.lse[int64_t(h) * a.lse_hstride + s0 + q];
+      l2 = lse * 1.4426950408889634f;
+    }
+    reinterpret_cast<float*>(rec + REC_LSE2)[tid] = l2;
+  }
+  const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + (t128 * a.H + h) * 16));
+  const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + (t128 * a.H + h) * 16));
+  auto pick = [](uint4 e, int tb) { return tb == 0 ? e.x : tb == 1 ? e.y : tb == 2 ? e.z : e.w; };
+  const int tb0 = (t & 1) * 2;
+  if (tid < 128) {
+    const int w = tid, rg = w & 3;
+    uint32_t* aq = reinterpret_cast<uint32_t*>(rec + REC_SFQ);
+    uint32_t* ad = reinterpret_cast<uint32_t*>(rec + REC_SFDO);
+    aq[w] = rg < 2 ? pick(q4, tb0 + rg) : 0x7F7F7F7Fu;   // rows = queries, k = d-blocks
+    ad[w] = rg < 2 ? pick(d4, tb0 + rg) : 0x7F7F7F7Fu;
+  } else {
+    const int w = tid - 128, rg = w & 3;               // rows = d (block rg), k = query blocks
+    const uint32_t sh = 8u * uint32_t(rg);
+    uint32_t* aqt = reinterpret_cast<uint32_t*>(rec + REC_SFQT);
+    uint32_t* adt = reinterpret_cast<uint32_t*>(rec + REC_SFDOT);
+    aqt[w] = ((pick(q4, tb0) >> sh) & 0xFFu) | (((pick(q4, tb0 + 1) >> sh) & 0xFFu) << 8) | 0x7F7F0000u;
+    adt[w] = ((pick(d4, tb0) >> sh) & 0xFFu) | (((pick(d4, tb0 + 1) >> sh) & 0xFFu) << 8) | 0x7F7F0000u;
   }
 }
 
@@ -181,13 +228,13 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
   const int first = a.causal ? min(nq, (kt * KT) / QT) : 0;
   const int ntile = nq - first;
   const int64_t tq_base = seq_units_before(a.sq, g, 128);
+  const int64_t tq64 = seq_units_before(a.sq, g, QT);  // first tile record of this sequence
   const int64_t tk = seq_units_before(a.sk, g, 128) + kt;
 
   const uint32_t bar0 = base + OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
   auto ATOM = [&](int i) { return smem + OFF_ATOM + 512 * i; };
   auto ATOMA = [&](int i) { return base + OFF_ATOM + 512u * uint32_t(i); };
-  float* ld_stage = reinterpret_cast<float*>(smem + OFF_LD);  // [NSF][2: lse2, delta][64]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);
 
@@ -198,10 +245,6 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     for (int s = 0; s < NSQ; s++) {
       mbar_init(BAR(B_QDOFULL + s), 1);
       mbar_init(BAR(B_QDOEMPTY + s), 1);
-    }
-    for (int f = 0; f < NSF; f++) {
-      mbar_init(BAR(B_SFINFULL + f), 64);
-      mbar_init(BAR(B_SFINEMPTY + f), 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(BAR(B_PFULL + b), 256);
@@ -251,17 +294,19 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           break;
         issued = ii + 1;
         const uint32_t fb = BAR(B_QDOFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * QD_BYTES);
+        mbar_arrive_expect_tx(fb, 2 * QD_BYTES + REC_BYTES);
         const int qrow = int(sq0 + int64_t(i) * QT);
         tma_load_3d(base + OFF_Q + s * QD_BYTES, &a.tm_q, fb, 0, h, qrow);
         tma_load_3d(base + OFF_DO + s * QD_BYTES, &a.tm_do, fb, 0, h, qrow);
+        bulk_load(base + OFF_REC + s * REC_BYTES, a.rec + ((tq64 + i) * a.H + h) * REC_BYTES,
+                  REC_BYTES, fb);
       }
       for (int ii = max(0, issued - NSQ); ii < issued; ii++)
         bwait_raw(BAR(B_QDOFULL + ii % NSQ), (ii / NSQ) & 1);
       bwait_raw(BAR(B_KVFULL), 0);
     }
   } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------ scale-atom builder
+    // ------------------------------------------------ key-tile scale atoms
     // Atom word w (bytes 4w..4w+3) holds row r = (w & 3) * 32 + (w >> 2),
     // k-blocks 0..3 in its bytes.  Square scale entry: byte 4 * tb + db.
     const int t = tid - 64;
@@ -283,39 +328,6 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     }
     fence_async_smem();
     mbar_arrive(BAR(B_KCONST));
-    const float l2e = 1.4426950408889634f;
-    for (int ii = 0; ii < ntile; ii++) {
-      const int i = first + ii, f = ii % NSF;
-      if (ii >= NSF &&
-          !mbar_wait(BAR(B_SFINEMPTY + f), ((ii / NSF) - 1) & 1, abort_flag, &g_status_bwd))
-        break;
-      const int64_t ent = ((tq_base + i / 2) * a.H + h) * 16;
-      const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + ent));
-      const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + ent));
-      const int tb0 = (i & 1) * 2;
-      for (int w = t; w < 128; w += 64) {
-        const int rg = w & 3;  // row group = 32-row block of the atom
-        reinterpret_cast<uint32_t*>(ATOM(A_SFQ + f))[w] = rg < 2 ? pick(q4, tb0 + rg) : 0x7F7F7F7Fu;
-        reinterpret_cast<uint32_t*>(ATOM(A_SFDO + f))[w] = rg < 2 ? pick(d4, tb0 + rg) : 0x7F7F7F7Fu;
-        reinterpret_cast<uint32_t*>(ATOM(A_SFQT + f))[w] = col_bytes(q4, rg, tb0, false);
-        reinterpret_cast<uint32_t*>(ATOM(A_SFDOT + f))[w] = col_bytes(d4, rg, tb0, false);
-      }
-      {
-        const int c = t;  // query column of the tile
-        const int q = i * QT + c;
-        float l2 = INFINITY, dl = 0.0f;  // queries past the end: P = 2^-inf = 0
-        if (q < lq) {
-          const float lse = a.dense_lse ? a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + q]
-                                        : a.lse[int64_t(h) * a.lse_hstride + sq0 + q];
-          l2 = lse * l2e;
-          dl = a.delta[int64_t(h) * a.total_q + sq0 + q];
-        }
-        ld_stage[(f * 2 + 0) * QT + c] = l2;
-        ld_stage[(f * 2 + 1) * QT + c] = dl;
-      }
-      fence_async_smem();
-      mbar_arrive(BAR(B_SFINFULL + f));
-    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -333,14 +345,15 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       }
       // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T for local tile jj
       auto grads = [&](int jj) -> bool {
-        const int s = jj % NSQ, b = jj & 1, f = jj % NSF;
+        const int s = jj % NSQ, b = jj & 1;
+        const uint32_t rec = base + OFF_REC + s * REC_BYTES;
         if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_bwd)) return false;
         if (jj >= 1 && !mbar_wait(BAR(B_DQEMPTY), (jj - 1) & 1, abort_flag, &g_status_bwd)) return false;
         tc_fence_after();
         cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
-        cp_sf(COL_SFDOT + 4 * b, ATOMA(A_SFDOT + f));
+        cp_sf(COL_SFDOT + 4 * b, rec + REC_SFDOT);
         cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
-        cp_sf(COL_SFQT + 4 * b, ATOMA(A_SFQT + f));
+        cp_sf(COL_SFQT + 4 * b, rec + REC_SFQT);
         cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
         const uint32_t pt = base + OFF_PT + b * PS_BYTES, dst = base + OFF_DST + b * PS_BYTES;
         const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
@@ -360,22 +373,20 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
                       smem_desc(dst + 2048 * k, 8192, 512, 4), idesc_mxf8(128, 64, 1, 1, k, k),
                       tmem + COL_SFKT, tmem + COL_SFDS + 4 * b, k > 0 ? 1u : 0u);
         tc_commit(BAR(B_QDOEMPTY + s));
-        tc_commit(BAR(B_SFINEMPTY + f));
         tc_commit(BAR(B_PDSEMPTY + b));
         tc_commit(BAR(B_DQFULL));
         return true;
       };
       for (int ii = 0; ok && ii < ntile; ii++) {
-        const int s = ii % NSQ, f = ii % NSF;
+        const int s = ii % NSQ;
         if (!mbar_wait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag, &g_status_bwd) ||
-            !mbar_wait(BAR(B_SFINFULL + f), (ii / NSF) & 1, abort_flag, &g_status_bwd) ||
             (ii >= 1 && !mbar_wait(BAR(B_SDPFREE), (ii - 1) & 1, abort_flag, &g_status_bwd))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        cp_sf(COL_SFQ, ATOMA(A_SFQ + f));
-        cp_sf(COL_SFDO, ATOMA(A_SFDO + f));
+        cp_sf(COL_SFQ, base + OFF_REC + s * REC_BYTES + REC_SFQ);
+        cp_sf(COL_SFDO, base + OFF_REC + s * REC_BYTES + REC_SFDO);
         const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
 #pragma unroll
         for (int k = 0; k < 4; k++)
@@ -414,10 +425,14 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(BAR(B_SDPFREE));
-      const int f = ii % NSF;
-      if (!wwait(BAR(B_SFINFULL + f), (ii / NSF) & 1, abort_flag)) { ok = false; break; }
-      const float* l2 = ld_stage + (f * 2 + 0) * QT + 32 * hq;
-      const float* dl = ld_stage + (f * 2 + 1) * QT + 32 * hq;
+      // lse2 / Delta of the tile: in the stage's record (its QDOFULL completed
+      // before the MMA issued S^T, which this warpgroup has already waited on;
+      // waiting on it here makes the record visible to these threads)
+      const int s = ii % NSQ;
+      if (!wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag)) { ok = false; break; }
+      const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
+      const float* l2 = reinterpret_cast<const float*>(rec + REC_LSE2) + 32 * hq;
+      const float* dl = reinterpret_cast<const float*>(rec + REC_DELTA) + 32 * hq;
       const int q0 = i * QT + 32 * hq;
       float pmax = 0.0f, dsmax = 0.0f;
 #pragma unroll
@@ -552,7 +567,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
   const size_t esz = a.dq_mode == 1 ? 2 : 4;
   cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, size_t(rows) * 128 * esz, st);
   if (e != cudaSuccess) return e;
-  bwd_pre_kernel<<<unsigned((rows + 7) / 8), 256, 0, st>>>(a.o, a.dout, a.delta, rows, a.H, a.total_q);
+  {
+    dim3 pg(unsigned((a.sq.seqlen + bwd::QT - 1) / bwd::QT), unsigned(a.H), unsigned(a.sq.nseq));
+    if (pg.x > 0) bwd_prep_kernel<<<pg, 256, 0, st>>>(a);
+  }
   dim3 grid;
   if (a.sk.cu == nullptr) {
     const int nkt = (a.sk.seqlen + bwd::KT - 1) / bwd::KT;

@@ -55,7 +55,7 @@ extern "C" mxfa_status mxfa_bwd_noalloc(const mxfa_mx* q, const mxfa_mx* k, cons
                                         float dq_static_scale, void* dq, void* dk, void* dv,
                                         mxfa_stream_t stream) {
   if (B <= 0 || S <= 0 || H <= 0 || D <= 0) return MXFA_ERR_INVALID_ARG;
-  const size_t need = mxfa_bwd_workspace_size(int64_t(B) * S, H, D, dq_mode);
+  const size_t need = mxfa_bwd_workspace_size(int64_t(B) * S, B, H, D, dq_mode);
   if (need == 0) return MXFA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return MXFA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = scratch_on_current_device();

@@ -90,7 +90,7 @@ struct BwdArgs {
   int dq_mode;        // 0 fp32 accumulation, 1 fp16 with static scale
   float dq_static_scale;
   uint16_t *dq, *dk, *dv;  // bf16 outputs
-  float* delta;            // workspace [H][total_q]
+  uint8_t* rec;            // workspace: one record per (64-query tile, head)
   void* dq_acc;            // workspace [total_q][H][128] fp32 or fp16
   int64_t lse_hstride;
   int dense_lse;

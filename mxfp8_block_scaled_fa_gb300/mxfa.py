@@ -64,7 +64,7 @@ def lib() -> ctypes.CDLL:
             "mxfa_fwd": (I, [P, P, P, I, I, I, I, F, I, P, P, P]),
             "mxfa_varlen_fwd": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P, P,
                                     P]),
-            "mxfa_bwd_workspace_size": (S, [I64, I, I, I]),
+            "mxfa_bwd_workspace_size": (S, [I64, I, I, I, I]),
             "mxfa_bwd": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P, S, P]),
             "mxfa_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I,
                                     F, I, I, F, P, P, P, P, S, P]),
@@ -132,8 +132,8 @@ def mxfa_varlen_fwd(q, k, v, cu_q, cu_k, nseq, max_sq, max_sk, total_q, total_k,
            "mxfa_varlen_fwd")
 
 
-def mxfa_bwd_workspace_size(total_q, H, D, dq_mode) -> int:
-    return int(lib().mxfa_bwd_workspace_size(total_q, H, D, dq_mode))
+def mxfa_bwd_workspace_size(total_q, nseq, H, D, dq_mode) -> int:
+    return int(lib().mxfa_bwd_workspace_size(total_q, nseq, H, D, dq_mode))
 
 
 def mxfa_bwd(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, dq_mode, dq_static, dq, dk,
@@ -278,7 +278,7 @@ def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Ten
     """Backward on quantized operands -> (dQ, dK, dV) bf16."""
     H, D = q.data.shape[-2], q.data.shape[-1]
     dev = q.data.device
-    wsb = mxfa_bwd_workspace_size(seqs_q.total, H, D, dq_mode)
+    wsb = mxfa_bwd_workspace_size(seqs_q.total, seqs_q.nseq, H, D, dq_mode)
     if ws is None:
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
     if out is None:

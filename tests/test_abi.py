@@ -52,9 +52,10 @@ def test_packed_tiles_and_sizes(lib):
     assert mxfa.mxfa_packed_tiles(cu, 3, 0) == 1 + 1 + 2
     assert lib.mxfa_sf_packed_bytes(0, 10, 4) == 10 * 4 * 512
     assert lib.mxfa_sf_packed_bytes(2, 10, 4) == 10 * 4 * 16
-    ws = mxfa.mxfa_bwd_workspace_size(1000, 8, 128, 0)
-    assert ws >= 1000 * 8 * 4 + 1000 * 8 * 128 * 4
-    assert mxfa.mxfa_bwd_workspace_size(1000, 8, 128, 1) < ws
+    ws = mxfa.mxfa_bwd_workspace_size(1000, 3, 8, 128, 0)
+    assert ws >= (16 + 3) * 8 * 2560 + 1000 * 8 * 128 * 4
+    assert mxfa.mxfa_bwd_workspace_size(1000, 3, 8, 128, 1) < ws
+    assert mxfa.mxfa_bwd_workspace_size(1000, 0, 8, 128, 0) == 0
 
 
 def _out(data=0x1000, sfc=0x2000, sfp=0x3000):
@@ -86,7 +87,7 @@ def test_attention_argument_checks(lib):
     assert f(r(m), r(m), r(m), 1, 256, 2, 128, -1.0, 0, 0x4000, 0x5000, None) == 1  # scale
     assert f(None, r(m), r(m), 1, 256, 2, 128, 0.1, 0, 0x4000, 0x5000, None) == 1
     b = lib.mxfa_bwd
-    ws = mxfa.mxfa_bwd_workspace_size(256, 2, 128, 0)
+    ws = mxfa.mxfa_bwd_workspace_size(256, 1, 2, 128, 0)
     args = lambda mode, st, wsb: (r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, 1, 256, 2, 128,
                                   0.1, 0, mode, st, 0x7000, 0x8000, 0x9000, 0xA000, wsb, None)
     assert b(*args(0, 1.0, ws - 1)) == 4           # workspace too small
