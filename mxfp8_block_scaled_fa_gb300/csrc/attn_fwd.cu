@@ -258,12 +258,6 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
           tmem_ld32(tmem + lane_base + COL_S0 + 128 * b + c0 + 32 * c, reinterpret_cast<uint32_t*>(s) + 32 * c);
         tmem_wait_ld();
         const bool need_mask = (kbase + W > lk) || (a.causal && kbase + W - 1 > qpos);
-#pragma unroll
-        for (int i = 0; i < W; i += 2) {
-          const float2 t = fmul2(make_float2(s[i], s[i + 1]), make_float2(sl2, sl2));
-          s[i] = t.x;
-          s[i + 1] = t.y;
-        }
         if (need_mask) {
 #pragma unroll
           for (int i = 0; i < W; i++)
@@ -286,40 +280,43 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
 #pragma unroll
       for (int v = 0; v < NWG * 4; v++) all_ok = all_ok && vote[b * (NWG * 4) + v] != 0;
       if (!all_ok) { ok = false; break; }
+      // raw-score maxima; fl(max S * sl2) = max fl(S * sl2) since sl2 > 0
       float mt = red[(b * NWG + 0) * 128 + row];
 #pragma unroll
       for (int g2 = 1; g2 < NWG; g2++) mt = fmaxf(mt, red[(b * NWG + g2) * 128 + row]);
+      mt = __fmul_rn(mt, sl2);
       const float mn = fmaxf(m, mt);
       const float mu = (m == -INFINITY || __fsub_rn(mn, m) > kRescaleThr) ? mn : m;
       const float mref = mu == -INFINITY ? 0.0f : mu;
       const float alpha = ex2(__fsub_rn(m, mref));
       const bool rescale = (m != -INFINITY) && (mu > m);
-      float rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < W; i += 2) {
-        s[i] = ex2(__fsub_rn(s[i], mref));
-        s[i + 1] = ex2(__fsub_rn(s[i + 1], mref));
-        rs0 += s[i];
-        rs1 += s[i + 1];
-      }
-      l = l * alpha + (rs0 + rs1);
-      // P -> E4M3 with one E8M0 scale per 32 keys; the block maximum of P is
-      // 2^(block max of s' - m), so no second pass over the elements.
+      // P -> E4M3, one E8M0 scale per 32 keys.  The block maximum of P~ is
+      // 2^(fl(block max S * sl2) - m) (no second pass over the elements); with
+      // its exponent X, each element is put on the E4M3 scale directly as
+      // 2^fma(S, sl2, -fl(m + X)) and converted, and the row sum adds
+      // 2^X * (block sum).
       uint32_t pw[W / 4];
       uint32_t sfw = 0;
+      float lt = 0.0f;
 #pragma unroll
       for (int kb = 0; kb < NB; kb++) {
-        const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(bm[kb], mref)));
+        const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(__fmul_rn(bm[kb], sl2), mref)));
         sfw |= sc << (8 * kb);
-        const float inv = e8m0_inv_scale(sc);
+        const float nmx = -__fadd_rn(mref, float(int(sc) - 127));
+        float2 rs = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 8; c++) {
-          const float* p = s + 32 * kb + 4 * c;
-          const float2 x01 = fmul2(make_float2(p[0], p[1]), make_float2(inv, inv));
-          const float2 x23 = fmul2(make_float2(p[2], p[3]), make_float2(inv, inv));
+          float* p = s + 32 * kb + 4 * c;
+          const float2 a01 = ffma2(make_float2(p[0], p[1]), make_float2(sl2, sl2), make_float2(nmx, nmx));
+          const float2 a23 = ffma2(make_float2(p[2], p[3]), make_float2(sl2, sl2), make_float2(nmx, nmx));
+          const float2 x01 = make_float2(ex2(a01.x), ex2(a01.y));
+          const float2 x23 = make_float2(ex2(a23.x), ex2(a23.y));
+          rs = fadd2(rs, fadd2(x01, x23));
           pw[8 * kb + c] = cvt_e4m3x2(x01.x, x01.y) | (cvt_e4m3x2(x23.x, x23.y) << 16);
         }
+        lt += (rs.x + rs.y) * e8m0_value(sc);
       }
+      l = l * alpha + lt;
       // O must hold PV(j-1) before it is rescaled and before PV(j) is issued
       if (j >= 1 &&
           !__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (j - 1) & 1, abort_flag, &g_status_fwd))) {

@@ -294,6 +294,27 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
   return *reinterpret_cast<float2*>(&r);
 }
+// Packed fp32 pair fused multiply-add a * b + c (one rounding per element).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+// Packed fp32 pair add.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+// 2^(s - 127) for an E8M0 byte s in [0, 254] as fp32 (2^-127 is subnormal).
+__device__ __forceinline__ float e8m0_value(uint32_t s) {
+  return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
 // Two fp32 -> E4M3 (round to nearest even, saturate to +-448): lo byte = a.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
   uint16_t r;

@@ -252,6 +252,24 @@ static double flush_fp32_subnormal(double p) {
   return p < ldexp(1.0, -126) ? 0.0 : p;
 }
 
+/* Quantize-dequantize one 32-key block of P in the kernel's fp32 steps: the
+ * shared exponent X comes from the block maximum of p (the unscaled fp32
+ * P~), and each element enters E4M3 as fl(2^fma(S, sl2, -fl(m + X))), which
+ * is P~ * 2^-X computed with one rounding of the exponent argument. */
+static void qdq_block_fp32(double* p, const float* s32, float m, float sl2f) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; i++)
+    if (p[i] > amax) amax = p[i];
+  int X = (int)mxo_e8m0_from_amax(amax) - 127;
+  volatile float mX = m + (float)X;
+  for (int i = 0; i < 32; i++) {
+    volatile float arg = fmaf(s32[i], sl2f, -mX);
+    volatile float pq = (float)exp2((double)arg);
+    double v = flush_fp32_subnormal((double)pq);
+    p[i] = mxo_e4m3_decode(mxo_e4m3_encode(v)) * ldexp(1.0, X);
+  }
+}
+
 /* ------------------------------------------------------------------ */
 /* Attention forward ([KDIM] paragraphs 1-2, [BITS])                   */
 /* ------------------------------------------------------------------ */
@@ -273,7 +291,10 @@ static double flush_fp32_subnormal(double p) {
  * score_fp32 = 0 is the fp64 definition.  score_fp32 = 1 takes the values
  * that decide quantization codes in fp32, the kernel's precision: S rounded
  * to fp32 (the MMA accumulator), s' = fl(S * fl(scale * log2 e)), the running
- * maximum test and s' - m in fp32, and P~ rounded to fp32. */
+ * maximum test in fp32, P~ = fl(2^fl(s' - m)) for the row sum and the block
+ * maxima, and, for each 32-key block with shared exponent X taken from its
+ * maximum, the value put on the E4M3 scale as fl(2^fma(S, fl(scale * log2 e),
+ * -fl(m + X))) -- one fused multiply-add, no separate scaling multiply. */
 void mxo_attn_fwd(const double* q, const double* k, const double* v,
                   const int32_t* cu_q, const int32_t* cu_k, int nseq, int H,
                   int D, double scale, int causal, int quant_p, int tile_n,
@@ -288,6 +309,7 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
 #pragma omp parallel
   {
     double* sp = (double*)malloc(sizeof(double) * (size_t)tile_n);
+    float* s32 = (float*)malloc(sizeof(float) * (size_t)tile_n);
     double* acc = (double*)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 16)
     for (int64_t w = 0; w < total_q * H; w++) {
@@ -311,7 +333,8 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
               double s = 0.0;
               for (int d = 0; d < D; d++) s += qi[d] * kj[d];
               if (score_fp32) { /* S, s' rounded to fp32 like the MMA and kernel */
-                volatile float t = (float)s * sl2f;
+                s32[j] = (float)s;
+                volatile float t = s32[j] * sl2f;
                 sp[j] = t;
               } else {
                 sp[j] = s * scale * log2e;
@@ -319,6 +342,7 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
               if (sp[j] > mt) mt = sp[j];
             } else {
               sp[j] = -INFINITY;
+              s32[j] = -INFINITY;
             }
           }
           double mn = mt > m ? mt : m;
@@ -333,7 +357,12 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
             l += sp[j];
           }
           if (quant_p)
-            for (int64_t b = 0; b < tile_n; b += 32) qdq_block(sp + b, 32, 1);
+            for (int64_t b = 0; b < tile_n; b += 32) {
+              if (score_fp32)
+                qdq_block_fp32(sp + b, s32 + b, (float)m, sl2f);
+              else
+                qdq_block(sp + b, 32, 1);
+            }
           for (int64_t j = 0; j < nt; j++) {
             if (sp[j] == 0.0) continue;
             const double* vj = v + ((k0 + t0 + j) * H + h) * D;
@@ -346,6 +375,7 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
       }
     }
     free(sp);
+    free(s32);
     free(acc);
   }
   free(seq_of);
