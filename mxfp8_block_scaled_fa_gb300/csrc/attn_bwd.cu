@@ -330,13 +330,24 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     mbar_arrive(BAR(B_KCONST));
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the schedule so that descriptors and TMEM addresses
+    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
+    {
+      const bool issuer = lane == 0;
+      const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
+      };
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
         const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + col), "l"(d) : "memory");
+        if (issuer)
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
       };
-      bool ok = mbar_wait(BAR(B_KVFULL), 0, abort_flag, &g_status_bwd) &&
-                mbar_wait(BAR(B_KCONST), 0, abort_flag, &g_status_bwd);
+      // descriptor bases (start-address field advanced by byte offset >> 4)
+      const uint64_t dK_k = smem_desc(base + OFF_K, 16, 1024, 2);       // K, K-major (S^T A)
+      const uint64_t dV_k = smem_desc(base + OFF_V, 16, 1024, 2);       // V, K-major (dP^T A)
+      const uint64_t dK_mn = smem_desc(base + OFF_K, 8192, 1024, 2);    // K^T, MN-major (dQ^T A)
+      bool ok = wait_all(BAR(B_KVFULL), 0) && wait_all(BAR(B_KCONST), 0);
       tc_fence_after();
       if (ok) {
         cp_sf(COL_SFK, ATOMA(A_SFK));
@@ -347,64 +358,75 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       auto grads = [&](int jj) -> bool {
         const int s = jj % NSQ, b = jj & 1;
         const uint32_t rec = base + OFF_REC + s * REC_BYTES;
-        if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_bwd)) return false;
-        if (jj >= 1 && !mbar_wait(BAR(B_DQEMPTY), (jj - 1) & 1, abort_flag, &g_status_bwd)) return false;
+        if (!wait_all(BAR(B_PFULL + b), (jj >> 1) & 1)) return false;
+        if (jj >= 1 && !wait_all(BAR(B_DQEMPTY), (jj - 1) & 1)) return false;
         tc_fence_after();
         cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
         cp_sf(COL_SFDOT + 4 * b, rec + REC_SFDOT);
         cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
         cp_sf(COL_SFQT + 4 * b, rec + REC_SFQT);
         cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
-        const uint32_t pt = base + OFF_PT + b * PS_BYTES, dst = base + OFF_DST + b * PS_BYTES;
-        const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
+        const uint64_t dPt = smem_desc(base + OFF_PT + b * PS_BYTES, 16, 512, 4);
+        const uint64_t dSt_k = smem_desc(base + OFF_DST + b * PS_BYTES, 16, 512, 4);
+        const uint64_t dSt_mn = smem_desc(base + OFF_DST + b * PS_BYTES, 8192, 512, 4);
+        const uint64_t dQ_mn = smem_desc(base + OFF_Q + s * QD_BYTES, 8192, 1024, 2);
+        const uint64_t dDO_mn = smem_desc(base + OFF_DO + s * QD_BYTES, 8192, 1024, 2);
+        if (issuer) {
 #pragma unroll
-        for (int k = 0; k < 2; k++) {
-          const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
-          mma_mxf8_ss(tmem + COL_DV, smem_desc(pt + 32 * k, 16, 512, 4),
-                      smem_desc(dos + 4096 * k, 8192, 1024, 2), idesc_mxf8(128, 128, 0, 1, k, k),
-                      tmem + COL_SFPT + 4 * b, tmem + COL_SFDOT + 4 * b, acc);
-          mma_mxf8_ss(tmem + COL_DK, smem_desc(dst + 32 * k, 16, 512, 4),
-                      smem_desc(qs + 4096 * k, 8192, 1024, 2), idesc_mxf8(128, 128, 0, 1, k, k),
-                      tmem + COL_SFDST + 4 * b, tmem + COL_SFQT + 4 * b, acc);
+          for (int k = 0; k < 2; k++) {
+            const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
+            mma_mxf8_ss(tm + COL_DV, dPt + uint64_t(2 * k), dDO_mn + uint64_t(256 * k),
+                        idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFPT + 4 * b, tm + COL_SFDOT + 4 * b,
+                        acc);
+            mma_mxf8_ss(tm + COL_DK, dSt_k + uint64_t(2 * k), dQ_mn + uint64_t(256 * k),
+                        idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFDST + 4 * b, tm + COL_SFQT + 4 * b,
+                        acc);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ss(tm + COL_DQ, dK_mn + uint64_t(256 * k), dSt_mn + uint64_t(128 * k),
+                        idesc_mxf8(128, 64, 1, 1, k, k), tm + COL_SFKT, tm + COL_SFDS + 4 * b,
+                        k > 0 ? 1u : 0u);
+          tc_commit(BAR(B_QDOEMPTY + s));
+          tc_commit(BAR(B_PDSEMPTY + b));
+          tc_commit(BAR(B_DQFULL));
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_mxf8_ss(tmem + COL_DQ, smem_desc(base + OFF_K + 4096 * k, 8192, 1024, 2),
-                      smem_desc(dst + 2048 * k, 8192, 512, 4), idesc_mxf8(128, 64, 1, 1, k, k),
-                      tmem + COL_SFKT, tmem + COL_SFDS + 4 * b, k > 0 ? 1u : 0u);
-        tc_commit(BAR(B_QDOEMPTY + s));
-        tc_commit(BAR(B_PDSEMPTY + b));
-        tc_commit(BAR(B_DQFULL));
+        __syncwarp();
         return true;
       };
       for (int ii = 0; ok && ii < ntile; ii++) {
         const int s = ii % NSQ;
-        if (!mbar_wait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag, &g_status_bwd) ||
-            (ii >= 1 && !mbar_wait(BAR(B_SDPFREE), (ii - 1) & 1, abort_flag, &g_status_bwd))) {
+        if (!wait_all(BAR(B_QDOFULL + s), (ii / NSQ) & 1) ||
+            (ii >= 1 && !wait_all(BAR(B_SDPFREE), (ii - 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
         cp_sf(COL_SFQ, base + OFF_REC + s * REC_BYTES + REC_SFQ);
         cp_sf(COL_SFDO, base + OFF_REC + s * REC_BYTES + REC_SFDO);
-        const uint32_t qs = base + OFF_Q + s * QD_BYTES, dos = base + OFF_DO + s * QD_BYTES;
+        const uint64_t dQ_k = smem_desc(base + OFF_Q + s * QD_BYTES, 16, 1024, 2);
+        const uint64_t dDO_k = smem_desc(base + OFF_DO + s * QD_BYTES, 16, 1024, 2);
+        if (issuer) {
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_mxf8_ss(tmem + COL_S, smem_desc(base + OFF_K + 32 * k, 16, 1024, 2),
-                      smem_desc(qs + 32 * k, 16, 1024, 2), idesc_mxf8(128, 64, 0, 0, k, k),
-                      tmem + COL_SFK, tmem + COL_SFQ, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ss(tm + COL_S, dK_k + uint64_t(2 * k), dQ_k + uint64_t(2 * k),
+                        idesc_mxf8(128, 64, 0, 0, k, k), tm + COL_SFK, tm + COL_SFQ, k > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_mxf8_ss(tmem + COL_DP, smem_desc(base + OFF_V + 32 * k, 16, 1024, 2),
-                      smem_desc(dos + 32 * k, 16, 1024, 2), idesc_mxf8(128, 64, 0, 0, k, k),
-                      tmem + COL_SFV, tmem + COL_SFDO, k > 0 ? 1u : 0u);
-        tc_commit(BAR(B_SDPFULL));
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ss(tm + COL_DP, dV_k + uint64_t(2 * k), dDO_k + uint64_t(2 * k),
+                        idesc_mxf8(128, 64, 0, 0, k, k), tm + COL_SFV, tm + COL_SFDO, k > 0 ? 1u : 0u);
+          tc_commit(BAR(B_SDPFULL));
+        }
+        __syncwarp();
         if (ii >= 1 && !grads(ii - 1)) { ok = false; break; }
       }
       if (ok && ntile > 0) grads(ntile - 1);
-      tc_commit(BAR(B_KVDONE));
-      tc_commit(BAR(B_TEAR));
-      bwait_raw(BAR(B_TEAR), 0);
+      if (issuer) {
+        tc_commit(BAR(B_KVDONE));
+        tc_commit(BAR(B_TEAR));
+        bwait_raw(BAR(B_TEAR), 0);
+      }
+      __syncwarp();
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS

@@ -176,52 +176,66 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
     }
   } else if (warp == 1 && !bad_tiles) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idS[4] = {idesc_mxf8(128, 128, 0, 0, 0, 0), idesc_mxf8(128, 128, 0, 0, 1, 1),
-                               idesc_mxf8(128, 128, 0, 0, 2, 2), idesc_mxf8(128, 128, 0, 0, 3, 3)};
-      const uint32_t idP[4] = {idesc_mxf8(128, 128, 0, 1, 0, 0), idesc_mxf8(128, 128, 0, 1, 1, 1),
-                               idesc_mxf8(128, 128, 0, 1, 2, 2), idesc_mxf8(128, 128, 0, 1, 3, 3)};
-      bool ok = mbar_wait(BAR(B_QFULL), 0, abort_flag, &g_status_fwd);
-      tc_fence_after();
+    // The whole warp walks the schedule so that descriptors and TMEM addresses
+    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
+    {
+      const bool issuer = lane == 0;
+      const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_fwd));
+      };
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
         const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + col), "l"(d) : "memory");
+        if (issuer)
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
       };
+      const uint64_t dQ = smem_desc(base + OFF_Q, 16, 1024, 2);
       auto issue_pv = [&](int jj) -> bool {
         const int s = jj % NS, b = jj & 1;
-        if (!mbar_wait(BAR(B_PFULL + b), (jj >> 1) & 1, abort_flag, &g_status_fwd)) return false;
+        if (!wait_all(BAR(B_PFULL + b), (jj >> 1) & 1)) return false;
         tc_fence_after();
         cp_sf(COL_SFP + 4 * b, base + OFF_SFP + b * 512);
         cp_sf(COL_SFV + 4 * b, base + OFF_SFV + s * 512);
-        const uint32_t vb = base + OFF_V + s * TILE_BYTES;
+        const uint64_t dV = smem_desc(base + OFF_V + s * TILE_BYTES, 8192, 1024, 2);
+        if (issuer) {
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_mxf8_ts(tmem + COL_O, tmem + COL_S0 + 128 * b + 8 * k,
-                      smem_desc(vb + 4096 * k, 8192, 1024, 2), idP[k], tmem + COL_SFP + 4 * b,
-                      tmem + COL_SFV + 4 * b, (jj > 0 || k > 0) ? 1u : 0u);
-        tc_commit(BAR(B_KVEMPTY + s));
-        tc_commit(BAR(B_ODONE));
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ts(tm + COL_O, tm + COL_S0 + 128 * b + 8 * k, dV + uint64_t(256 * k),
+                        idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFP + 4 * b, tm + COL_SFV + 4 * b,
+                        (jj > 0 || k > 0) ? 1u : 0u);
+          tc_commit(BAR(B_KVEMPTY + s));
+          tc_commit(BAR(B_ODONE));
+        }
+        __syncwarp();
         return true;
       };
+      bool ok = wait_all(BAR(B_QFULL), 0);
+      tc_fence_after();
       if (ok) cp_sf(COL_SFQ, base + OFF_SFQ);
       for (int j = 0; ok && j < nkv; j++) {
         const int s = j % NS, b = j & 1;
-        if (!mbar_wait(BAR(B_KVFULL + s), (j / NS) & 1, abort_flag, &g_status_fwd)) { ok = false; break; }
+        if (!wait_all(BAR(B_KVFULL + s), (j / NS) & 1)) { ok = false; break; }
         tc_fence_after();
         cp_sf(COL_SFK + 4 * b, base + OFF_SFK + s * 512);
-        const uint32_t kb = base + OFF_K + s * TILE_BYTES;
+        const uint64_t dK = smem_desc(base + OFF_K + s * TILE_BYTES, 16, 1024, 2);
+        if (issuer) {
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_mxf8_ss(tmem + COL_S0 + 128 * b, smem_desc(base + OFF_Q + 32 * k, 16, 1024, 2),
-                      smem_desc(kb + 32 * k, 16, 1024, 2), idS[k], tmem + COL_SFQ,
-                      tmem + COL_SFK + 4 * b, k > 0 ? 1u : 0u);
-        tc_commit(BAR(B_SFULL + b));
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ss(tm + COL_S0 + 128 * b, dQ + uint64_t(2 * k), dK + uint64_t(2 * k),
+                        idesc_mxf8(128, 128, 0, 0, k, k), tm + COL_SFQ, tm + COL_SFK + 4 * b,
+                        k > 0 ? 1u : 0u);
+          tc_commit(BAR(B_SFULL + b));
+        }
+        __syncwarp();
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && nkv > 0) issue_pv(nkv - 1);
       // all MMAs of this CTA retired before TMEM is released
-      tc_commit(BAR(B_TEAR));
-      mbar_wait_raw(BAR(B_TEAR), 0);
+      if (issuer) {
+        tc_commit(BAR(B_TEAR));
+        mbar_wait_raw(BAR(B_TEAR), 0);
+      }
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
