@@ -42,9 +42,9 @@ constexpr int QT = 64;                  // queries per inner tile
 constexpr int NSQ = 3;                  // Q / dO / tile-record ring stages
 // Per (64-query tile, head) record written by the preparation kernel:
 // four scale atoms (Q and dO, rows = queries; dO and Q, rows = d) and the
-// tile's lse * log2(e) and Delta.
-constexpr int REC_SFQ = 0, REC_SFDO = 512, REC_SFDOT = 1024, REC_SFQT = 1536, REC_LSE2 = 2048,
-              REC_DELTA = 2304, REC_BYTES = 2560;
+// tile's -lse * log2(e) and -Delta (negated so that each enters one FMA / add).
+constexpr int REC_SFQ = 0, REC_SFDO = 512, REC_SFDOT = 1024, REC_SFQT = 1536, REC_NL2 = 2048,
+              REC_NDELTA = 2304, REC_BYTES = 2560;
 constexpr int KV_BYTES = KT * 128;      // 16 KB
 constexpr int QD_BYTES = QT * 128;      // 8 KB
 constexpr int PS_BYTES = KT * QT;       // 8 KB (128 rows x 64 B)
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   }
   uint8_t* rec = a.rec + ((seq_units_before(a.sq, g, QT) + t) * a.H + h) * REC_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* delta = reinterpret_cast<float*>(rec + REC_DELTA);
+  float* ndelta = reinterpret_cast<float*>(rec + REC_NDELTA);
   for (int r = warp * 8; r < warp * 8 + 8; r++) {
     const int q = t * QT + r;
     float d = 0.0f;
@@ -115,17 +115,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
 #pragma unroll
       for (int off2 = 16; off2 >= 1; off2 >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off2);
     }
-    if (lane == 0) delta[r] = d;
+    if (lane == 0) ndelta[r] = -d;
   }
   if (tid < QT) {
     const int q = t * QT + tid;
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;  // rows past the sequence: P = 2^-inf = 0
     if (q < L) {
       const float lse = a.dense_lse ? a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + q]
                                     : a.lse[int64_t(h) * a.lse_hstride + s0 + q];
-      l2 = lse * 1.4426950408889634f;
+      nl2 = -(lse * 1.4426950408889634f);
     }
-    reinterpret_cast<float*>(rec + REC_LSE2)[tid] = l2;
+    reinterpret_cast<float*>(rec + REC_NL2)[tid] = nl2;
   }
   const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + (t128 * a.H + h) * 16));
   const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + (t128 * a.H + h) * 16));
@@ -184,7 +184,7 @@ __device__ __forceinline__ float bex2(float x) {
 }
 __device__ __forceinline__ bool bwait_raw(uint32_t bar, uint32_t parity) {
   unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity))
     if (global_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }
@@ -338,34 +338,18 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
       };
-      auto cp_sf = [&](uint32_t col, uint32_t saddr) {
-        const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        if (issuer)
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
-      };
       // descriptor bases (start-address field advanced by byte offset >> 4)
       const uint64_t dK_k = smem_desc(base + OFF_K, 16, 1024, 2);       // K, K-major (S^T A)
       const uint64_t dV_k = smem_desc(base + OFF_V, 16, 1024, 2);       // V, K-major (dP^T A)
       const uint64_t dK_mn = smem_desc(base + OFF_K, 8192, 1024, 2);    // K^T, MN-major (dQ^T A)
-      bool ok = wait_all(BAR(B_KVFULL), 0) && wait_all(BAR(B_KCONST), 0);
+      bool ok = wait_all(BAR(B_KVFULL), 0);
       tc_fence_after();
-      if (ok) {
-        cp_sf(COL_SFK, ATOMA(A_SFK));
-        cp_sf(COL_SFV, ATOMA(A_SFV));
-        cp_sf(COL_SFKT, ATOMA(A_SFKT));
-      }
       // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T for local tile jj
       auto grads = [&](int jj) -> bool {
         const int s = jj % NSQ, b = jj & 1;
-        const uint32_t rec = base + OFF_REC + s * REC_BYTES;
         if (!wait_all(BAR(B_PFULL + b), (jj >> 1) & 1)) return false;
         if (jj >= 1 && !wait_all(BAR(B_DQEMPTY), (jj - 1) & 1)) return false;
         tc_fence_after();
-        cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
-        cp_sf(COL_SFDOT + 4 * b, rec + REC_SFDOT);
-        cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
-        cp_sf(COL_SFQT + 4 * b, rec + REC_SFQT);
-        cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
         const uint64_t dPt = smem_desc(base + OFF_PT + b * PS_BYTES, 16, 512, 4);
         const uint64_t dSt_k = smem_desc(base + OFF_DST + b * PS_BYTES, 16, 512, 4);
         const uint64_t dSt_mn = smem_desc(base + OFF_DST + b * PS_BYTES, 8192, 512, 4);
@@ -396,14 +380,12 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       };
       for (int ii = 0; ok && ii < ntile; ii++) {
         const int s = ii % NSQ;
-        if (!wait_all(BAR(B_QDOFULL + s), (ii / NSQ) & 1) ||
-            (ii >= 1 && !wait_all(BAR(B_SDPFREE), (ii - 1) & 1))) {
+        // SDPFREE completion ii: S^T / dP^T slots free and this tile's scales in TMEM
+        if (!wait_all(BAR(B_QDOFULL + s), (ii / NSQ) & 1) || !wait_all(BAR(B_SDPFREE), ii & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        cp_sf(COL_SFQ, base + OFF_REC + s * REC_BYTES + REC_SFQ);
-        cp_sf(COL_SFDO, base + OFF_REC + s * REC_BYTES + REC_SFDO);
         const uint64_t dQ_k = smem_desc(base + OFF_Q + s * QD_BYTES, 16, 1024, 2);
         const uint64_t dDO_k = smem_desc(base + OFF_DO + s * QD_BYTES, 16, 1024, 2);
         if (issuer) {
@@ -430,68 +412,146 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS
+    // These warps also write every scale slot of the tensor core into TMEM
+    // (tcgen05.st of a 512-byte atom in the replicated 32x128b x4 layout):
+    // the key tile's constant scales once, the next tile's S^T / dP^T scales
+    // as soon as S^T and dP^T of this tile are loaded, and the gradient
+    // GEMMs' scales once P and dS are quantized.  Two warps cover each lane
+    // quadrant (one per warpgroup), so the two warpgroups split the atoms.
     const int hq = (warp - 4) >> 2;            // query half of the tile
     const int r = (warp & 3) * 32 + lane;      // key row = TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int kpos = kt * KT + r;
     const bool kvalid = kpos < lk;
     const float sl2 = a.scale * 1.4426950408889634f;
-    bool ok = true;
+    auto st_atom = [&](uint32_t col, const uint8_t* atom) {
+      const uint4 v = *reinterpret_cast<const uint4*>(atom + lane * 16);
+      tmem_st4(tmem + lane_base + col, v.x, v.y, v.z, v.w);
+    };
+    bool ok = wwait(BAR(B_KVFULL), 0, abort_flag) && wwait(BAR(B_KCONST), 0, abort_flag);
+    if (ok) {
+      if (hq == 0) {
+        st_atom(COL_SFK, ATOM(A_SFK));
+        st_atom(COL_SFKT, ATOM(A_SFKT));
+      } else {
+        st_atom(COL_SFV, ATOM(A_SFV));
+      }
+      if (ntile > 0) {
+        if (wwait(BAR(B_QDOFULL), 0, abort_flag))
+          st_atom(hq == 0 ? COL_SFQ : COL_SFDO, smem + OFF_REC + (hq == 0 ? REC_SFQ : REC_SFDO));
+        else
+          ok = false;
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    mbar_arrive(BAR(B_SDPFREE));  // completion 0: scales of tile 0 in place
+    bool failed = !ok;
     for (int ii = 0; ii < ntile; ii++) {
-      const int i = first + ii, b = ii & 1;
-      if (!wwait(BAR(B_SDPFULL), ii & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
+      const int i = first + ii, b = ii & 1, s = ii % NSQ;
       float sv[32], dp[32];
-      tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
-      tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(BAR(B_SDPFREE));
-      // lse2 / Delta of the tile: in the stage's record (its QDOFULL completed
-      // before the MMA issued S^T, which this warpgroup has already waited on;
-      // waiting on it here makes the record visible to these threads)
-      const int s = ii % NSQ;
-      if (!wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag)) { ok = false; break; }
-      const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
-      const float* l2 = reinterpret_cast<const float*>(rec + REC_LSE2) + 32 * hq;
-      const float* dl = reinterpret_cast<const float*>(rec + REC_DELTA) + 32 * hq;
-      const int q0 = i * QT + 32 * hq;
-      float pmax = 0.0f, dsmax = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 32; c++) {
-        const bool vis = kvalid && !(a.causal && kpos > q0 + c);
-        // P = 2^(fl(S * scale * log2 e) - lse * log2 e), dS = P * (dP - Delta)
-        const float p = vis ? bex2(__fsub_rn(__fmul_rn(sv[c], sl2), l2[c])) : 0.0f;
-        const float ds = __fmul_rn(p, __fsub_rn(dp[c], dl[c]));
-        sv[c] = p;
-        dp[c] = ds;
-        pmax = fmaxf(pmax, p);
-        dsmax = fmaxf(dsmax, fabsf(ds));
-      }
-      // P^T: one 1x32 block along queries per thread; dS: one 32x32 block per
-      // warp, its maximum by a warp-wide absolute-maximum reduction
-      float wmax;
-      asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(dsmax));
-      const uint32_t sp = e8m0_from_amax(pmax), sd = e8m0_from_amax(wmax);
-      const float ip = e8m0_inv_scale(sp), id = e8m0_inv_scale(sd);
+      float pmax = 0.0f;
       uint32_t pw[8], dw[8];
-#pragma unroll
-      for (int c = 0; c < 8; c++) {
-        pw[c] = pack4_e4m3(sv[4 * c] * ip, sv[4 * c + 1] * ip, sv[4 * c + 2] * ip, sv[4 * c + 3] * ip);
-        dw[c] = pack4_e4m3(dp[4 * c] * id, dp[4 * c + 1] * id, dp[4 * c + 2] * id, dp[4 * c + 3] * id);
+      uint32_t sp = 0, sd = 0;
+      failed = failed || !wwait(BAR(B_SDPFULL), ii & 1, abort_flag);
+      if (!failed) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
+        tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
+        tmem_wait_ld();
+        // scales of the next tile's S^T / dP^T (their slots were read by this
+        // tile's MMAs, which have completed)
+        if (ii + 1 < ntile) {
+          const int sn = (ii + 1) % NSQ;
+          if (wwait(BAR(B_QDOFULL + sn), ((ii + 1) / NSQ) & 1, abort_flag)) {
+            const uint8_t* recn = smem + OFF_REC + sn * REC_BYTES;
+            st_atom(hq == 0 ? COL_SFQ : COL_SFDO, recn + (hq == 0 ? REC_SFQ : REC_SFDO));
+            tmem_wait_st();
+          } else {
+            failed = true;
+          }
+        }
       }
-      if (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-      uint8_t* pt = smem + OFF_PT + b * PS_BYTES;
-      uint8_t* dst = smem + OFF_DST + b * PS_BYTES;
-      *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
-      *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq + 1)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
-      const int aoff = (r & 31) * 16 + (r >> 5) * 4 + hq;      // row = key, k-block = query half
-      ATOM(A_SFPT + b)[aoff] = uint8_t(sp);
-      ATOM(A_SFDST + b)[aoff] = uint8_t(sd);
-      ATOM(A_SFDS + b)[lane * 16 + hq * 4 + (warp & 3)] = uint8_t(sd);  // row = query, k-block = key block
+      tc_fence_before();
+      mbar_arrive(BAR(B_SDPFREE));  // completion ii + 1
+      // -lse * log2 e and -Delta of the tile, from the stage's record
+      failed = failed || !wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag);
+      const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
+      if (!failed) {
+        const float2* nl2 = reinterpret_cast<const float2*>(rec + REC_NL2) + 16 * hq;
+        const float2* ndl = reinterpret_cast<const float2*>(rec + REC_NDELTA) + 16 * hq;
+        const int q0 = i * QT + 32 * hq;
+        // keys past the sequence and (causal) keys after the query: S = -inf,
+        // so that P = 2^-inf = 0 and dS = 0; only tiles on the edge need it
+        if (__any_sync(0xFFFFFFFFu, !kvalid || (a.causal && kpos > q0))) {
+#pragma unroll
+          for (int c = 0; c < 32; c++)
+            if (!kvalid || (a.causal && kpos > q0 + c)) sv[c] = -INFINITY;
+        }
+        const float2 sl2v = make_float2(sl2, sl2);
+        float dmax = 0.0f, dmin = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          // P = 2^fl(S * fl(scale * log2 e) - lse * log2 e), dS = P * (dP - Delta)
+          const float2 t = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, nl2[c / 2]);
+          const float p0 = bex2(t.x), p1 = bex2(t.y);
+          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp[c], dp[c + 1]), ndl[c / 2]));
+          sv[c] = p0;
+          sv[c + 1] = p1;
+          dp[c] = ds.x;
+          dp[c + 1] = ds.y;
+          pmax = fmax3(pmax, p0, p1);
+          dmax = fmax3(dmax, ds.x, ds.y);
+          dmin = fmin3(dmin, ds.x, ds.y);
+        }
+        // P^T: one 1x32 block along queries per thread; dS: one 32x32 block
+        // per warp, its maximum by a warp-wide absolute-maximum reduction
+        float wmax;
+        asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(fmaxf(dmax, -dmin)));
+        sp = e8m0_from_amax(pmax);
+        sd = e8m0_from_amax(wmax);
+        const float2 ip = make_float2(e8m0_inv_scale(sp), e8m0_inv_scale(sp));
+        const float2 id = make_float2(e8m0_inv_scale(sd), e8m0_inv_scale(sd));
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const float2 p01 = fmul2(make_float2(sv[4 * c], sv[4 * c + 1]), ip);
+          const float2 p23 = fmul2(make_float2(sv[4 * c + 2], sv[4 * c + 3]), ip);
+          const float2 d01 = fmul2(make_float2(dp[4 * c], dp[4 * c + 1]), id);
+          const float2 d23 = fmul2(make_float2(dp[4 * c + 2], dp[4 * c + 3]), id);
+          pw[c] = cvt_e4m3x2(p01.x, p01.y) | (cvt_e4m3x2(p23.x, p23.y) << 16);
+          dw[c] = cvt_e4m3x2(d01.x, d01.y) | (cvt_e4m3x2(d23.x, d23.y) << 16);
+        }
+      }
+      failed = failed || (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag));
+      if (!failed) {
+        uint8_t* pt = smem + OFF_PT + b * PS_BYTES;
+        uint8_t* dst = smem + OFF_DST + b * PS_BYTES;
+        *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        *reinterpret_cast<uint4*>(dst + sw64(r, 2 * hq + 1)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+        const int aoff = (r & 31) * 16 + (r >> 5) * 4 + hq;      // row = key, k-block = query half
+        ATOM(A_SFPT + b)[aoff] = uint8_t(sp);
+        ATOM(A_SFDST + b)[aoff] = uint8_t(sd);
+        ATOM(A_SFDS + b)[lane * 16 + hq * 4 + (warp & 3)] = uint8_t(sd);  // row = query, k-block = key block
+        // the B-operand scales of dV and dK come straight from the record
+        if (hq == 1) {
+          st_atom(COL_SFDOT + 4 * b, rec + REC_SFDOT);
+          st_atom(COL_SFQT + 4 * b, rec + REC_SFQT);
+        }
+      }
+      // every P / dS warp reaches this barrier, which also ANDs their outcomes:
+      // all leave together on a failure
+      if (!named_bar_and(3, 256, !failed)) { ok = false; break; }
+      if (hq == 0) {
+        st_atom(COL_SFPT + 4 * b, ATOM(A_SFPT + b));
+        st_atom(COL_SFDST + 4 * b, ATOM(A_SFDST + b));
+      } else {
+        st_atom(COL_SFDS + 4 * b, ATOM(A_SFDS + b));
+      }
+      tmem_wait_st();
       fence_async_smem();
+      tc_fence_before();
       mbar_arrive(BAR(B_PFULL + b));
     }
     // ---- dV (query half 0) and dK (query half 1): TMEM -> bf16

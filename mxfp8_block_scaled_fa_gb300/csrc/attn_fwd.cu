@@ -72,7 +72,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ bool mbar_wait_raw(uint32_t bar, uint32_t parity) {
   unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity))
     if (global_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }

@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase has not completed may sleep (up
+// to the hint, 1 ms) until it does, instead of spinning on the issue slots
+// that the working warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait on phase `parity` of an mbarrier.  Returns false (and raises
 // *abort and the status word) if the barrier has not completed within the
@@ -66,14 +79,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicOr(status, DEV_TIMEOUT);
-        return false;
-      }
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort) return false;
+    if ((i & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicOr(status, DEV_TIMEOUT);
+      return false;
     }
   }
 }
@@ -285,6 +296,28 @@ __device__ __forceinline__ uint32_t e8m0_from_amax(float amax) {
 // s <= 253 keeps it a normal number.
 __device__ __forceinline__ float e8m0_inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
+}
+// Three-input fp32 maximum / minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Named barrier `id` over `n` threads that also returns the AND of `v` over them.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 // Packed fp32 pair multiply (one f32x2 instruction), round to nearest.
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {

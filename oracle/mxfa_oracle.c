@@ -397,8 +397,9 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  *   dV_j = sum_i P^_ij dO_i;  dK_j = scale sum_i dS^_ij q_i;
  *   dQ_i = scale sum_j dS^_ij k_j.
  * score_fp32 = 1: S, dP, Delta rounded to fp32 and
- *   P = fl(2^fl(fl(S * fl(scale * log2 e)) - fl(lse * log2 e))),
- *   dS = fl(P * fl(dP - Delta)), the kernel's fp32 steps (see the forward). */
+ *   P = fl(2^fma(S, fl(scale * log2 e), -fl(lse * log2 e))) (one rounding of
+ *   the exponent argument), dS = fl(P * fl(dP - Delta)): the fp32 steps of a
+ *   kernel that evaluates the exponent with a fused multiply-add. */
 void mxo_attn_bwd(const double* q, const double* k, const double* v,
                   const double* dO, const double* o_bf, const double* do_bf,
                   const double* lse, const int32_t* cu_q, const int32_t* cu_k,
@@ -432,9 +433,8 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
             dp += doi[d] * vj[d];
           }
           if (score_fp32) { /* fp32 S, dP (MMA outputs) and fp32 elementwise steps */
-            volatile float t = (float)s * sl2f;
             volatile float l2 = (float)li * 1.4426950408889634f;
-            volatile float arg = t - l2;
+            volatile float arg = fmaf((float)s, sl2f, -l2);
             volatile float pf = (float)exp2((double)arg);
             double p = flush_fp32_subnormal((double)pf);
             volatile float diff = (float)dp - (float)delta;

@@ -269,3 +269,32 @@ def test_fp32_mode_close_to_definition(causal):
     g32 = oracle.attn_bwd(q, k, v, do, o64, do, l64, None, None, scale, causal, False, False, True)
     for a, b in zip(g32, g64):
         assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-5
+
+
+def _f32_with_product(target):
+    """An fp32 x with fl32(x * fl32(log2 e)) == target (searched near target / log2 e)."""
+    l2e = np.float32(1.4426950408889634)
+    x = np.float32(float(target) / float(l2e))
+    for step in range(64):
+        for y in (x, np.float32(x + step * np.spacing(x)), np.float32(x - step * np.spacing(x))):
+            if np.float32(y * l2e) == np.float32(target):
+                return float(y)
+    raise AssertionError("no fp32 input found")
+
+
+def test_fp32_mode_backward_exponent_rounded_once():
+    # One query, one key, D = 1: S = 4097, fl(scale * log2 e) = 1 + 2^-20 and
+    # fl(lse * log2 e) = 4097 + 2^-8.  The exact argument S * c - l is 2^-20;
+    # rounding S * c to fp32 first (ulp 2^-11 there) would give 0.  With
+    # dO = 1 and no quantization, dV = P = fl32(2^(2^-20)) for one rounding.
+    scale = _f32_with_product(1 + 2.0 ** -20)
+    lse = _f32_with_product(4097 + 2.0 ** -8)
+    q = np.full((1, 1, 1), 4097.0)
+    k = np.ones((1, 1, 1))
+    v = np.zeros((1, 1, 1))
+    do = np.ones((1, 1, 1))
+    o = np.zeros((1, 1, 1))
+    lse_a = np.full((1, 1), lse)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, o, do, lse_a, None, None, scale, False, False, False, True)
+    assert dv[0, 0, 0] == float(np.float32(2.0 ** (2.0 ** -20)))
+    assert dv[0, 0, 0] != 1.0
