@@ -16,13 +16,15 @@
 //
 // Structure: one CTA = one 128-key tile of one head, looping over 64-query
 // tiles (16 warps, 1 CTA per SM):
-//   warp 0       TMA producer: K, V (+ V scale atom) once; Q_i, dO_i ring
-//   warp 1       TMEM owner + MMA issuer (scale atoms enter TMEM by tcgen05.cp)
-//   warps 2-3    scale-atom builder: per-tile Q / dO atoms in both
-//                orientations from the packed square scales; lse, Delta
+//   warp 0       TMA producer: K, V (+ V scale atom) once; ring of Q_i, dO_i
+//                and the tile records made by the preparation kernel
+//   warp 1       TMEM owner + MMA issuer for S^T and dP^T
+//   warps 2-3    key-tile scale atoms (K, rows = keys and rows = d); warp 2
+//                then issues the gradient GEMMs (dV, dK, dQ^T)
 //   warps 4-11   P / dS: thread = key row, warpgroup 0 queries 0-31,
 //                warpgroup 1 queries 32-63 of the tile
-//   warps 12-15  dQ drain: TMEM dQ^T -> shared -> bulk reduce-add
+//   warps 12-15  dQ drain: TMEM dQ^T -> shared -> one tiled TMA reduce-add
+// Scale atoms enter TMEM by tcgen05.cp, issued by the MMA issuer that reads them.
 // TMEM columns: dV [0,128) dK [128,256) S^T [256,320) dP^T [320,384)
 //               dQ^T [384,448) scale slots [448,512).
 #include <cuda_bf16.h>
@@ -39,7 +41,7 @@ static __device__ unsigned g_status_bwd;
 namespace bwd {
 constexpr int KT = 128;                 // keys per CTA
 constexpr int QT = 64;                  // queries per inner tile
-constexpr int NSQ = 3;                  // Q / dO / tile-record ring stages
+constexpr int NSQ = 4;                  // Q / dO / tile-record ring stages
 // Per (64-query tile, head) record written by the preparation kernel:
 // four scale atoms (Q and dO, rows = queries; dO and Q, rows = d) and the
 // tile's -lse * log2(e) and -Delta (negated so that each enters one FMA / add).
@@ -66,11 +68,12 @@ constexpr int NATOM = A_SFDS + 2;
 constexpr int OFF_BAR = OFF_ATOM + NATOM * 512;
 enum {
   B_KVFULL = 0, B_KCONST, B_QDOFULL, B_QDOEMPTY = B_QDOFULL + NSQ,
-  B_SDPFULL = B_QDOEMPTY + NSQ, B_SDPFREE, B_PFULL,
-  B_PDSEMPTY = B_PFULL + 2, B_DQFULL = B_PDSEMPTY + 2, B_DQEMPTY, B_KVDONE, B_TEAR, NBAR
+  B_SDPFULL = B_QDOEMPTY + NSQ, B_SDPFREE, B_PATOM, B_PDSEMPTY = B_PATOM + 2,
+  B_DQFULL = B_PDSEMPTY + 2, B_DQEMPTY, B_KVDONE, B_TEAR, B_TEAR2, NBAR
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "backward tile exceeds the shared memory of one CTA");
 
 constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384;
 constexpr uint32_t COL_SFK = 448, COL_SFV = 452, COL_SFKT = 456, COL_SFQ = 460, COL_SFDO = 464,
@@ -81,8 +84,8 @@ constexpr int NTHREADS = 512;
 
 // ------------------------------------------------------------ pre / post
 // Tile records.  One CTA (256 threads) per (64-query tile of a sequence, head):
-//   Delta[r] = sum_d dO[r,d] * O[r,d] (fp32 from bf16, warp per row),
-//   lse2[r]  = lse[r] * log2(e)  (+inf past the sequence end: P = 2^-inf = 0),
+//   -Delta[r] with Delta[r] = sum_d dO[r,d] * O[r,d] (fp32 from bf16, warp per row),
+//   -lse[r] * log2(e)  (-inf past the sequence end: P = 2^-inf = 0),
 //   the four scale atoms of the tile built from the packed square scales of
 //   Q and dO: rows = queries (for S^T and dP^T) and rows = d (for dK and dV).
 // Atom word w (bytes 4w..4w+3) holds row (w & 3) * 32 + (w >> 2), k-blocks
@@ -147,25 +150,28 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   }
 }
 
-// dQ = bf16(acc / static_scale); acc is fp32 (mode 0) or fp16 (mode 1).
+// dQ = bf16(acc * mult): acc is fp32 holding unscaled sums (mode 0, mult =
+// softmax scale) or fp16 holding scale * static_scale times them (mode 1,
+// mult = 1 / static_scale).
 __global__ void __launch_bounds__(256) bwd_post_kernel(const void* __restrict__ acc,
                                                        uint16_t* __restrict__ dq, int64_t n,
-                                                       int mode, float inv_static) {
+                                                       int mode, float mult) {
   const int64_t i = (int64_t(blockIdx.x) * 256 + threadIdx.x) * 8;
   if (i >= n) return;
   float v[8];
   if (mode == 0) {
     const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i);
     const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    v[0] = a.x * mult; v[1] = a.y * mult; v[2] = a.z * mult; v[3] = a.w * mult;
+    v[4] = b.x * mult; v[5] = b.y * mult; v[6] = b.z * mult; v[7] = b.w * mult;
   } else {
     const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __half*>(acc) + i);
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-      v[2 * j] = f.x * inv_static;
-      v[2 * j + 1] = f.y * inv_static;
+      v[2 * j] = f.x * mult;
+      v[2 * j + 1] = f.y * mult;
     }
   }
   uint32_t w[4];
@@ -187,6 +193,12 @@ __device__ __forceinline__ bool bwait_raw(uint32_t bar, uint32_t parity) {
   while (!mbar_try_wait_sleep(bar, parity))
     if (global_ns() - t0 > kWaitLimitNs) return false;
   return true;
+}
+// One arrival for the whole warp, after every lane's prior work (each lane
+// fences its own tcgen05 / shared-memory writes before calling this).
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 // Warp-uniform bounded wait (all lanes agree on the outcome).
 __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -241,21 +253,22 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(BAR(B_KVFULL), 1);
-    mbar_init(BAR(B_KCONST), 64);
+    mbar_init(BAR(B_KCONST), 2);  // arrivals are one per warp
     for (int s = 0; s < NSQ; s++) {
       mbar_init(BAR(B_QDOFULL + s), 1);
       mbar_init(BAR(B_QDOEMPTY + s), 1);
     }
     for (int b = 0; b < 2; b++) {
-      mbar_init(BAR(B_PFULL + b), 256);
+      mbar_init(BAR(B_PATOM + b), 8);   // P / dS warps
       mbar_init(BAR(B_PDSEMPTY + b), 1);
     }
     mbar_init(BAR(B_SDPFULL), 1);
-    mbar_init(BAR(B_SDPFREE), 256);
+    mbar_init(BAR(B_SDPFREE), 8);
     mbar_init(BAR(B_DQFULL), 1);
-    mbar_init(BAR(B_DQEMPTY), 128);
+    mbar_init(BAR(B_DQEMPTY), 4);
     mbar_init(BAR(B_KVDONE), 1);
     mbar_init(BAR(B_TEAR), 1);
+    mbar_init(BAR(B_TEAR2), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -326,30 +339,41 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       reinterpret_cast<uint32_t*>(ATOM(A_SFK))[w] = pick(k4, w & 3);                 // rows = keys
       reinterpret_cast<uint32_t*>(ATOM(A_SFKT))[w] = col_bytes(k4, w & 3, 0, true);  // rows = d
     }
-    fence_async_smem();
-    mbar_arrive(BAR(B_KCONST));
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule so that descriptors and TMEM addresses
-    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
-    {
+    warp_arrive(BAR(B_KCONST), lane);
+    if (warp == 2) {
+      // -------------------------------------- MMA issuer: dV, dK, dQ^T
       const bool issuer = lane == 0;
       const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
       };
-      // descriptor bases (start-address field advanced by byte offset >> 4)
-      const uint64_t dK_k = smem_desc(base + OFF_K, 16, 1024, 2);       // K, K-major (S^T A)
-      const uint64_t dV_k = smem_desc(base + OFF_V, 16, 1024, 2);       // V, K-major (dP^T A)
+      // scale atom (512 bytes in shared memory) -> TMEM slot, replicated to the
+      // four lane quadrants; ordered before this thread's later MMAs
+      auto cp_sf = [&](uint32_t col, uint32_t saddr) {
+        const uint64_t d = smem_desc(saddr, 128, 128, 0);
+        if (issuer)
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
+      };
       const uint64_t dK_mn = smem_desc(base + OFF_K, 8192, 1024, 2);    // K^T, MN-major (dQ^T A)
-      bool ok = wait_all(BAR(B_KVFULL), 0);
+      // K (shared memory) and the K^T scale atom
+      bool ok = wait_all(BAR(B_KVFULL), 0) && wait_all(BAR(B_KCONST), 0);
       tc_fence_after();
+      cp_sf(COL_SFKT, ATOMA(A_SFKT));
       // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T for local tile jj
       auto grads = [&](int jj) -> bool {
         const int s = jj % NSQ, b = jj & 1;
-        if (!wait_all(BAR(B_PFULL + b), (jj >> 1) & 1)) return false;
-        if (jj >= 1 && !wait_all(BAR(B_DQEMPTY), (jj - 1) & 1)) return false;
+        // P^T, dS^T and their scale atoms written; the tile record in place;
+        // the dQ^T accumulator drained
+        if (!wait_all(BAR(B_PATOM + b), (jj >> 1) & 1) || !wait_all(BAR(B_QDOFULL + s), (jj / NSQ) & 1))
+          return false;
         tc_fence_after();
+        // slot b was last read by tile jj - 2's MMAs, earlier in this stream
+        const uint32_t rec = base + OFF_REC + s * REC_BYTES;
+        cp_sf(COL_SFPT + 4 * b, ATOMA(A_SFPT + b));
+        cp_sf(COL_SFDOT + 4 * b, rec + REC_SFDOT);
+        cp_sf(COL_SFDST + 4 * b, ATOMA(A_SFDST + b));
+        cp_sf(COL_SFQT + 4 * b, rec + REC_SFQT);
+        cp_sf(COL_SFDS + 4 * b, ATOMA(A_SFDS + b));
         const uint64_t dPt = smem_desc(base + OFF_PT + b * PS_BYTES, 16, 512, 4);
         const uint64_t dSt_k = smem_desc(base + OFF_DST + b * PS_BYTES, 16, 512, 4);
         const uint64_t dSt_mn = smem_desc(base + OFF_DST + b * PS_BYTES, 8192, 512, 4);
@@ -366,26 +390,73 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
                         idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFDST + 4 * b, tm + COL_SFQT + 4 * b,
                         acc);
           }
+          tc_commit(BAR(B_QDOEMPTY + s));  // Q_j and dO_j are no longer read
+        }
+        __syncwarp();
+        // dQ^T reuses one accumulator: the previous tile's must have been drained
+        if (jj >= 1 && !wait_all(BAR(B_DQEMPTY), (jj - 1) & 1)) return false;
+        tc_fence_after();
+        if (issuer) {
 #pragma unroll
           for (int k = 0; k < 4; k++)
             mma_mxf8_ss(tm + COL_DQ, dK_mn + uint64_t(256 * k), dSt_mn + uint64_t(128 * k),
                         idesc_mxf8(128, 64, 1, 1, k, k), tm + COL_SFKT, tm + COL_SFDS + 4 * b,
                         k > 0 ? 1u : 0u);
-          tc_commit(BAR(B_QDOEMPTY + s));
           tc_commit(BAR(B_PDSEMPTY + b));
           tc_commit(BAR(B_DQFULL));
         }
         __syncwarp();
         return true;
       };
+      for (int jj = 0; ok && jj < ntile; jj++) ok = grads(jj);
+      if (issuer) {
+        tc_commit(BAR(B_KVDONE));
+        tc_commit(BAR(B_TEAR2));
+        bwait_raw(BAR(B_TEAR2), 0);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer: S^T, dP^T
+    // The whole warp walks the schedule so that descriptors and TMEM addresses
+    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
+    // Scale atoms enter TMEM by tcgen05.cp in the same stream as the MMAs
+    // that read them (replicated 32x128b x4 layout: lane L, column c holds
+    // rows 32c + L % 32, k-blocks in its bytes).
+    // The gradient GEMMs have an issuer of their own (warp 2): tcgen05.mma
+    // issue stalls while the tensor pipe's queue is full, and an issuing warp
+    // shares its SM sub-partition with arithmetic-heavy warps, so two
+    // independent issue streams keep the pipe fed better than one.
+    {
+      const bool issuer = lane == 0;
+      const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+      auto wait_all = [&](uint32_t bar, uint32_t par) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
+      };
+      // descriptor bases (start-address field advanced by byte offset >> 4)
+      const uint64_t dK_k = smem_desc(base + OFF_K, 16, 1024, 2);       // K, K-major (S^T A)
+      const uint64_t dV_k = smem_desc(base + OFF_V, 16, 1024, 2);       // V, K-major (dP^T A)
+      auto cp_sf = [&](uint32_t col, uint32_t saddr) {
+        const uint64_t d = smem_desc(saddr, 128, 128, 0);
+        if (issuer)
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
+      };
+      bool ok = wait_all(BAR(B_KVFULL), 0) && wait_all(BAR(B_KCONST), 0);
+      tc_fence_after();
+      cp_sf(COL_SFK, ATOMA(A_SFK));
+      cp_sf(COL_SFV, ATOMA(A_SFV));
       for (int ii = 0; ok && ii < ntile; ii++) {
         const int s = ii % NSQ;
-        // SDPFREE completion ii: S^T / dP^T slots free and this tile's scales in TMEM
+        // completion ii of SDPFREE: the S^T / dP^T columns are free
         if (!wait_all(BAR(B_QDOFULL + s), (ii / NSQ) & 1) || !wait_all(BAR(B_SDPFREE), ii & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        // this tile's Q / dO scales; the slots were last read by the previous
+        // tile's MMAs, earlier in this stream
+        cp_sf(COL_SFQ, base + OFF_REC + s * REC_BYTES + REC_SFQ);
+        cp_sf(COL_SFDO, base + OFF_REC + s * REC_BYTES + REC_SFDO);
         const uint64_t dQ_k = smem_desc(base + OFF_Q + s * QD_BYTES, 16, 1024, 2);
         const uint64_t dDO_k = smem_desc(base + OFF_DO + s * QD_BYTES, 16, 1024, 2);
         if (issuer) {
@@ -400,11 +471,9 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           tc_commit(BAR(B_SDPFULL));
         }
         __syncwarp();
-        if (ii >= 1 && !grads(ii - 1)) { ok = false; break; }
       }
-      if (ok && ntile > 0) grads(ntile - 1);
+      // every MMA of this issuer has completed before TMEM is released
       if (issuer) {
-        tc_commit(BAR(B_KVDONE));
         tc_commit(BAR(B_TEAR));
         bwait_raw(BAR(B_TEAR), 0);
       }
@@ -412,72 +481,37 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS
-    // These warps also write every scale slot of the tensor core into TMEM
-    // (tcgen05.st of a 512-byte atom in the replicated 32x128b x4 layout):
-    // the key tile's constant scales once, the next tile's S^T / dP^T scales
-    // as soon as S^T and dP^T of this tile are loaded, and the gradient
-    // GEMMs' scales once P and dS are quantized.  Two warps cover each lane
-    // quadrant (one per warpgroup), so the two warpgroups split the atoms.
+    // Load S^T and dP^T of the tile from TMEM, free their columns, form and
+    // quantize P and dS, store P^T / dS^T (shared memory, the gradient GEMMs'
+    // A / B operands) and the scale bytes of the three computed scale atoms,
+    // then signal the gradient issuer.  No barrier among these warps.
     const int hq = (warp - 4) >> 2;            // query half of the tile
     const int r = (warp & 3) * 32 + lane;      // key row = TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int kpos = kt * KT + r;
     const bool kvalid = kpos < lk;
     const float sl2 = a.scale * 1.4426950408889634f;
-    auto st_atom = [&](uint32_t col, const uint8_t* atom) {
-      const uint4 v = *reinterpret_cast<const uint4*>(atom + lane * 16);
-      tmem_st4(tmem + lane_base + col, v.x, v.y, v.z, v.w);
-    };
-    bool ok = wwait(BAR(B_KVFULL), 0, abort_flag) && wwait(BAR(B_KCONST), 0, abort_flag);
-    if (ok) {
-      if (hq == 0) {
-        st_atom(COL_SFK, ATOM(A_SFK));
-        st_atom(COL_SFKT, ATOM(A_SFKT));
-      } else {
-        st_atom(COL_SFV, ATOM(A_SFV));
-      }
-      if (ntile > 0) {
-        if (wwait(BAR(B_QDOFULL), 0, abort_flag))
-          st_atom(hq == 0 ? COL_SFQ : COL_SFDO, smem + OFF_REC + (hq == 0 ? REC_SFQ : REC_SFDO));
-        else
-          ok = false;
-      }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    mbar_arrive(BAR(B_SDPFREE));  // completion 0: scales of tile 0 in place
-    bool failed = !ok;
+    warp_arrive(BAR(B_SDPFREE), lane);  // completion 0: S^T / dP^T columns free
+    bool ok = true;
     for (int ii = 0; ii < ntile; ii++) {
       const int i = first + ii, b = ii & 1, s = ii % NSQ;
       float sv[32], dp[32];
       float pmax = 0.0f;
       uint32_t pw[8], dw[8];
       uint32_t sp = 0, sd = 0;
-      failed = failed || !wwait(BAR(B_SDPFULL), ii & 1, abort_flag);
-      if (!failed) {
-        tc_fence_after();
-        tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
-        tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
-        tmem_wait_ld();
-        // scales of the next tile's S^T / dP^T (their slots were read by this
-        // tile's MMAs, which have completed)
-        if (ii + 1 < ntile) {
-          const int sn = (ii + 1) % NSQ;
-          if (wwait(BAR(B_QDOFULL + sn), ((ii + 1) / NSQ) & 1, abort_flag)) {
-            const uint8_t* recn = smem + OFF_REC + sn * REC_BYTES;
-            st_atom(hq == 0 ? COL_SFQ : COL_SFDO, recn + (hq == 0 ? REC_SFQ : REC_SFDO));
-            tmem_wait_st();
-          } else {
-            failed = true;
-          }
-        }
-      }
+      if (!wwait(BAR(B_SDPFULL), ii & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
+      tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
+      tmem_wait_ld();
+      reg_fence32(reinterpret_cast<uint32_t*>(sv));
+      reg_fence32(reinterpret_cast<uint32_t*>(dp));
       tc_fence_before();
-      mbar_arrive(BAR(B_SDPFREE));  // completion ii + 1
+      warp_arrive(BAR(B_SDPFREE), lane);  // completion ii + 1
       // -lse * log2 e and -Delta of the tile, from the stage's record
-      failed = failed || !wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag);
+      if (!wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag)) { ok = false; break; }
       const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
-      if (!failed) {
+      {
         const float2* nl2 = reinterpret_cast<const float2*>(rec + REC_NL2) + 16 * hq;
         const float2* ndl = reinterpret_cast<const float2*>(rec + REC_NDELTA) + 16 * hq;
         const int q0 = i * QT + 32 * hq;
@@ -522,8 +556,8 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           dw[c] = cvt_e4m3x2(d01.x, d01.y) | (cvt_e4m3x2(d23.x, d23.y) << 16);
         }
       }
-      failed = failed || (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag));
-      if (!failed) {
+      if (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      {
         uint8_t* pt = smem + OFF_PT + b * PS_BYTES;
         uint8_t* dst = smem + OFF_DST + b * PS_BYTES;
         *reinterpret_cast<uint4*>(pt + sw64(r, 2 * hq)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -534,25 +568,9 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         ATOM(A_SFPT + b)[aoff] = uint8_t(sp);
         ATOM(A_SFDST + b)[aoff] = uint8_t(sd);
         ATOM(A_SFDS + b)[lane * 16 + hq * 4 + (warp & 3)] = uint8_t(sd);  // row = query, k-block = key block
-        // the B-operand scales of dV and dK come straight from the record
-        if (hq == 1) {
-          st_atom(COL_SFDOT + 4 * b, rec + REC_SFDOT);
-          st_atom(COL_SFQT + 4 * b, rec + REC_SFQT);
-        }
       }
-      // every P / dS warp reaches this barrier, which also ANDs their outcomes:
-      // all leave together on a failure
-      if (!named_bar_and(3, 256, !failed)) { ok = false; break; }
-      if (hq == 0) {
-        st_atom(COL_SFPT + 4 * b, ATOM(A_SFPT + b));
-        st_atom(COL_SFDST + 4 * b, ATOM(A_SFDST + b));
-      } else {
-        st_atom(COL_SFDS + 4 * b, ATOM(A_SFDS + b));
-      }
-      tmem_wait_st();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(B_PFULL + b));
+      fence_async_smem();  // P^T / dS^T are read by the tensor core
+      warp_arrive(BAR(B_PATOM + b), lane);
     }
     // ---- dV (query half 0) and dK (query half 1): TMEM -> bf16
     if (__all_sync(0xFFFFFFFFu, ok) && wwait(BAR(B_KVDONE), 0, abort_flag)) {
@@ -583,36 +601,41 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain
+    // dQ^T of each tile: TMEM -> shared staging -> one tiled TMA reduce-add
+    // into the global accumulator.
     const int d = (warp & 3) * 32 + lane;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const bool leader = tid == 12 * 32;
     const int esz = a.dq_mode == 1 ? 2 : 4;
     const uint32_t rowb = 128u * esz;
+    // fp32 partials are stored unscaled (the final pass applies the softmax
+    // scale); fp16 partials carry scale * static scale to stay in range
     const float mult = a.scale * a.dq_static_scale;
     uint8_t* stg0 = smem + OFF_DQS;
-    volatile int* vote = reinterpret_cast<volatile int*>(smem + OFF_MISC + 16);  // 4 ints
-    for (int ii = 0; ii < ntile; ii++) {
-      const int i = first + ii;
-      // all four warps reach the named barrier whatever their wait returned,
-      // then leave together if any of them gave up
-      const bool okw = wwait(BAR(B_DQFULL), ii & 1, abort_flag);
-      if (lane == 0) vote[warp & 3] = okw ? 1 : 0;
-      named_bar_sync(1, 128);
-      if (!(vote[0] && vote[1] && vote[2] && vote[3])) break;
-      tc_fence_after();
+    for (int jj = 0; jj < ntile; jj++) {
+      // free the TMEM accumulator first, so that the next tile's dQ^T GEMMs
+      // can start while this one is staged and reduced
+      const bool okw = wwait(BAR(B_DQFULL), jj & 1, abort_flag);
       float v[64];
-      tmem_ld32(tmem + lane_base + COL_DQ, reinterpret_cast<uint32_t*>(v));
-      tmem_ld32(tmem + lane_base + COL_DQ + 32, reinterpret_cast<uint32_t*>(v) + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(BAR(B_DQEMPTY));
-      // the reduction issued two tiles ago has finished reading this staging buffer
+      if (okw) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + COL_DQ, reinterpret_cast<uint32_t*>(v));
+        tmem_ld32(tmem + lane_base + COL_DQ + 32, reinterpret_cast<uint32_t*>(v) + 32);
+        tmem_wait_ld();
+        reg_fence32(reinterpret_cast<uint32_t*>(v));
+        reg_fence32(reinterpret_cast<uint32_t*>(v) + 32);
+        tc_fence_before();
+        warp_arrive(BAR(B_DQEMPTY), lane);
+      }
+      // the reduction issued two tiles ago has finished reading this staging
+      // buffer; all four warps reach the barrier whatever their wait returned,
+      // and leave together if any of them gave up
       if (leader) bulk_wait_read1();
-      named_bar_sync(1, 128);
-      uint8_t* stg = stg0 + (ii & 1) * DQS_BYTES;
+      if (!named_bar_and(1, 128, okw)) break;
+      uint8_t* stg = stg0 + (jj & 1) * DQS_BYTES;
       if (esz == 4) {
 #pragma unroll
-        for (int q = 0; q < 64; q++) reinterpret_cast<float*>(stg + q * rowb)[d] = v[q] * mult;
+        for (int q = 0; q < 64; q++) reinterpret_cast<float*>(stg + q * rowb)[d] = v[q];
       } else {
 #pragma unroll
         for (int q = 0; q < 64; q++) reinterpret_cast<__half*>(stg + q * rowb)[d] = __float2half_rn(v[q] * mult);
@@ -622,8 +645,8 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       if (leader) {
         // one tiled reduce-add of the 64 x 128 partial; rows past the sequence
         // hold exact zeros (their dS is zero) and rows past the tensor are clipped
-        tma_reduce_add_3d(&a.tm_dqacc, base + OFF_DQS + (ii & 1) * DQS_BYTES, 0, h,
-                          int(sq0 + int64_t(i) * QT));
+        tma_reduce_add_3d(&a.tm_dqacc, base + OFF_DQS + (jj & 1) * DQS_BYTES, 0, h,
+                          int(sq0 + int64_t(first + jj) * QT));
         bulk_commit();
       }
     }
@@ -663,8 +686,8 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
   if (grid.x > 0 && grid.y > 0 && grid.z > 0)
     attn_bwd_kernel<<<grid, bwd::NTHREADS, bwd::SMEM_BYTES, st>>>(a);
   const int64_t n = rows * 128;
-  bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode,
-                                                               1.0f / a.dq_static_scale);
+  bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(
+      a.dq_acc, a.dq, n, a.dq_mode, a.dq_mode == 1 ? 1.0f / a.dq_static_scale : a.scale);
   return cudaPeekAtLastError();
 }
 
