@@ -10,17 +10,19 @@
 //   (bit extraction, no log or division), O += P V as a block-scaled MMA with
 //   P read from tensor memory and V scaled per 32 keys.
 //
-// Structure (one CTA = one 128-query tile of one head, 1 CTA per SM):
-//   warp 0      TMA producer: Q once; K, V tiles + their scale atoms into a
-//               3-stage shared-memory ring (mbarrier complete_tx)
-//   warp 1      TMEM owner and MMA issuer: scale atoms enter TMEM through
-//               tcgen05.cp (in issue order with the MMAs); S(j) into one of
-//               two TMEM S buffers, then O += P(j-1) V(j-1)
-//   warps 4..7  softmax: thread i owns query row i (TMEM lane i); writes
-//               P(j) over the first 32 columns of S(j) and its scales to a
-//               shared atom; rescales O in TMEM when the running max moves;
-//               final O / l and LSE
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,384) scales [384,..).
+// Structure: one CTA = two 128-query tiles (A and B) of one head, 1 CTA per
+// SM, 12 warps.  The tensor core alternates between the tiles, so that one
+// tile's softmax runs while the other tile's GEMMs execute:
+//   S_A(j), PV_B(j-1), S_B(j), PV_A(j), S_A(j+1), ...
+//   warp 0      TMA producer: Q_A, Q_B once; K, V tiles + scale atoms ring
+//   warp 1      TMEM owner and MMA issuer; scale atoms enter TMEM through
+//               tcgen05.cp in issue order with the MMAs that read them
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread =
+//               query row = TMEM lane, the whole 128-key row in registers
+// TMEM (all 512 columns): S_A [0,128) S_B [128,256) O_A [256,384)
+// O_B [384,512).  Once a tile's softmax has loaded S_X(j), the columns of S_X
+// carry P_X(j) [0,32), its scales [32,36), the V scales [36,40) (read by
+// PV_X(j)), and the Q / K scales of the other tile's next S GEMM [40,48).
 // The running max moves only when it grows by more than kRescaleThr (log2
 // units); P~ then stays below 2^kRescaleThr, which the E8M0 block scale
 // absorbs, and O and l carry the stale max exactly.
@@ -35,33 +37,34 @@ namespace mxfa {
 static __device__ unsigned g_status_fwd;
 
 namespace fwd {
-constexpr int NS = 3;  // K/V pipeline stages
+constexpr int NS = 4;  // K/V pipeline stages
 constexpr int TILE = 128;
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows x 128 E4M3
 constexpr float kRescaleThr = 8.0f;
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;
-constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
-constexpr int OFF_SF = OFF_V + NS * TILE_BYTES;
-constexpr int OFF_SFQ = OFF_SF;
-constexpr int OFF_SFK = OFF_SFQ + 512;
-constexpr int OFF_SFV = OFF_SFK + NS * 512;
-constexpr int OFF_SFP = OFF_SFV + NS * 512;
-constexpr int NWG = 2;               // softmax warpgroups sharing each S tile
-constexpr int W = 128 / NWG;         // key columns per warpgroup
-constexpr int NB = W / 32;           // P blocks per thread
-constexpr int OFF_RED = OFF_SFP + 2 * 512;             // row maxima [2][NWG][128], sums [NWG][128]
-constexpr int OFF_VOTE = OFF_RED + 3 * NWG * 128 * 4;  // exit votes [3][NWG*4]
-constexpr int OFF_BAR = OFF_VOTE + 3 * NWG * 4 * 4;
-// barriers: q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done, teardown
-constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
+constexpr int OFF_Q = 0;                               // Q_A, Q_B
+constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;          // NS stages
+constexpr int OFF_V = OFF_K + NS * TILE_BYTES;         // NS stages
+constexpr int OFF_SFQ = OFF_V + NS * TILE_BYTES;       // 2 atoms (A, B)
+constexpr int OFF_SFK = OFF_SFQ + 2 * 512;             // NS atoms
+constexpr int OFF_SFV = OFF_SFK + NS * 512;            // NS atoms
+constexpr int OFF_SFP = OFF_SFV + NS * 512;            // 2 atoms (A, B)
+constexpr int OFF_BAR = OFF_SFP + 2 * 512;
+enum {
+  B_QFULL = 0, B_KVFULL, B_KVEMPTY = B_KVFULL + NS, B_SFULL = B_KVEMPTY + NS,
+  B_SLOAD = B_SFULL + 2, B_PFULL = B_SLOAD + 2, B_ODONE = B_PFULL + 2, B_TEAR = B_ODONE + 2, NBAR
+};
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "forward tiles exceed the shared memory of one CTA");
 
-constexpr uint32_t COL_S0 = 0, COL_O = 256, COL_SFQ = 384, COL_SFK = 388, COL_SFV = 396,
-                   COL_SFP = 404;
-constexpr int NTHREADS = 128 + NWG * 128;
+constexpr uint32_t COL_S = 0, COL_O = 256;                       // + 128 * tile
+constexpr uint32_t SUB_SFP = 32, SUB_SFV = 36, SUB_SFQ = 40, SUB_SFK = 44;  // inside an S region
+constexpr int NTHREADS = 384;
+// registers per thread after the split: warps 0-3 give up, the softmax warps take
+constexpr int REG_SMALL = 64, REG_SOFTMAX = 216;
+static_assert(4 * 32 * REG_SMALL + 8 * 32 * REG_SOFTMAX <= NTHREADS * 168,
+              "register split exceeds the launch allocation");
 }  // namespace fwd
 
 __device__ __forceinline__ float ex2(float x) {
@@ -77,6 +80,13 @@ __device__ __forceinline__ bool mbar_wait_raw(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// One arrival for the whole warp, after every lane's prior work (each lane
+// fences its own tcgen05 / shared-memory writes before calling this).
+__device__ __forceinline__ void fwd_warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
@@ -85,17 +95,17 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
   uint8_t* smem = smem_raw + (base - raw_addr);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- work item
-  int g, h, qt;
-  if (a.sq.cu == nullptr) {  // dense: heavy (late) query tiles first
-    const int nqt = (a.sq.seqlen + TILE - 1) / TILE;
+  // ---- work item: (sequence g, head h, query pair qp = queries [256 qp, 256 qp + 256))
+  int g, h, qp;
+  if (a.sq.cu == nullptr) {  // dense: heavy (late) query pairs first
+    const int npair = (a.sq.seqlen + 2 * TILE - 1) / (2 * TILE);
     const int per = a.H * a.sq.nseq;
-    qt = nqt - 1 - int(blockIdx.x) / per;
+    qp = npair - 1 - int(blockIdx.x) / per;
     const int bh = int(blockIdx.x) % per;
     g = bh / a.H;
     h = bh % a.H;
   } else {
-    qt = blockIdx.x;
+    qp = blockIdx.x;
     h = blockIdx.y;
     g = blockIdx.z;
   }
@@ -103,17 +113,19 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
   int lq, lk;
   seq_info(a.sq, g, sq0, lq);
   seq_info(a.sk, g, sk0, lk);
-  if (qt * TILE >= lq) return;  // empty tile of a short sequence (before any setup)
-  int nkv = (lk + TILE - 1) / TILE;
-  if (a.causal) nkv = min(nkv, qt + 1);
-  const int64_t tq_g = seq_units_before(a.sq, g, TILE) + qt;
+  if (qp * 2 * TILE >= lq) return;  // empty pair of a short sequence (before any setup)
+  const bool has_b = qp * 2 * TILE + TILE < lq;
+  const int nkv_all = (lk + TILE - 1) / TILE;
+  // key tiles each query tile needs (causal: up to its last query)
+  int nkv[2];
+  nkv[0] = a.causal ? min(nkv_all, 2 * qp + 1) : nkv_all;
+  nkv[1] = !has_b ? 0 : a.causal ? min(nkv_all, 2 * qp + 2) : nkv_all;
+  const int nkv_max = max(nkv[0], nkv[1]);
+  const int64_t tq_g = seq_units_before(a.sq, g, TILE) + 2 * qp;  // packed tile of Q_A
   const int64_t tk_g0 = seq_units_before(a.sk, g, TILE);
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t bar0 = base + OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
-  const int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + NS, B_SFULL = 1 + 2 * NS,
-            B_PFULL = 3 + 2 * NS, B_ODONE = 5 + 2 * NS, B_TEAR = 6 + 2 * NS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8);
 
@@ -124,11 +136,12 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       mbar_init(BAR(B_KVFULL + s), 1);
       mbar_init(BAR(B_KVEMPTY + s), 1);
     }
-    for (int b = 0; b < 2; b++) {
-      mbar_init(BAR(B_SFULL + b), 1);
-      mbar_init(BAR(B_PFULL + b), NWG * 128);
+    for (int x = 0; x < 2; x++) {
+      mbar_init(BAR(B_SFULL + x), 1);
+      mbar_init(BAR(B_SLOAD + x), 4);  // one arrival per softmax warp
+      mbar_init(BAR(B_PFULL + x), 4);
+      mbar_init(BAR(B_ODONE + x), 1);
     }
-    mbar_init(BAR(B_ODONE), 1);
     mbar_init(BAR(B_TEAR), 1);
     fence_mbar_init();
   }
@@ -140,96 +153,123 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const bool bad_tiles = (tq_g >= a.ptiles_q) || (tk_g0 + nkv > a.ptiles_k);
+  const bool bad_tiles = (tq_g + (has_b ? 2 : 1) > a.ptiles_q) || (tk_g0 + nkv_all > a.ptiles_k);
   if (bad_tiles && tid == 0) {
     atomicOr(&g_status_fwd, DEV_BAD_INDEX);
     *abort_flag = 1;
   }
   __syncthreads();
-
-  if (warp == 0 && !bad_tiles) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(BAR(B_QFULL), TILE_BYTES + 512);
-      tma_load_3d(base + OFF_Q, &a.tm_q, BAR(B_QFULL), 0, h, int(sq0 + int64_t(qt) * TILE));
-      bulk_load(base + OFF_SFQ, a.sfq + (tq_g * a.H + h) * 512, 512, BAR(B_QFULL));
-      int issued = 0;
-      for (int j = 0; j < nkv; j++) {
-        const int s = j % NS, u = j / NS;
-        if (j >= NS && !mbar_wait(BAR(B_KVEMPTY + s), (u - 1) & 1, abort_flag, &g_status_fwd)) break;
-        issued = j + 1;
-        const uint32_t fb = BAR(B_KVFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 1024);
-        const int krow = int(sk0 + int64_t(j) * TILE);
-        tma_load_3d(base + OFF_K + s * TILE_BYTES, &a.tm_k, fb, 0, h, krow);
-        tma_load_3d(base + OFF_V + s * TILE_BYTES, &a.tm_v, fb, 0, h, krow);
-        const int64_t atom = ((tk_g0 + j) * a.H + h) * 512;
-        bulk_load(base + OFF_SFK + s * 512, a.sfk + atom, 512, fb);
-        bulk_load(base + OFF_SFV + s * 512, a.sfv + atom, 512, fb);
+  // register split (whole warpgroups): the softmax rows live in registers
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_SMALL));
+    if (warp == 0 && !bad_tiles) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+        mbar_arrive_expect_tx(BAR(B_QFULL), (has_b ? 2 : 1) * (TILE_BYTES + 512));
+        const int qrow = int(sq0 + int64_t(qp) * 2 * TILE);
+        tma_load_3d(base + OFF_Q, &a.tm_q, BAR(B_QFULL), 0, h, qrow);
+        bulk_load(base + OFF_SFQ, a.sfq + (tq_g * a.H + h) * 512, 512, BAR(B_QFULL));
+        if (has_b) {
+          tma_load_3d(base + OFF_Q + TILE_BYTES, &a.tm_q, BAR(B_QFULL), 0, h, qrow + TILE);
+          bulk_load(base + OFF_SFQ + 512, a.sfq + ((tq_g + 1) * a.H + h) * 512, 512, BAR(B_QFULL));
+        }
+        int issued = 0;
+        for (int j = 0; j < nkv_max; j++) {
+          const int s = j % NS, u = j / NS;
+          if (j >= NS && !mbar_wait(BAR(B_KVEMPTY + s), (u - 1) & 1, abort_flag, &g_status_fwd)) break;
+          issued = j + 1;
+          const uint32_t fb = BAR(B_KVFULL + s);
+          mbar_arrive_expect_tx(fb, 2 * TILE_BYTES + 1024);
+          const int krow = int(sk0 + int64_t(j) * TILE);
+          tma_load_3d(base + OFF_K + s * TILE_BYTES, &a.tm_k, fb, 0, h, krow);
+          tma_load_3d(base + OFF_V + s * TILE_BYTES, &a.tm_v, fb, 0, h, krow);
+          const int64_t atom = ((tk_g0 + j) * a.H + h) * 512;
+          bulk_load(base + OFF_SFK + s * 512, a.sfk + atom, 512, fb);
+          bulk_load(base + OFF_SFV + s * 512, a.sfv + atom, 512, fb);
+        }
+        // every issued copy has landed before the CTA may exit
+        for (int j = max(0, issued - NS); j < issued; j++) mbar_wait_raw(BAR(B_KVFULL + j % NS), (j / NS) & 1);
+        mbar_wait_raw(BAR(B_QFULL), 0);
       }
-      // every issued copy has landed before the CTA may exit
-      for (int j = max(0, issued - NS); j < issued; j++) mbar_wait_raw(BAR(B_KVFULL + j % NS), (j / NS) & 1);
-      mbar_wait_raw(BAR(B_QFULL), 0);
-    }
-  } else if (warp == 1 && !bad_tiles) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule so that descriptors and TMEM addresses
-    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
-    {
+    } else if (warp == 1 && !bad_tiles) {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp walks the schedule so that descriptors and TMEM addresses
+      // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
       const bool issuer = lane == 0;
       const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_fwd));
       };
+      // scale atom (shared memory) -> TMEM, replicated to the four lane quadrants
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
         const uint64_t d = smem_desc(saddr, 128, 128, 0);
         if (issuer)
           asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
       };
-      const uint64_t dQ = smem_desc(base + OFF_Q, 16, 1024, 2);
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj % NS, b = jj & 1;
-        if (!wait_all(BAR(B_PFULL + b), (jj >> 1) & 1)) return false;
+      // S_X(j) = Q_X K_j^T; its scales go into the other tile's S columns,
+      // which that tile's softmax has already loaded (or never used)
+      auto issue_s = [&](int x, int j) {
+        const int s = j % NS;
+        const uint32_t other = COL_S + 128u * uint32_t(1 - x);
+        cp_sf(other + SUB_SFQ, base + OFF_SFQ + 512 * x);
+        cp_sf(other + SUB_SFK, base + OFF_SFK + s * 512);
+        const uint64_t dQ = smem_desc(base + OFF_Q + x * TILE_BYTES, 16, 1024, 2);
+        const uint64_t dK = smem_desc(base + OFF_K + s * TILE_BYTES, 16, 1024, 2);
+        if (issuer) {
+  #pragma unroll
+          for (int k = 0; k < 4; k++)
+            mma_mxf8_ss(tm + COL_S + 128 * x, dQ + uint64_t(2 * k), dK + uint64_t(2 * k),
+                        idesc_mxf8(128, 128, 0, 0, k, k), tm + other + SUB_SFQ, tm + other + SUB_SFK,
+                        k > 0 ? 1u : 0u);
+          tc_commit(BAR(B_SFULL + x));
+        }
+        __syncwarp();
+      };
+      // O_X += P_X(j) V_j, P_X read from the S_X columns
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int s = j % NS;
+        if (!wait_all(BAR(B_PFULL + x), j & 1)) return false;
         tc_fence_after();
-        cp_sf(COL_SFP + 4 * b, base + OFF_SFP + b * 512);
-        cp_sf(COL_SFV + 4 * b, base + OFF_SFV + s * 512);
+        const uint32_t sx = COL_S + 128u * uint32_t(x);
+        cp_sf(sx + SUB_SFP, base + OFF_SFP + 512 * x);
+        cp_sf(sx + SUB_SFV, base + OFF_SFV + s * 512);
         const uint64_t dV = smem_desc(base + OFF_V + s * TILE_BYTES, 8192, 1024, 2);
         if (issuer) {
-#pragma unroll
+  #pragma unroll
           for (int k = 0; k < 4; k++)
-            mma_mxf8_ts(tm + COL_O, tm + COL_S0 + 128 * b + 8 * k, dV + uint64_t(256 * k),
-                        idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFP + 4 * b, tm + COL_SFV + 4 * b,
-                        (jj > 0 || k > 0) ? 1u : 0u);
-          tc_commit(BAR(B_KVEMPTY + s));
-          tc_commit(BAR(B_ODONE));
+            mma_mxf8_ts(tm + COL_O + 128 * x, tm + sx + 8 * k, dV + uint64_t(256 * k),
+                        idesc_mxf8(128, 128, 0, 1, k, k), tm + sx + SUB_SFP, tm + sx + SUB_SFV,
+                        (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(BAR(B_ODONE + x));
+          // the last GEMM that reads K_j / V_j releases the stage
+          if (x == 1 || j >= nkv[1]) tc_commit(BAR(B_KVEMPTY + s));
         }
         __syncwarp();
         return true;
       };
       bool ok = wait_all(BAR(B_QFULL), 0);
-      tc_fence_after();
-      if (ok) cp_sf(COL_SFQ, base + OFF_SFQ);
-      for (int j = 0; ok && j < nkv; j++) {
-        const int s = j % NS, b = j & 1;
+      for (int j = 0; ok && j < nkv_max; j++) {
+        const int s = j % NS;
+        const bool act_a = j < nkv[0], act_b = j < nkv[1];
         if (!wait_all(BAR(B_KVFULL + s), (j / NS) & 1)) { ok = false; break; }
-        tc_fence_after();
-        cp_sf(COL_SFK + 4 * b, base + OFF_SFK + s * 512);
-        const uint64_t dK = smem_desc(base + OFF_K + s * TILE_BYTES, 16, 1024, 2);
-        if (issuer) {
-#pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ss(tm + COL_S0 + 128 * b, dQ + uint64_t(2 * k), dK + uint64_t(2 * k),
-                        idesc_mxf8(128, 128, 0, 0, k, k), tm + COL_SFQ, tm + COL_SFK + 4 * b,
-                        k > 0 ? 1u : 0u);
-          tc_commit(BAR(B_SFULL + b));
+        if (act_a) {
+          // S_B(j-1) loaded by its softmax: S_B's columns may take S_A's scales
+          if (j >= 1 && j - 1 < nkv[1] && !wait_all(BAR(B_SLOAD + 1), (j - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(0, j);
         }
-        __syncwarp();
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (j >= 1 && j - 1 < nkv[1] && !issue_pv(1, j - 1)) { ok = false; break; }
+        if (act_b) {
+          if (act_a && !wait_all(BAR(B_SLOAD + 0), j & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(1, j);
+        }
+        if (act_a && !issue_pv(0, j)) { ok = false; break; }
       }
-      if (ok && nkv > 0) issue_pv(nkv - 1);
+      if (ok && nkv[1] >= 1 && nkv[1] == nkv_max) ok = issue_pv(1, nkv[1] - 1);
       // all MMAs of this CTA retired before TMEM is released
       if (issuer) {
         tc_commit(BAR(B_TEAR));
@@ -237,68 +277,55 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       }
       __syncwarp();
     }
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_SOFTMAX));
     // ------------------------------------------------------------ softmax
-    // NWG warpgroups share each 128 x 128 S tile: warpgroup g owns key columns
-    // [g*W, (g+1)*W) of every row (thread = query row = TMEM lane).  They
-    // exchange their partial row maxima once per tile; each keeps its own
-    // partial row sum, writes its own P columns and rescales its own O columns.
-    // Every exit decision is a vote read after a barrier all of them reach, so
-    // they always leave together.
-    const int gw = (warp - 4) >> 2;
-    const int wi = warp - 4;                       // softmax warp index
+    // Warpgroup x owns query tile x: thread = query row = TMEM lane, and the
+    // whole 128-key row of S_X(j) is loaded into registers at once, which
+    // frees the S_X columns for the other tile's scales right away.
+    const int x = (warp - 4) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    const int qpos = qt * TILE + row;
+    const uint32_t col_s = COL_S + 128u * uint32_t(x), col_o = COL_O + 128u * uint32_t(x);
+    const int qpos = qp * 2 * TILE + x * TILE + row;
     const float sl2 = a.scale_log2;
-    const int c0 = gw * W;
-    float* red = reinterpret_cast<float*>(smem + OFF_RED);            // [2][NWG][128]
-    volatile int* vote = reinterpret_cast<volatile int*>(smem + OFF_VOTE);  // [2][NWG*4]
+    const int klim = a.causal ? min(lk, qpos + 1) : lk;  // keys < klim are visible
     float m = -INFINITY, l = 0.0f;
-    bool failed = false, ok = true;
-    for (int j = 0; j < nkv; j++) {
-      const int b = j & 1;
-      const bool okw = !failed &&
-          __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + b), (j >> 1) & 1, abort_flag, &g_status_fwd));
-      float s[W];
-      float bm[NB];
-      float pm = -INFINITY;
-      const int kbase = j * TILE + c0;
-      const int klim = a.causal ? min(lk, qpos + 1) : lk;  // keys < klim are visible
-      if (okw) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < W / 32; c++)
-          tmem_ld32(tmem + lane_base + COL_S0 + 128 * b + c0 + 32 * c, reinterpret_cast<uint32_t*>(s) + 32 * c);
-        tmem_wait_ld();
-        const bool need_mask = (kbase + W > lk) || (a.causal && kbase + W - 1 > qpos);
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < W; i++)
-            if (kbase + i >= klim) s[i] = -INFINITY;
-        }
-#pragma unroll
-        for (int kb = 0; kb < NB; kb++) {
-          float x = s[32 * kb];
-#pragma unroll
-          for (int i = 1; i < 31; i += 2)
-            asm("max.f32 %0, %1, %2, %3;" : "=f"(x) : "f"(x), "f"(s[32 * kb + i]), "f"(s[32 * kb + i + 1]));
-          bm[kb] = fmaxf(x, s[32 * kb + 31]);
-          pm = fmaxf(pm, bm[kb]);
-        }
+    bool ok = !bad_tiles;
+    for (int j = 0; ok && j < nkv[x]; j++) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + x), j & 1, abort_flag, &g_status_fwd))) {
+        ok = false;
+        break;
       }
-      red[(b * NWG + gw) * 128 + row] = pm;
-      if (lane == 0) vote[b * (NWG * 4) + wi] = okw ? 1 : 0;
-      named_bar_sync(2, NWG * 128);
-      bool all_ok = true;
+      tc_fence_after();
+      float s[128];
 #pragma unroll
-      for (int v = 0; v < NWG * 4; v++) all_ok = all_ok && vote[b * (NWG * 4) + v] != 0;
-      if (!all_ok) { ok = false; break; }
-      // raw-score maxima; fl(max S * sl2) = max fl(S * sl2) since sl2 > 0
-      float mt = red[(b * NWG + 0) * 128 + row];
+      for (int c = 0; c < 4; c++)
+        tmem_ld32(tmem + lane_base + col_s + 32 * c, reinterpret_cast<uint32_t*>(s) + 32 * c);
+      tmem_wait_ld();
 #pragma unroll
-      for (int g2 = 1; g2 < NWG; g2++) mt = fmaxf(mt, red[(b * NWG + g2) * 128 + row]);
-      mt = __fmul_rn(mt, sl2);
+      for (int c = 0; c < 4; c++) reg_fence32(reinterpret_cast<uint32_t*>(s) + 32 * c);
+      tc_fence_before();
+      fwd_warp_arrive(BAR(B_SLOAD + x), lane);
+      const int kbase = j * TILE;
+      if (__any_sync(0xFFFFFFFFu, kbase + TILE > klim)) {
+#pragma unroll
+        for (int i = 0; i < 128; i++)
+          if (kbase + i >= klim) s[i] = -INFINITY;
+      }
+      // raw-score block maxima (32 keys each) and row maximum
+      float bm[4];
+      float pm = -INFINITY;
+#pragma unroll
+      for (int kb = 0; kb < 4; kb++) {
+        float v = s[32 * kb];
+#pragma unroll
+        for (int i = 1; i < 31; i += 2) v = fmax3(v, s[32 * kb + i], s[32 * kb + i + 1]);
+        bm[kb] = fmaxf(v, s[32 * kb + 31]);
+        pm = fmaxf(pm, bm[kb]);
+      }
+      // fl(max S * sl2) = max fl(S * sl2) since sl2 > 0
+      const float mt = __fmul_rn(pm, sl2);
       const float mn = fmaxf(m, mt);
       const float mu = (m == -INFINITY || __fsub_rn(mn, m) > kRescaleThr) ? mn : m;
       const float mref = mu == -INFINITY ? 0.0f : mu;
@@ -309,18 +336,18 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       // its exponent X, each element is put on the E4M3 scale directly as
       // 2^fma(S, sl2, -fl(m + X)) and converted, and the row sum adds
       // 2^X * (block sum).
-      uint32_t pw[W / 4];
+      uint32_t pw[32];
       uint32_t sfw = 0;
       float lt = 0.0f;
 #pragma unroll
-      for (int kb = 0; kb < NB; kb++) {
+      for (int kb = 0; kb < 4; kb++) {
         const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(__fmul_rn(bm[kb], sl2), mref)));
         sfw |= sc << (8 * kb);
         const float nmx = -__fadd_rn(mref, float(int(sc) - 127));
         float2 rs = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 8; c++) {
-          float* p = s + 32 * kb + 4 * c;
+          const float* p = s + 32 * kb + 4 * c;
           const float2 a01 = ffma2(make_float2(p[0], p[1]), make_float2(sl2, sl2), make_float2(nmx, nmx));
           const float2 a23 = ffma2(make_float2(p[2], p[3]), make_float2(sl2, sl2), make_float2(nmx, nmx));
           const float2 x01 = make_float2(ex2(a01.x), ex2(a01.y));
@@ -331,19 +358,13 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         lt += (rs.x + rs.y) * e8m0_value(sc);
       }
       l = l * alpha + lt;
-      // O must hold PV(j-1) before it is rescaled and before PV(j) is issued
-      if (j >= 1 &&
-          !__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (j - 1) & 1, abort_flag, &g_status_fwd))) {
-        failed = true;  // leave at the next vote, together with the others
-        m = mu;
-        continue;
-      }
-      tc_fence_after();
+      // O_X holds PV_X(j-1): S_X(j) completed, and its commit covers every
+      // earlier MMA of the issuer.  PV_X(j) waits for this tile's P.
       if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll
-        for (int c = 0; c < W / 32; c++) {
+        for (int c = 0; c < 4; c++) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + COL_O + c0 + 32 * c, o);
+          tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -352,44 +373,31 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
             o[i] = __float_as_uint(t.x);
             o[i + 1] = __float_as_uint(t.y);
           }
-          tmem_st16(tmem + lane_base + COL_O + c0 + 32 * c, o);
-          tmem_st16(tmem + lane_base + COL_O + c0 + 32 * c + 16, o + 16);
+          tmem_st16(tmem + lane_base + col_o + 32 * c, o);
+          tmem_st16(tmem + lane_base + col_o + 32 * c + 16, o + 16);
         }
       }
-#pragma unroll
-      for (int c = 0; c < W / 4; c += 16)
-        tmem_st16(tmem + lane_base + COL_S0 + 128 * b + c0 / 4 + c, pw + c);
-      uint8_t* atom = smem + OFF_SFP + b * 512 + (row & 31) * 16 + (row >> 5) * 4 + gw * NB;
-#pragma unroll
-      for (int kb = 0; kb < NB; kb++) atom[kb] = uint8_t(sfw >> (8 * kb));
+      tmem_st16(tmem + lane_base + col_s, pw);
+      tmem_st16(tmem + lane_base + col_s + 16, pw + 16);
+      // this row's four P scales: atom word (row % 32) * 4 + row / 32
+      *reinterpret_cast<uint32_t*>(smem + OFF_SFP + 512 * x + (row & 31) * 16 + (row >> 5) * 4) = sfw;
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(BAR(B_PFULL + b));
+      fwd_warp_arrive(BAR(B_PFULL + x), lane);
       m = mu;
     }
-    // ---- epilogue: O / l -> bf16 (each warpgroup its own columns), LSE
-    const bool okf = ok && !failed && nkv > 0 &&
-        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE), (nkv - 1) & 1, abort_flag, &g_status_fwd));
-    float* lsum = red + 2 * NWG * 128;  // [NWG][128]
-    lsum[gw * 128 + row] = l;
-    if (lane == 0) vote[2 * (NWG * 4) + wi] = okf ? 1 : 0;
-    named_bar_sync(2, NWG * 128);
-    bool all_ok = true;
-#pragma unroll
-    for (int v = 0; v < NWG * 4; v++) all_ok = all_ok && vote[2 * (NWG * 4) + v] != 0;
-    if (all_ok) {
+    // ---- epilogue: O / l -> bf16, LSE
+    if (ok && nkv[x] > 0 &&
+        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE + x), (nkv[x] - 1) & 1, abort_flag, &g_status_fwd))) {
       tc_fence_after();
-      float lt = lsum[row];
-#pragma unroll
-      for (int g2 = 1; g2 < NWG; g2++) lt += lsum[g2 * 128 + row];
       const bool valid = qpos < lq;
-      const float rl = 1.0f / lt;
-      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128 + c0;
+      const float rl = 1.0f / l;
+      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128;
 #pragma unroll
-      for (int c = 0; c < W / 32; c++) {
+      for (int c = 0; c < 4; c++) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + COL_O + c0 + 32 * c, o);
+        tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
@@ -405,8 +413,8 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
           }
         }
       }
-      if (valid && gw == 0) {
-        const float lse = (m + log2f(lt)) * 0.69314718055994530942f;
+      if (valid) {
+        const float lse = (m + log2f(l)) * 0.69314718055994530942f;
         if (a.dense_lse)
           a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + qpos] = lse;
         else
@@ -432,10 +440,11 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   }
   dim3 grid;
   if (a.sq.cu == nullptr) {
-    const int nqt = (a.sq.seqlen + fwd::TILE - 1) / fwd::TILE;
-    grid = dim3(unsigned(nqt * a.H * a.sq.nseq), 1, 1);
+    const int npair = (a.sq.seqlen + 2 * fwd::TILE - 1) / (2 * fwd::TILE);
+    grid = dim3(unsigned(npair * a.H * a.sq.nseq), 1, 1);
   } else {
-    grid = dim3(unsigned((a.sq.seqlen + fwd::TILE - 1) / fwd::TILE), unsigned(a.H), unsigned(a.sq.nseq));
+    grid = dim3(unsigned((a.sq.seqlen + 2 * fwd::TILE - 1) / (2 * fwd::TILE)), unsigned(a.H),
+                unsigned(a.sq.nseq));
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   attn_fwd_kernel<<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
