@@ -62,7 +62,7 @@ constexpr uint32_t COL_S = 0, COL_O = 256;                       // + 128 * tile
 constexpr uint32_t SUB_SFP = 32, SUB_SFV = 36, SUB_SFQ = 40, SUB_SFK = 44;  // inside an S region
 constexpr int NTHREADS = 384;
 // registers per thread after the split: warps 0-3 give up, the softmax warps take
-constexpr int REG_SMALL = 64, REG_SOFTMAX = 216;
+constexpr int REG_SMALL = 56, REG_SOFTMAX = 224;
 static_assert(4 * 32 * REG_SMALL + 8 * 32 * REG_SOFTMAX <= NTHREADS * 168,
               "register split exceeds the launch allocation");
 }  // namespace fwd
@@ -117,10 +117,9 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
   const bool has_b = qp * 2 * TILE + TILE < lq;
   const int nkv_all = (lk + TILE - 1) / TILE;
   // key tiles each query tile needs (causal: up to its last query)
-  int nkv[2];
-  nkv[0] = a.causal ? min(nkv_all, 2 * qp + 1) : nkv_all;
-  nkv[1] = !has_b ? 0 : a.causal ? min(nkv_all, 2 * qp + 2) : nkv_all;
-  const int nkv_max = max(nkv[0], nkv[1]);
+  const int nkv_a = a.causal ? min(nkv_all, 2 * qp + 1) : nkv_all;
+  const int nkv_b = !has_b ? 0 : a.causal ? min(nkv_all, 2 * qp + 2) : nkv_all;
+  const int nkv_max = max(nkv_a, nkv_b);
   const int64_t tq_g = seq_units_before(a.sq, g, TILE) + 2 * qp;  // packed tile of Q_A
   const int64_t tk_g0 = seq_units_before(a.sk, g, TILE);
 
@@ -245,7 +244,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
                         (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(BAR(B_ODONE + x));
           // the last GEMM that reads K_j / V_j releases the stage
-          if (x == 1 || j >= nkv[1]) tc_commit(BAR(B_KVEMPTY + s));
+          if (x == 1 || j >= nkv_b) tc_commit(BAR(B_KVEMPTY + s));
         }
         __syncwarp();
         return true;
@@ -253,15 +252,15 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       bool ok = wait_all(BAR(B_QFULL), 0);
       for (int j = 0; ok && j < nkv_max; j++) {
         const int s = j % NS;
-        const bool act_a = j < nkv[0], act_b = j < nkv[1];
+        const bool act_a = j < nkv_a, act_b = j < nkv_b;
         if (!wait_all(BAR(B_KVFULL + s), (j / NS) & 1)) { ok = false; break; }
         if (act_a) {
           // S_B(j-1) loaded by its softmax: S_B's columns may take S_A's scales
-          if (j >= 1 && j - 1 < nkv[1] && !wait_all(BAR(B_SLOAD + 1), (j - 1) & 1)) { ok = false; break; }
+          if (j >= 1 && j - 1 < nkv_b && !wait_all(BAR(B_SLOAD + 1), (j - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_s(0, j);
         }
-        if (j >= 1 && j - 1 < nkv[1] && !issue_pv(1, j - 1)) { ok = false; break; }
+        if (j >= 1 && j - 1 < nkv_b && !issue_pv(1, j - 1)) { ok = false; break; }
         if (act_b) {
           if (act_a && !wait_all(BAR(B_SLOAD + 0), j & 1)) { ok = false; break; }
           tc_fence_after();
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         }
         if (act_a && !issue_pv(0, j)) { ok = false; break; }
       }
-      if (ok && nkv[1] >= 1 && nkv[1] == nkv_max) ok = issue_pv(1, nkv[1] - 1);
+      if (ok && nkv_b >= 1 && nkv_b == nkv_max) ok = issue_pv(1, nkv_b - 1);
       // all MMAs of this CTA retired before TMEM is released
       if (issuer) {
         tc_commit(BAR(B_TEAR));
@@ -290,9 +289,10 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
     const int qpos = qp * 2 * TILE + x * TILE + row;
     const float sl2 = a.scale_log2;
     const int klim = a.causal ? min(lk, qpos + 1) : lk;  // keys < klim are visible
+    const int nkv_x = x == 0 ? nkv_a : nkv_b;
     float m = -INFINITY, l = 0.0f;
     bool ok = !bad_tiles;
-    for (int j = 0; ok && j < nkv[x]; j++) {
+    for (int j = 0; ok && j < nkv_x; j++) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_SFULL + x), j & 1, abort_flag, &g_status_fwd))) {
         ok = false;
         break;
@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       m = mu;
     }
     // ---- epilogue: O / l -> bf16, LSE
-    if (ok && nkv[x] > 0 &&
-        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE + x), (nkv[x] - 1) & 1, abort_flag, &g_status_fwd))) {
+    if (ok && nkv_x > 0 &&
+        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE + x), (nkv_x - 1) & 1, abort_flag, &g_status_fwd))) {
       tc_fence_after();
       const bool valid = qpos < lq;
       const float rl = 1.0f / l;
