@@ -9,8 +9,13 @@ reduction.  value = algorithmic PFLOP/s of the step (forward 4*D and backward
 10*D FLOPs per unmasked (query, key) pair, S^2/2 pairs per causal head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxfa|reference]
+  python bench.py --profile-op fwd|bwd [--profile-seq S] [--profile-batch B] [--steps K] [--warmup W]
 
-One JSON line on rank 0.  Under torchrun (N > 1) every rank runs the same
+One JSON line on rank 0.  --profile-op runs W + K launches of one operation
+on a causal case (B=--profile-batch, H=16, S=--profile-seq) for kernel profiling,
+and prints its timing instead of the benchmark line.
+
+Under torchrun (N > 1) every rank runs the same
 per-GPU workload (replicas; no collective on the data path) and value is the
 sum of all ranks' work over the slowest rank's time.
 """
@@ -41,6 +46,10 @@ def attn_flops(b, h, s, d, causal, per_pair):
     return per_pair * d * pairs
 
 
+# DRAM bytes of one attn_bwd_kernel launch at this workload, from one ncu capture
+# (profiles/attn_bwd_kernel_llm_traffic.md); null once the kernel changes.
+BWD_TRAFFIC_BYTES = 1327060224 + 921061632
+
 FWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 4)
 BWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 10)
 
@@ -48,11 +57,14 @@ BWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 10)
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="mxfa", choices=["mxfa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-components", action="store_true")
+    p.add_argument("--profile-op", choices=["fwd", "bwd"], default=None)
+    p.add_argument("--profile-seq", type=int, default=4096)
+    p.add_argument("--profile-batch", type=int, default=1)
     return p.parse_args()
 
 
@@ -348,11 +360,48 @@ def reference_arm(args):
     return 0
 
 
+def profile_op(args):
+    """W + K launches of one operation (B=--profile-batch, H=16, S=--profile-seq, causal)."""
+    import torch
+    from mxfp8_block_scaled_fa_gb300 import build, inputs
+    build.build()
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    b, s = args.profile_batch, args.profile_seq
+    qb, kb, vb, dob = inputs.dense_attn(b, H, s, D, seed=SEED)
+    dev = torch.device("cuda", 0)
+    t = lambda x: torch.from_numpy(x.view("int16")).view(torch.bfloat16).reshape(b * s, H, D).to(dev)
+    q, k, v, do = t(qb), t(kb), t(vb), t(dob)
+    seqs = mxfa.Seqs.dense(b, s)
+    scale = 1.0 / math.sqrt(D)
+    qR, kR, vC = mxfa.quantize(q, 0, seqs), mxfa.quantize(k, 0, seqs), mxfa.quantize(v, 1, seqs)
+    o, lse = mxfa.attention_fwd(qR, kR, vC, seqs, seqs, scale, CAUSAL)
+    if args.profile_op == "fwd":
+        run = lambda: mxfa.attention_fwd(qR, kR, vC, seqs, seqs, scale, CAUSAL, out=(o, lse))
+        per_pair = 4
+    else:
+        ops = (mxfa.quantize(q, 2, seqs), mxfa.quantize(k, 2, seqs), mxfa.quantize(v, 0, seqs),
+               mxfa.quantize(do, 2, seqs))
+        ws = torch.empty(mxfa.mxfa_bwd_workspace_size(b * s, b, H, D, 0), dtype=torch.uint8,
+                         device=dev)
+        grads = tuple(torch.empty_like(o) for _ in range(3))
+        run = lambda: mxfa.attention_bwd(*ops, o, do, lse, seqs, seqs, scale, CAUSAL, ws=ws,
+                                         out=grads)
+        per_pair = 10
+    ms = time_loop(torch, run, args.steps, args.warmup)
+    assert mxfa.device_status() == 0, "device status"
+    fl = attn_flops(b, H, s, D, CAUSAL, per_pair)
+    print(json.dumps({"profile_op": args.profile_op, "B": b, "H": H, "seq_len": s, "D": D,
+                      "causal": CAUSAL, "ms": ms, "pflops": fl / ms / 1e12}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile_op:
+        return profile_op(args)
     import torch
     import torch.distributed as dist
     from mxfp8_block_scaled_fa_gb300 import build, inputs
@@ -443,7 +492,9 @@ def main():
         line["roofline"] = {"bound": "tensor", "kernel": "attn_bwd_kernel (mxfa_bwd call incl. "
                             "pre/post)" if dom == "bwd" else "attn_fwd_kernel",
                             "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                            "frac": achieved / fp8_peak, "traffic": None,
+                            "frac": achieved / fp8_peak,
+                            "traffic": BWD_TRAFFIC_BYTES if dom == "bwd" else None,
+                            "traffic_unit": "bytes per launch (ncu dram read + write)",
                             "peak_source": f"{peak_src} bf16 burst {bf16_peak} x 2 (fp8/bf16 "
                                            f"nominal ratio)"}
         line["components"] = comp
