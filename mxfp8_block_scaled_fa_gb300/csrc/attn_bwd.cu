@@ -342,7 +342,8 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     warp_arrive(BAR(B_KCONST), lane);
     if (warp == 2) {
       // -------------------------------------- MMA issuer: dV, dK, dQ^T
-      const bool issuer = lane == 0;
+      // The whole warp walks the schedule; every tcgen05 operation is issued
+      // through a lane elected inside the instruction.
       const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
@@ -350,9 +351,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       // scale atom (512 bytes in shared memory) -> TMEM slot, replicated to the
       // four lane quadrants; ordered before this thread's later MMAs
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
-        const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        if (issuer)
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
+        tc_cp_sf_w(tm + col, smem_desc(saddr, 128, 128, 0));
       };
       const uint64_t dK_mn = smem_desc(base + OFF_K, 8192, 1024, 2);    // K^T, MN-major (dQ^T A)
       // K (shared memory) and the K^T scale atom
@@ -379,48 +378,40 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         const uint64_t dSt_mn = smem_desc(base + OFF_DST + b * PS_BYTES, 8192, 512, 4);
         const uint64_t dQ_mn = smem_desc(base + OFF_Q + s * QD_BYTES, 8192, 1024, 2);
         const uint64_t dDO_mn = smem_desc(base + OFF_DO + s * QD_BYTES, 8192, 1024, 2);
-        if (issuer) {
 #pragma unroll
-          for (int k = 0; k < 2; k++) {
-            const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
-            mma_mxf8_ss(tm + COL_DV, dPt + uint64_t(2 * k), dDO_mn + uint64_t(256 * k),
+        for (int k = 0; k < 2; k++) {
+          const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
+          mma_mxf8_ss_w(tm + COL_DV, dPt + uint64_t(2 * k), dDO_mn + uint64_t(256 * k),
                         idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFPT + 4 * b, tm + COL_SFDOT + 4 * b,
                         acc);
-            mma_mxf8_ss(tm + COL_DK, dSt_k + uint64_t(2 * k), dQ_mn + uint64_t(256 * k),
+          mma_mxf8_ss_w(tm + COL_DK, dSt_k + uint64_t(2 * k), dQ_mn + uint64_t(256 * k),
                         idesc_mxf8(128, 128, 0, 1, k, k), tm + COL_SFDST + 4 * b, tm + COL_SFQT + 4 * b,
                         acc);
-          }
-          tc_commit(BAR(B_QDOEMPTY + s));  // Q_j and dO_j are no longer read
         }
-        __syncwarp();
+        tc_commit_w(BAR(B_QDOEMPTY + s));  // Q_j and dO_j are no longer read
         // dQ^T reuses one accumulator: the previous tile's must have been drained
         if (jj >= 1 && !wait_all(BAR(B_DQEMPTY), (jj - 1) & 1)) return false;
         tc_fence_after();
-        if (issuer) {
 #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ss(tm + COL_DQ, dK_mn + uint64_t(256 * k), dSt_mn + uint64_t(128 * k),
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss_w(tm + COL_DQ, dK_mn + uint64_t(256 * k), dSt_mn + uint64_t(128 * k),
                         idesc_mxf8(128, 64, 1, 1, k, k), tm + COL_SFKT, tm + COL_SFDS + 4 * b,
                         k > 0 ? 1u : 0u);
-          tc_commit(BAR(B_PDSEMPTY + b));
-          tc_commit(BAR(B_DQFULL));
-        }
-        __syncwarp();
+        tc_commit_w(BAR(B_PDSEMPTY + b));
+        tc_commit_w(BAR(B_DQFULL));
         return true;
       };
       for (int jj = 0; ok && jj < ntile; jj++) ok = grads(jj);
-      if (issuer) {
-        tc_commit(BAR(B_KVDONE));
-        tc_commit(BAR(B_TEAR2));
-        bwait_raw(BAR(B_TEAR2), 0);
-      }
+      tc_commit_w(BAR(B_KVDONE));
+      tc_commit_w(BAR(B_TEAR2));
+      bwait_raw(BAR(B_TEAR2), 0);
       __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer: S^T, dP^T
-    // The whole warp walks the schedule so that descriptors and TMEM addresses
-    // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
-    // Scale atoms enter TMEM by tcgen05.cp in the same stream as the MMAs
+    // The whole warp walks the schedule (descriptors and TMEM addresses are
+    // warp-uniform) and issues every tcgen05 operation through a lane elected
+    // inside the instruction.  Scale atoms enter TMEM by tcgen05.cp in the same stream as the MMAs
     // that read them (replicated 32x128b x4 layout: lane L, column c holds
     // rows 32c + L % 32, k-blocks in its bytes).
     // The gradient GEMMs have an issuer of their own (warp 2): tcgen05.mma
@@ -428,7 +419,6 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     // shares its SM sub-partition with arithmetic-heavy warps, so two
     // independent issue streams keep the pipe fed better than one.
     {
-      const bool issuer = lane == 0;
       const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_bwd));
@@ -437,9 +427,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       const uint64_t dK_k = smem_desc(base + OFF_K, 16, 1024, 2);       // K, K-major (S^T A)
       const uint64_t dV_k = smem_desc(base + OFF_V, 16, 1024, 2);       // V, K-major (dP^T A)
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
-        const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        if (issuer)
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
+        tc_cp_sf_w(tm + col, smem_desc(saddr, 128, 128, 0));
       };
       bool ok = wait_all(BAR(B_KVFULL), 0) && wait_all(BAR(B_KCONST), 0);
       tc_fence_after();
@@ -459,24 +447,19 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         cp_sf(COL_SFDO, base + OFF_REC + s * REC_BYTES + REC_SFDO);
         const uint64_t dQ_k = smem_desc(base + OFF_Q + s * QD_BYTES, 16, 1024, 2);
         const uint64_t dDO_k = smem_desc(base + OFF_DO + s * QD_BYTES, 16, 1024, 2);
-        if (issuer) {
 #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ss(tm + COL_S, dK_k + uint64_t(2 * k), dQ_k + uint64_t(2 * k),
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss_w(tm + COL_S, dK_k + uint64_t(2 * k), dQ_k + uint64_t(2 * k),
                         idesc_mxf8(128, 64, 0, 0, k, k), tm + COL_SFK, tm + COL_SFQ, k > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ss(tm + COL_DP, dV_k + uint64_t(2 * k), dDO_k + uint64_t(2 * k),
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss_w(tm + COL_DP, dV_k + uint64_t(2 * k), dDO_k + uint64_t(2 * k),
                         idesc_mxf8(128, 64, 0, 0, k, k), tm + COL_SFV, tm + COL_SFDO, k > 0 ? 1u : 0u);
-          tc_commit(BAR(B_SDPFULL));
-        }
-        __syncwarp();
+        tc_commit_w(BAR(B_SDPFULL));
       }
       // every MMA of this issuer has completed before TMEM is released
-      if (issuer) {
-        tc_commit(BAR(B_TEAR));
-        bwait_raw(BAR(B_TEAR), 0);
-      }
+      tc_commit_w(BAR(B_TEAR));
+      bwait_raw(BAR(B_TEAR), 0);
       __syncwarp();
     }
   } else if (warp >= 4 && warp < 12) {

@@ -195,18 +195,16 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       }
     } else if (warp == 1 && !bad_tiles) {
       // ------------------------------------------------------------ MMA issuer
-      // The whole warp walks the schedule so that descriptors and TMEM addresses
-      // are warp-uniform values; lane 0 alone issues the tcgen05 operations.
-      const bool issuer = lane == 0;
+      // The whole warp walks the schedule (descriptors and TMEM addresses are
+      // warp-uniform) and issues every tcgen05 operation through a lane elected
+      // inside the instruction.
       const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
       auto wait_all = [&](uint32_t bar, uint32_t par) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, par, abort_flag, &g_status_fwd));
       };
       // scale atom (shared memory) -> TMEM, replicated to the four lane quadrants
       auto cp_sf = [&](uint32_t col, uint32_t saddr) {
-        const uint64_t d = smem_desc(saddr, 128, 128, 0);
-        if (issuer)
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tm + col), "l"(d) : "memory");
+        tc_cp_sf_w(tm + col, smem_desc(saddr, 128, 128, 0));
       };
       // S_X(j) = Q_X K_j^T; its scales go into the other tile's S columns,
       // which that tile's softmax has already loaded (or never used)
@@ -217,15 +215,12 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         cp_sf(other + SUB_SFK, base + OFF_SFK + s * 512);
         const uint64_t dQ = smem_desc(base + OFF_Q + x * TILE_BYTES, 16, 1024, 2);
         const uint64_t dK = smem_desc(base + OFF_K + s * TILE_BYTES, 16, 1024, 2);
-        if (issuer) {
-  #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ss(tm + COL_S + 128 * x, dQ + uint64_t(2 * k), dK + uint64_t(2 * k),
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ss_w(tm + COL_S + 128 * x, dQ + uint64_t(2 * k), dK + uint64_t(2 * k),
                         idesc_mxf8(128, 128, 0, 0, k, k), tm + other + SUB_SFQ, tm + other + SUB_SFK,
                         k > 0 ? 1u : 0u);
-          tc_commit(BAR(B_SFULL + x));
-        }
-        __syncwarp();
+        tc_commit_w(BAR(B_SFULL + x));
       };
       // O_X += P_X(j) V_j, P_X read from the S_X columns
       auto issue_pv = [&](int x, int j) -> bool {
@@ -236,17 +231,14 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         cp_sf(sx + SUB_SFP, base + OFF_SFP + 512 * x);
         cp_sf(sx + SUB_SFV, base + OFF_SFV + s * 512);
         const uint64_t dV = smem_desc(base + OFF_V + s * TILE_BYTES, 8192, 1024, 2);
-        if (issuer) {
-  #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_mxf8_ts(tm + COL_O + 128 * x, tm + sx + 8 * k, dV + uint64_t(256 * k),
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_mxf8_ts_w(tm + COL_O + 128 * x, tm + sx + 8 * k, dV + uint64_t(256 * k),
                         idesc_mxf8(128, 128, 0, 1, k, k), tm + sx + SUB_SFP, tm + sx + SUB_SFV,
                         (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit(BAR(B_ODONE + x));
-          // the last GEMM that reads K_j / V_j releases the stage
-          if (x == 1 || j >= nkv_b) tc_commit(BAR(B_KVEMPTY + s));
-        }
-        __syncwarp();
+        tc_commit_w(BAR(B_ODONE + x));
+        // the last GEMM that reads K_j / V_j releases the stage
+        if (x == 1 || j >= nkv_b) tc_commit_w(BAR(B_KVEMPTY + s));
         return true;
       };
       bool ok = wait_all(BAR(B_QFULL), 0);
@@ -270,10 +262,8 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       }
       if (ok && nkv_b >= 1 && nkv_b == nkv_max) ok = issue_pv(1, nkv_b - 1);
       // all MMAs of this CTA retired before TMEM is released
-      if (issuer) {
-        tc_commit(BAR(B_TEAR));
-        mbar_wait_raw(BAR(B_TEAR), 0);
-      }
+      tc_commit_w(BAR(B_TEAR));
+      mbar_wait_raw(BAR(B_TEAR), 0);
       __syncwarp();
     }
   } else {

@@ -195,6 +195,45 @@ __device__ __forceinline__ void mma_mxf8_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Warp-wide forms: the whole (converged) warp executes the instruction and
+// one lane elected inside it issues the operation.  An issuing warp that
+// shares its SM sub-partition with arithmetic-heavy warps issues tcgen05
+// operations markedly faster this way than from a lane-0 branch.
+__device__ __forceinline__ void mma_mxf8_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+// 512-byte scale atom (shared memory) -> TMEM columns col..col+3, replicated to
+// the four lane quadrants (32x128b x4).
+__device__ __forceinline__ void tc_cp_sf_w(uint32_t tmem_col, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(tmem_col), "l"(sdesc)
+      : "memory");
+}
+
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, E8M0 scales,
 // fp32 accumulation.  a_mn / b_mn: 1 = operand is MN-major in smem.
 // sfa_id / sfb_id select the byte of each 32-bit scale column.
