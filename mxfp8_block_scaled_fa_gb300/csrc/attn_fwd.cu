@@ -222,11 +222,9 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
                         k > 0 ? 1u : 0u);
         tc_commit_w(BAR(B_SFULL + x));
       };
-      // O_X += P_X(j) V_j, P_X read from the S_X columns
-      auto issue_pv = [&](int x, int j) -> bool {
+      // O_X += P_X(j) V_j, P_X read from the S_X columns (P_X(j) written)
+      auto issue_pv = [&](int x, int j) {
         const int s = j % NS;
-        if (!wait_all(BAR(B_PFULL + x), j & 1)) return false;
-        tc_fence_after();
         const uint32_t sx = COL_S + 128u * uint32_t(x);
         cp_sf(sx + SUB_SFP, base + OFF_SFP + 512 * x);
         cp_sf(sx + SUB_SFV, base + OFF_SFV + s * 512);
@@ -239,28 +237,45 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         tc_commit_w(BAR(B_ODONE + x));
         // the last GEMM that reads K_j / V_j releases the stage
         if (x == 1 || j >= nkv_b) tc_commit_w(BAR(B_KVEMPTY + s));
-        return true;
       };
-      bool ok = wait_all(BAR(B_QFULL), 0);
-      for (int j = 0; ok && j < nkv_max; j++) {
-        const int s = j % NS;
-        const bool act_a = j < nkv_a, act_b = j < nkv_b;
-        if (!wait_all(BAR(B_KVFULL + s), (j / NS) & 1)) { ok = false; break; }
-        if (act_a) {
-          // S_B(j-1) loaded by its softmax: S_B's columns may take S_A's scales
-          if (j >= 1 && j - 1 < nkv_b && !wait_all(BAR(B_SLOAD + 1), (j - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(0, j);
-        }
-        if (j >= 1 && j - 1 < nkv_b && !issue_pv(1, j - 1)) { ok = false; break; }
-        if (act_b) {
-          if (act_a && !wait_all(BAR(B_SLOAD + 0), j & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(1, j);
-        }
-        if (act_a && !issue_pv(0, j)) { ok = false; break; }
+      auto kv_ready = [&](int j) { return wait_all(BAR(B_KVFULL + j % NS), (j / NS) & 1); };
+      // Schedule: S_A(0), S_B(0), then per key tile j two blocks,
+      //   A: PV_A(j), S_A(j+1)   B: PV_B(j), S_B(j+1)
+      // each issued back to back once everything both GEMMs wait for is in:
+      // P_X(j) written; K/V(j+1) landed; the other tile's S loaded by its
+      // softmax (its columns take this tile's S scales).
+      bool ok = wait_all(BAR(B_QFULL), 0) && (nkv_max == 0 || kv_ready(0));
+      if (ok && nkv_a > 0) {
+        tc_fence_after();
+        issue_s(0, 0);
       }
-      if (ok && nkv_b >= 1 && nkv_b == nkv_max) ok = issue_pv(1, nkv_b - 1);
+      if (ok && nkv_b > 0) {
+        ok = nkv_a == 0 || wait_all(BAR(B_SLOAD + 0), 0);
+        tc_fence_after();
+        if (ok) issue_s(1, 0);
+      }
+      for (int j = 0; ok && j < nkv_max; j++) {
+        if (j < nkv_a) {
+          const bool next = j + 1 < nkv_a;
+          // the waits that usually complete first come first, P_A(j) last
+          ok = (!next || j >= nkv_b || wait_all(BAR(B_SLOAD + 1), j & 1)) && (!next || kv_ready(j + 1)) &&
+               wait_all(BAR(B_PFULL + 0), j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (next) issue_s(0, j + 1);
+        }
+        if (j < nkv_b) {
+          const bool next = j + 1 < nkv_b;
+          // K/V(j+1) was waited for in block A unless A has no tile j+1
+          ok = (!next || (j + 1 < nkv_a ? wait_all(BAR(B_SLOAD + 0), (j + 1) & 1) : kv_ready(j + 1))) &&
+               wait_all(BAR(B_PFULL + 1), j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          if (next) issue_s(1, j + 1);
+        }
+      }
       // all MMAs of this CTA retired before TMEM is released
       tc_commit_w(BAR(B_TEAR));
       mbar_wait_raw(BAR(B_TEAR), 0);
