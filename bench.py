@@ -9,11 +9,12 @@ reduction.  value = algorithmic PFLOP/s of the step (forward 4*D and backward
 10*D FLOPs per unmasked (query, key) pair, S^2/2 pairs per causal head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxfa|reference]
-  python bench.py --profile-op fwd|bwd [--profile-seq S] [--profile-batch B] [--steps K] [--warmup W]
+  python bench.py --profile-op fwd|bwd|rmsnorm [--profile-seq S] [--profile-batch B] [--steps K] [--warmup W]
 
 One JSON line on rank 0.  --profile-op runs W + K launches of one operation
-on a causal case (B=--profile-batch, H=16, S=--profile-seq) for kernel profiling,
-and prints its timing instead of the benchmark line.
+on a causal case (B=--profile-batch, H=16, S=--profile-seq; for rmsnorm the
+fused producer's X[32768, 2048] with row and column outputs) for kernel
+profiling, and prints its timing instead of the benchmark line.
 
 Under torchrun (N > 1) every rank runs the same
 per-GPU workload (replicas; no collective on the data path) and value is the
@@ -62,7 +63,7 @@ def parse():
     p.add_argument("--impl", default="mxfa", choices=["mxfa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-components", action="store_true")
-    p.add_argument("--profile-op", choices=["fwd", "bwd"], default=None)
+    p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm"], default=None)
     p.add_argument("--profile-seq", type=int, default=4096)
     p.add_argument("--profile-batch", type=int, default=1)
     return p.parse_args()
@@ -366,6 +367,22 @@ def profile_op(args):
     from mxfp8_block_scaled_fa_gb300 import build, inputs
     build.build()
     from mxfp8_block_scaled_fa_gb300 import mxfa
+    if args.profile_op == "rmsnorm":
+        x, g, _ = inputs.fused_inputs()
+        dev = torch.device("cuda", 0)
+        xd = torch.from_numpy(x.view("int16")).view(torch.bfloat16).to(dev)
+        gd = torch.from_numpy(g).to(dev)
+        outs = mxfa.rmsnorm_quant(xd, gd, 1e-6, 8192, 16, outputs=("row", "col"))
+        st = {k: mxfa.MxOut(v.data.data_ptr(), v.sf_compact.data_ptr(), v.sf_packed.data_ptr())
+              for k, v in outs.items()}
+        run = lambda: mxfa.mxfa_rmsnorm_quant(xd, gd, 32768, 2048, 1e-6, 8192, 16, st["row"],
+                                               st["col"], None, None)
+        ms = time_loop(torch, run, args.steps, args.warmup)
+        assert mxfa.device_status() == 0, "device status"
+        nb = 32768 * 2048 * (2 + 2 * (1 + 1 / 32))
+        print(json.dumps({"profile_op": "rmsnorm", "T": 32768, "C": 2048, "outputs": "row+col",
+                          "ms": ms, "GB_s": nb / ms / 1e6}), flush=True)
+        return 0
     b, s = args.profile_batch, args.profile_seq
     qb, kb, vb, dob = inputs.dense_attn(b, H, s, D, seed=SEED)
     dev = torch.device("cuda", 0)

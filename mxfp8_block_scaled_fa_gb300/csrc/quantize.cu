@@ -259,160 +259,268 @@ cudaError_t launch_sf_pack(const PackArgs& a, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------- RMSNorm+Quantize
-// One CTA = 32 rows, warp w = row w; lane l owns columns 8l + 256k + j.
-// Sum of squares in that order (k outer, j inner), then a butterfly over
-// 16, 8, 4, 2, 1; mean = ss / C; r = 1 / sqrt(mean + eps); y = (x * r) * gamma,
-// each a correctly rounded fp32 operation.  Column (32x1) and square (32x32)
-// maxima are exchanged through shared memory, one 256-column chunk at a time.
+// Persistent: one CTA (1024 threads) per SM walks 32-row blocks.  Each block
+// arrives by one bulk copy into shared memory; as soon as every thread has
+// taken its slice into registers, the next block's copy is issued, so that it
+// lands while this block is normalised, quantised and stored.  The column and
+// square outputs, written after the block's scales are known, read the block
+// again from L2, where the bulk copy has just put it.
+// Warp w = row w; lane l owns columns 8l + 256k + j.  Sum of squares in that
+// order (k outer, j inner), then a butterfly over 16, 8, 4, 2, 1;
+// mean = ss / C; r = 1 / sqrt(mean + eps); y = (x * r) * gamma, each a
+// correctly rounded fp32 operation.  The column (32x1) and square (32x32)
+// scales come from the exponent byte of each |y| (the E8M0 rule reads only the
+// exponent of the block maximum), written to shared memory and reduced with
+// byte-wise maxima: two CTA barriers per block.
+namespace rms {
+constexpr int NTHREADS = 1024;
+__host__ __device__ constexpr int smem_bytes(int C) { return 32 * C * 2 + 32 * C + C * 4 + C * 4 + C + C / 32; }
+}  // namespace rms
+
+__device__ __forceinline__ float rms_y(uint32_t w, bool hi, float r, float g) {
+  return __fmul_rn(__fmul_rn(hi ? bf_hi(w) : bf_lo(w), r), g);
+}
+// E8M0 byte from the exponent byte of a block maximum (0xFF: Inf / NaN present).
+__device__ __forceinline__ uint32_t e8m0_from_exp(uint32_t e) {
+  return e == 0xFFu ? 0xFFu : (e > 8u ? e - 8u : 0u);
+}
+
 template <int NK>
-__global__ void __launch_bounds__(1024, 1) rms_quant_kernel(RmsArgs a) {
-  __shared__ uint32_t sm_abs[32][257];
-  __shared__ uint32_t sm_part[4][256];
-  __shared__ float sm_colinv[256];
-  __shared__ float sm_sqinv[8];
-  __shared__ uint8_t sm_colbad[256];
+__global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) {
   constexpr int C = NK * 256;
+  extern __shared__ __align__(128) uint8_t rms_smem[];
+  uint8_t* sx = rms_smem;                       // [32][C] bf16 of the block
+  uint8_t* sexp = sx + 32 * C * 2;              // [32][C] exponent bytes of |y|
+  float* sgm = reinterpret_cast<float*>(sexp + 32 * C);  // [C] gamma
+  float* scinv = sgm + C;                       // [C] column inverse scales of the block
+  uint8_t* scol = sexp + 32 * C + C * 8;        // [C] column scales of the block
+  uint8_t* ssq = scol + C;                      // [C/32] square scales
+  __shared__ __align__(8) uint64_t bar[1];
+  __shared__ int abort_flag;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31, t = threadIdx.x;
-  const int64_t row = int64_t(blockIdx.x) * 32 + w;
-  const bool valid = row < a.T;
+  const int64_t nblk = (a.T + 31) / 32;
   const bool want_cs = a.col_data || a.sq_data;
-  const int64_t seg = row / a.seg_len;       // sequence of this row (packed layouts)
-  const int64_t pos = row % a.seg_len;       // position in the sequence
-  const int64_t tiles_per_seq = a.seg_len / 128;
-  const int64_t tile_g = seg * tiles_per_seq + pos / 128;
-  const int rr = int(pos % 128);
-  const int kb4 = int(pos % 128) / 32;  // same for all rows of the CTA (seg_len % 32 == 0)
-
-  uint4 xv[NK];
-#pragma unroll
-  for (int k = 0; k < NK; k++)
-    xv[k] = valid ? ldg16(a.x + row * C + 256 * k + 8 * l) : make_uint4(0, 0, 0, 0);
-
-  float ss = 0.0f;
-#pragma unroll
-  for (int k = 0; k < NK; k++) {
-    const uint32_t wv[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      float lo = bf_lo(wv[j]), hi = bf_hi(wv[j]);
-      ss = __fadd_rn(ss, __fmul_rn(lo, lo));
-      ss = __fadd_rn(ss, __fmul_rn(hi, hi));
-    }
+  const uint32_t bar_a = smem_u32(bar);
+  if (t == 0) {
+    abort_flag = 0;
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
   }
+  __syncthreads();
+  auto issue_load = [&](int64_t rb) {
+    const int64_t left = a.T - rb * 32;
+    const int nr = left < 32 ? int(left) : 32;
+    const uint32_t bytes = uint32_t(nr) * C * 2;
+    mbar_arrive_expect_tx(bar_a, bytes);
+    bulk_load(smem_u32(sx), a.x + rb * 32 * C, bytes, bar_a);
+  };
+  if (t == 0 && int64_t(blockIdx.x) < nblk) issue_load(blockIdx.x);
+  // gamma, the same for every block, into shared memory once
+  for (int i = t; i < C / 4; i += rms::NTHREADS)
+    reinterpret_cast<float4*>(sgm)[i] = __ldg(reinterpret_cast<const float4*>(a.gamma) + i);
+  __syncthreads();
+  int it = 0;
+  bool pending = int64_t(blockIdx.x) < nblk;  // a bulk copy is in flight
+  for (int64_t rb = blockIdx.x; rb < nblk; rb += gridDim.x, it++) {
+    const bool got = mbar_wait(bar_a, it & 1, &abort_flag, &g_status_quant);
+    if (!__syncthreads_and(got)) break;
+    pending = false;
+    const int64_t row = rb * 32 + w;
+    const bool valid = row < a.T;
+    const int64_t seg = (rb * 32) / a.seg_len;  // sequence of the block (seg_len % 32 == 0)
+    const int64_t pos0 = (rb * 32) % a.seg_len;
+    const int64_t tile_g = seg * (a.seg_len / 128) + pos0 / 128;
+    const int kb4 = int(pos0 % 128) / 32;
+    const int rr = int(pos0 % 128) + w;
+    // this row's slice, read from shared memory where needed (twice)
+    auto xs = [&](int k) {
+      return valid ? *reinterpret_cast<const uint4*>(sx + (w * C + 256 * k + 8 * l) * 2) : make_uint4(0, 0, 0, 0);
+    };
+    float ss = 0.0f;
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
-  const float mean = __fdiv_rn(ss, float(C));
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
-
+    for (int k = 0; k < NK; k++) {
+      const uint4 xk = xs(k);
+      const uint32_t wv[4] = {xk.x, xk.y, xk.z, xk.w};
 #pragma unroll
-  for (int k = 0; k < NK; k++) {
-    const int c0 = 256 * k + 8 * l;
-    const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0));
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0 + 4));
-    const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    const uint32_t wv[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
-    float y[8];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      y[2 * j] = __fmul_rn(__fmul_rn(bf_lo(wv[j]), r), gm[2 * j]);
-      y[2 * j + 1] = __fmul_rn(__fmul_rn(bf_hi(wv[j]), r), gm[2 * j + 1]);
-    }
-    uint32_t am = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) am = max(am, __float_as_uint(y[j]) & 0x7FFFFFFFu);
-    const int h = c0 / a.D, d0 = c0 % a.D;
-
-    if (a.row_data) {  // 1x32 along C: 4 lanes per block
-      uint32_t m = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      uint32_t s = m >= 0x7F800000u ? 0xFFu : e8m0_from_amax(__uint_as_float(m));
-      float f = s == 0xFFu ? 0.0f : e8m0_inv_scale(s);
-      uint2 out;
-      out.x = pack4_e4m3(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
-      out.y = pack4_e4m3(y[4] * f, y[5] * f, y[6] * f, y[7] * f);
-      if (s == 0xFFu) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-      if (valid) {
-        *reinterpret_cast<uint2*>(a.row_data + row * C + c0) = out;
-        if ((l & 3) == 0) {
-          if (a.row_sfc) a.row_sfc[row * (C / 32) + c0 / 32] = uint8_t(s);
-          if (a.row_sfp) a.row_sfp[(tile_g * a.H + h) * 512 + atom_off(rr, d0 / 32)] = uint8_t(s);
-        }
+      for (int j = 0; j < 4; j++) {
+        const float lo = bf_lo(wv[j]), hi = bf_hi(wv[j]);
+        ss = __fadd_rn(ss, __fmul_rn(lo, lo));
+        ss = __fadd_rn(ss, __fmul_rn(hi, hi));
       }
     }
-    if (want_cs) {
 #pragma unroll
-      for (int j = 0; j < 8; j++) sm_abs[w][8 * l + j] = __float_as_uint(y[j]) & 0x7FFFFFFFu;
-      __syncthreads();
-      {
-        const int c = t & 255, part = t >> 8;
-        uint32_t m = 0;
+    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, float(C)), a.eps)));
+    // row (1x32) output and the exponent bytes of |y|
 #pragma unroll
-        for (int i = 0; i < 8; i++) m = max(m, sm_abs[part * 8 + i][c]);
-        sm_part[part][c] = m;
+    for (int k = 0; k < NK; k++) {
+      const int c0 = 256 * k + 8 * l;
+      const uint4 xk = xs(k);
+      const uint32_t wv[4] = {xk.x, xk.y, xk.z, xk.w};
+      const float4 g0 = *reinterpret_cast<const float4*>(sgm + c0);
+      const float4 g1 = *reinterpret_cast<const float4*>(sgm + c0 + 4);
+      const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        y[2 * j] = rms_y(wv[j], false, r, gm[2 * j]);
+        y[2 * j + 1] = rms_y(wv[j], true, r, gm[2 * j + 1]);
       }
-      __syncthreads();
-      if (t < 256) {
-        uint32_t m = max(max(sm_part[0][t], sm_part[1][t]), max(sm_part[2][t], sm_part[3][t]));
-        const int cc = 256 * k + t, hh = cc / a.D, dd = cc % a.D;
-        uint32_t s = m >= 0x7F800000u ? 0xFFu : e8m0_from_amax(__uint_as_float(m));
-        sm_colinv[t] = s == 0xFFu ? 0.0f : e8m0_inv_scale(s);
-        sm_colbad[t] = s == 0xFFu;
-        if (a.col_data) {
-          if (a.col_sfc) a.col_sfc[int64_t(blockIdx.x) * C + cc] = uint8_t(s);
-          if (a.col_sfp) a.col_sfp[(tile_g * a.H + hh) * 512 + atom_off(dd, kb4)] = uint8_t(s);
-        }
-        // one warp = 32 columns = one square block
-        uint32_t bm = m;
+      // exponent bytes of |y| (y's bits shifted left by one hold the exponent
+      // in their top byte), four per word
+      uint32_t u[8];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, off));
-        if (l == 0) {
-          uint32_t sq = bm >= 0x7F800000u ? 0xFFu : e8m0_from_amax(__uint_as_float(bm));
-          sm_sqinv[w] = sq == 0xFFu ? -1.0f : e8m0_inv_scale(sq);
-          if (a.sq_data) {
-            if (a.sq_sfc) a.sq_sfc[int64_t(blockIdx.x) * (C / 32) + 8 * k + w] = uint8_t(sq);
-            if (a.sq_sfp) a.sq_sfp[(tile_g * a.H + hh) * 16 + kb4 * 4 + dd / 32] = uint8_t(sq);
+      for (int j = 0; j < 8; j++) u[j] = __float_as_uint(y[j]) * 2u;
+      const uint32_t e0 = __byte_perm(__byte_perm(u[0], u[1], 0x0073), __byte_perm(u[2], u[3], 0x0073), 0x5410);
+      const uint32_t e1 = __byte_perm(__byte_perm(u[4], u[5], 0x0073), __byte_perm(u[6], u[7], 0x0073), 0x5410);
+      if (want_cs) *reinterpret_cast<uint2*>(sexp + w * C + c0) = make_uint2(e0, e1);
+      if (a.row_data) {  // 1x32 along C: 4 lanes per block; the scale reads only the max exponent
+        uint32_t em = __vmaxu4(e0, e1);
+        em = __vmaxu4(em, em >> 16);
+        uint32_t e = max(em & 0xFFu, (em >> 8) & 0xFFu);
+        e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
+        e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 2));
+        const uint32_t s = e8m0_from_exp(e);
+        const float f = e8m0_inv_scale(s);
+        uint2 out;
+        out.x = pack4_e4m3(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
+        out.y = pack4_e4m3(y[4] * f, y[5] * f, y[6] * f, y[7] * f);
+        if (s == 0xFFu) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        if (valid) {
+          *reinterpret_cast<uint2*>(a.row_data + row * C + c0) = out;
+          if ((l & 3) == 0) {
+            const int h = c0 / a.D, d0 = c0 % a.D;
+            if (a.row_sfc) a.row_sfc[row * (C / 32) + c0 / 32] = uint8_t(s);
+            if (a.row_sfp) a.row_sfp[(tile_g * a.H + h) * 512 + atom_off(rr, d0 / 32)] = uint8_t(s);
           }
         }
       }
-      __syncthreads();
-      if (valid && a.col_data) {
-        uint2 out;
-        const float* ci = sm_colinv + 8 * l;
-        out.x = pack4_e4m3(y[0] * ci[0], y[1] * ci[1], y[2] * ci[2], y[3] * ci[3]);
-        out.y = pack4_e4m3(y[4] * ci[4], y[5] * ci[5], y[6] * ci[6], y[7] * ci[7]);
-        uint8_t* ob = reinterpret_cast<uint8_t*>(&out);
+    }
+    // every thread has its slice and its exponent bytes: the next block may land
+    __syncthreads();
+    if (t == 0 && rb + gridDim.x < nblk) {
+      issue_load(rb + gridDim.x);
+      pending = true;
+    }
+    if (!want_cs) continue;
+    // column scales (4 columns per thread) and square scales (8 threads per block)
+    if (t < C / 4) {
+      uint32_t m = 0;
+#pragma unroll 8
+      for (int rw = 0; rw < 32; rw++) m = __vmaxu4(m, *reinterpret_cast<const uint32_t*>(sexp + rw * C + 4 * t));
+      uint32_t sw = 0;
 #pragma unroll
-        for (int j = 0; j < 8; j++)
-          if (sm_colbad[8 * l + j]) ob[j] = 0x7F;
+      for (int i = 0; i < 4; i++) sw |= e8m0_from_exp((m >> (8 * i)) & 0xFFu) << (8 * i);
+      *reinterpret_cast<uint32_t*>(scol + 4 * t) = sw;
+      *reinterpret_cast<float4*>(scinv + 4 * t) =
+          make_float4(e8m0_inv_scale(sw & 0xFFu), e8m0_inv_scale((sw >> 8) & 0xFFu),
+                      e8m0_inv_scale((sw >> 16) & 0xFFu), e8m0_inv_scale(sw >> 24));
+      if (a.col_data) {
+        if (a.col_sfc) *reinterpret_cast<uint32_t*>(a.col_sfc + rb * C + 4 * t) = sw;
+        if (a.col_sfp) {
+          const int hh = (4 * t) / a.D, dd = (4 * t) % a.D;
+#pragma unroll
+          for (int i = 0; i < 4; i++)
+            a.col_sfp[(tile_g * a.H + hh) * 512 + atom_off(dd + i, kb4)] = uint8_t(sw >> (8 * i));
+        }
+      }
+      uint32_t bm = m;
+      bm = __vmaxu4(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
+      bm = __vmaxu4(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 2));
+      bm = __vmaxu4(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 4));
+      if ((t & 7) == 0) {
+        const uint32_t e = max(max(bm & 0xFFu, (bm >> 8) & 0xFFu), max((bm >> 16) & 0xFFu, bm >> 24));
+        const uint32_t sq = e8m0_from_exp(e);
+        ssq[t >> 3] = uint8_t(sq);
+        if (a.sq_data) {
+          const int cc = 4 * t, hh = cc / a.D, dd = cc % a.D;
+          if (a.sq_sfc) a.sq_sfc[rb * (C / 32) + (t >> 3)] = uint8_t(sq);
+          if (a.sq_sfp) a.sq_sfp[(tile_g * a.H + hh) * 16 + kb4 * 4 + dd / 32] = uint8_t(sq);
+        }
+      }
+    }
+    __syncthreads();
+    if (!valid) continue;
+#pragma unroll
+    for (int k = 0; k < NK; k++) {
+      const int c0 = 256 * k + 8 * l;
+      const uint4 xk = ldg16(a.x + row * C + c0);  // from L2: this block was just copied
+      const uint32_t wv[4] = {xk.x, xk.y, xk.z, xk.w};
+      const float4 g0 = *reinterpret_cast<const float4*>(sgm + c0);
+      const float4 g1 = *reinterpret_cast<const float4*>(sgm + c0 + 4);
+      const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        y[2 * j] = rms_y(wv[j], false, r, gm[2 * j]);
+        y[2 * j + 1] = rms_y(wv[j], true, r, gm[2 * j + 1]);
+      }
+      if (a.col_data) {
+        const float4 i0 = *reinterpret_cast<const float4*>(scinv + c0);
+        const float4 i1 = *reinterpret_cast<const float4*>(scinv + c0 + 4);
+        uint2 out;
+        out.x = pack4_e4m3(y[0] * i0.x, y[1] * i0.y, y[2] * i0.z, y[3] * i0.w);
+        out.y = pack4_e4m3(y[4] * i1.x, y[5] * i1.y, y[6] * i1.z, y[7] * i1.w);
+        // columns with Inf / NaN (scale 0xFF) carry 0x7F payloads
+        const uint2 sw = *reinterpret_cast<const uint2*>(scol + c0);
+        const uint32_t b0 = __vcmpeq4(sw.x, 0xFFFFFFFFu), b1 = __vcmpeq4(sw.y, 0xFFFFFFFFu);
+        out.x = (out.x & ~b0) | (0x7F7F7F7Fu & b0);
+        out.y = (out.y & ~b1) | (0x7F7F7F7Fu & b1);
         *reinterpret_cast<uint2*>(a.col_data + row * C + c0) = out;
       }
-      if (valid && a.sq_data) {
-        const float f = sm_sqinv[l >> 2];
+      if (a.sq_data) {
+        const uint32_t s = ssq[c0 >> 5];
         uint2 out;
-        if (f < 0.0f) {
+        if (s == 0xFFu) {
           out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
+          const float f = e8m0_inv_scale(s);
           out.x = pack4_e4m3(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
           out.y = pack4_e4m3(y[4] * f, y[5] * f, y[6] * f, y[7] * f);
         }
         *reinterpret_cast<uint2*>(a.sq_data + row * C + c0) = out;
       }
-      __syncthreads();
     }
   }
+  // a copy issued before a failed wait still lands before the CTA exits
+  if (t == 0 && pending) {
+    unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_sleep(bar_a, it & 1))
+      if (global_ns() - t0 > kWaitLimitNs) break;
+  }
+  __syncthreads();
+}
+
+template <int NK>
+cudaError_t launch_rms_nk(const RmsArgs& a, cudaStream_t st) {
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(rms_quant_kernel<NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               rms::smem_bytes(NK * 256));
+    if (e != cudaSuccess) {
+      nsm = 0;
+      return e;
+    }
+  }
+  const int64_t nblk = (a.T + 31) / 32;
+  const unsigned grid = unsigned(nblk < nsm ? nblk : int64_t(nsm));
+  rms_quant_kernel<NK><<<grid, rms::NTHREADS, rms::smem_bytes(NK * 256), st>>>(a);
+  return cudaPeekAtLastError();
 }
 
 cudaError_t launch_rmsnorm_quant(const RmsArgs& a, cudaStream_t st) {
-  dim3 grid(unsigned((a.T + 31) / 32));
-  if (grid.x == 0) return cudaSuccess;
+  if (a.T <= 0) return cudaSuccess;
   switch (a.C) {
-    case 256: rms_quant_kernel<1><<<grid, 1024, 0, st>>>(a); break;
-    case 512: rms_quant_kernel<2><<<grid, 1024, 0, st>>>(a); break;
-    case 1024: rms_quant_kernel<4><<<grid, 1024, 0, st>>>(a); break;
-    case 2048: rms_quant_kernel<8><<<grid, 1024, 0, st>>>(a); break;
+    case 256: return launch_rms_nk<1>(a, st);
+    case 512: return launch_rms_nk<2>(a, st);
+    case 1024: return launch_rms_nk<4>(a, st);
+    case 2048: return launch_rms_nk<8>(a, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaPeekAtLastError();
 }
 
 unsigned read_status_quant(cudaStream_t st) {

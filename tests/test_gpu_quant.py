@@ -130,3 +130,23 @@ def test_rmsnorm_quant_full_fused_config(mx):
     for name in ("row", "col", "sq"):
         np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
         np.testing.assert_array_equal(host(res[name].sf_compact), ref[name][1], err_msg=name)
+
+
+def test_rmsnorm_quant_inf_nan_rows(mx):
+    # an Inf and a NaN in the input: their rows normalise to NaN / 0 values,
+    # so row, column and square blocks holding them take scale 0xFF and 0x7F
+    # payloads, exactly as the oracle's OCP rule says
+    import torch
+    T, C, H, seg = 96, 256, 2, 32
+    x = inputs.normal_bf16((T, C), 9)
+    x[5, 10] = 0x7F80   # +Inf (bf16 bits)
+    x[40, 100] = 0x7FC0  # NaN
+    g = np.random.default_rng(10).uniform(0.5, 1.5, C).astype(np.float32)
+    res = mx.rmsnorm_quant(to_dev(x), torch.from_numpy(g).cuda(), 1e-6, seg, H, packed=False)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    ref = oracle.rmsnorm_quant(inputs.bf16_bits_to_f32(x), g, 1e-6, 7, seg)
+    assert (ref["col"][1] == 0xFF).any() and (ref["row"][1] == 0xFF).any()
+    for name in ("row", "col", "sq"):
+        np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
+        np.testing.assert_array_equal(host(res[name].sf_compact), ref[name][1], err_msg=name)
