@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         const int s = jj % NSQ, b = jj & 1;
         // P^T, dS^T and their scale atoms written; the tile record in place;
         // the dQ^T accumulator drained
-        if (!wait_all(BAR(B_PATOM + b), (jj >> 1) & 1) || !wait_all(BAR(B_QDOFULL + s), (jj / NSQ) & 1))
+        if (!wait_all(BAR(B_QDOFULL + s), (jj / NSQ) & 1) || !wait_all(BAR(B_PATOM + b), (jj >> 1) & 1))
           return false;
         tc_fence_after();
         // slot b was last read by tile jj - 2's MMAs, earlier in this stream
@@ -486,13 +486,20 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       tc_fence_after();
       tmem_ld32(tmem + lane_base + COL_S + 32 * hq, reinterpret_cast<uint32_t*>(sv));
       tmem_ld32(tmem + lane_base + COL_DP + 32 * hq, reinterpret_cast<uint32_t*>(dp));
+      // the tile's record and the P^T / dS^T buffer are nearly always ready by
+      // now: test both while the loads are in flight, wait only if needed
+      const bool rec_ready = mbar_test(BAR(B_QDOFULL + s), (ii / NSQ) & 1);
+      const bool buf_ready = ii < 2 || mbar_test(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1);
       tmem_wait_ld();
       reg_fence32(reinterpret_cast<uint32_t*>(sv));
       reg_fence32(reinterpret_cast<uint32_t*>(dp));
       tc_fence_before();
       warp_arrive(BAR(B_SDPFREE), lane);  // completion ii + 1
       // -lse * log2 e and -Delta of the tile, from the stage's record
-      if (!wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag)) { ok = false; break; }
+      if (!__all_sync(0xFFFFFFFFu, rec_ready) && !wwait(BAR(B_QDOFULL + s), (ii / NSQ) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
       {
         const float2* nl2 = reinterpret_cast<const float2*>(rec + REC_NL2) + 16 * hq;
@@ -539,7 +546,10 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           dw[c] = cvt_e4m3x2(d01.x, d01.y) | (cvt_e4m3x2(d23.x, d23.y) << 16);
         }
       }
-      if (ii >= 2 && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      if (!__all_sync(0xFFFFFFFFu, buf_ready) && !wwait(BAR(B_PDSEMPTY + b), ((ii >> 1) - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       {
         uint8_t* pt = smem + OFF_PT + b * PS_BYTES;
         uint8_t* dst = smem + OFF_DST + b * PS_BYTES;
