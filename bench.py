@@ -9,11 +9,13 @@ reduction.  value = algorithmic PFLOP/s of the step (forward 4*D and backward
 10*D FLOPs per unmasked (query, key) pair, S^2/2 pairs per causal head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxfa|reference]
-  python bench.py --profile-op fwd|bwd|rmsnorm [--profile-seq S] [--profile-batch B] [--steps K] [--warmup W]
+  python bench.py --profile-op fwd|bwd|rmsnorm|quant_row|quant_col|quant_sq [--profile-seq S]
+                   [--profile-batch B] [--steps K] [--warmup W]
 
 One JSON line on rank 0.  --profile-op runs W + K launches of one operation
 on a causal case (B=--profile-batch, H=16, S=--profile-seq; for rmsnorm the
-fused producer's X[32768, 2048] with row and column outputs) for kernel
+fused producer's X[32768, 2048] with row and column outputs; for quant_* one
+quantization of the benchmark's Q tensor into packed scales) for kernel
 profiling, and prints its timing instead of the benchmark line.
 
 Under torchrun (N > 1) every rank runs the same
@@ -63,7 +65,8 @@ def parse():
     p.add_argument("--impl", default="mxfa", choices=["mxfa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-components", action="store_true")
-    p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm"], default=None)
+    p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm", "quant_row", "quant_col",
+                                            "quant_sq"], default=None)
     p.add_argument("--profile-seq", type=int, default=4096)
     p.add_argument("--profile-batch", type=int, default=1)
     return p.parse_args()
@@ -384,6 +387,23 @@ def profile_op(args):
                           "ms": ms, "GB_s": nb / ms / 1e6}), flush=True)
         return 0
     b, s = args.profile_batch, args.profile_seq
+    if args.profile_op.startswith("quant"):
+        blk = {"quant_row": 0, "quant_col": 1, "quant_sq": 2}[args.profile_op]
+        qb = inputs.normal_bf16((B, S, H, D), SEED)
+        dev = torch.device("cuda", 0)
+        q = torch.from_numpy(qb.view("int16")).view(torch.bfloat16).reshape(B * S, H, D).to(dev)
+        seqs = mxfa.Seqs.dense(B, S)
+        m = mxfa.quantize(q, blk, seqs)
+        out = mxfa.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+        run = lambda: mxfa.mxfa_quantize(q, seqs.total, H, D, blk, None, seqs.nseq, seqs.max_len,
+                                         seqs.ptiles, out)
+        ms = time_loop(torch, run, args.steps, args.warmup)
+        assert mxfa.device_status() == 0, "device status"
+        n = B * S * H * D
+        nb = n * (2 + 1 + (1 / 1024 if blk == 2 else 1 / 32))
+        print(json.dumps({"profile_op": args.profile_op, "shape": [B * S, H, D], "ms": ms,
+                          "GB_s": nb / ms / 1e6}), flush=True)
+        return 0
     qb, kb, vb, dob = inputs.dense_attn(b, H, s, D, seed=SEED)
     dev = torch.device("cuda", 0)
     t = lambda x: torch.from_numpy(x.view("int16")).view(torch.bfloat16).reshape(b * s, H, D).to(dev)
