@@ -513,21 +513,38 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
             if (!kvalid || (a.causal && kpos > q0 + c)) sv[c] = -INFINITY;
         }
         const float2 sl2v = make_float2(sl2, sl2);
+        // exponent arguments t = fl(S * fl(scale * log2 e) - lse * log2 e)
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 t = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, nl2[c / 2]);
+          sv[c] = t.x;
+          sv[c + 1] = t.y;
+          tmax = fmax3(tmax, t.x, t.y);
+        }
+        // P <= 1: exact attention has S * scale <= lse, but S recomputed from
+        // the square-block operands can exceed the forward's lse (by hundreds
+        // when outliers meet coarse shared scales), so t is clamped at 0
+        if (tmax > 0.0f) {
+#pragma unroll
+          for (int c = 0; c < 32; c++) sv[c] = fminf(sv[c], 0.0f);
+          tmax = 0.0f;
+        }
         float dmax = 0.0f, dmin = 0.0f;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          // P = 2^fl(S * fl(scale * log2 e) - lse * log2 e), dS = P * (dP - Delta)
-          const float2 t = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, nl2[c / 2]);
-          const float p0 = bex2(t.x), p1 = bex2(t.y);
+          // P = 2^t, dS = P * (dP - Delta)
+          const float p0 = bex2(sv[c]), p1 = bex2(sv[c + 1]);
           const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp[c], dp[c + 1]), ndl[c / 2]));
           sv[c] = p0;
           sv[c + 1] = p1;
           dp[c] = ds.x;
           dp[c + 1] = ds.y;
-          pmax = fmax3(pmax, p0, p1);
           dmax = fmax3(dmax, ds.x, ds.y);
           dmin = fmin3(dmin, ds.x, ds.y);
         }
+        // the largest P of this thread's block (2^t is monotone in t)
+        pmax = bex2(tmax);
         // P^T: one 1x32 block along queries per thread; dS: one 32x32 block
         // per warp, its maximum by a warp-wide absolute-maximum reduction
         float wmax;

@@ -389,7 +389,10 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  * row-block operand; o_bf and do_bf are the bf16 O and dO (as fp64 values);
  * lse[head][query token] from the forward pass.  Per sequence and head:
  *   Delta_i = sum_d dO_bf[i,d] * O_bf[i,d]
- *   P_ij = exp(q_i.k_j * scale - lse_i)      (0 where masked; < 2^-126 -> 0)
+ *   P_ij = exp(min(q_i.k_j * scale - lse_i, 0))   (0 where masked; < 2^-126 -> 0)
+ *   The min keeps P <= 1, the bound exact attention obeys: the square-block
+ *   operands recompute S differently from the forward's row-block operands,
+ *   and with outliers S * scale can exceed the forward's lse by hundreds.
  *   dP_ij = dO_i.v_j;   dS_ij = P_ij (dP_ij - Delta_i)
  *   P^ : P quantized in 1x32 blocks along queries (per key), quant_p
  *   dS^: dS quantized in 32x32 blocks, quant_ds
@@ -397,8 +400,8 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  *   dV_j = sum_i P^_ij dO_i;  dK_j = scale sum_i dS^_ij q_i;
  *   dQ_i = scale sum_j dS^_ij k_j.
  * score_fp32 = 1: S, dP, Delta rounded to fp32 and
- *   P = fl(2^fma(S, fl(scale * log2 e), -fl(lse * log2 e))) (one rounding of
- *   the exponent argument), dS = fl(P * fl(dP - Delta)): the fp32 steps of a
+ *   P = fl(2^min(fma(S, fl(scale * log2 e), -fl(lse * log2 e)), 0)) (one
+ *   rounding of the exponent argument), dS = fl(P * fl(dP - Delta)): the fp32 steps of a
  *   kernel that evaluates the exponent with a fused multiply-add. */
 void mxo_attn_bwd(const double* q, const double* k, const double* v,
                   const double* dO, const double* o_bf, const double* do_bf,
@@ -434,7 +437,7 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
           }
           if (score_fp32) { /* fp32 S, dP (MMA outputs) and fp32 elementwise steps */
             volatile float l2 = (float)li * 1.4426950408889634f;
-            volatile float arg = fmaf((float)s, sl2f, -l2);
+            volatile float arg = fminf(fmaf((float)s, sl2f, -l2), 0.0f);
             volatile float pf = (float)exp2((double)arg);
             double p = flush_fp32_subnormal((double)pf);
             volatile float diff = (float)dp - (float)delta;
@@ -442,7 +445,7 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
             P[i * lk + j] = p;
             dS[i * lk + j] = dsf;
           } else {
-            double p = flush_fp32_subnormal(exp(s * scale - li));
+            double p = flush_fp32_subnormal(exp(fmin(s * scale - li, 0.0)));
             P[i * lk + j] = p;
             dS[i * lk + j] = p * (dp - delta);
           }

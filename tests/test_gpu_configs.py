@@ -1,0 +1,252 @@
+"""The remaining workloads of the method on the GPU, each against the oracle:
+the outlier recipe through the backward, the jagged cross-attention
+batch (sampled sequences, every head), and the fused RMSNorm+Quantize producer
+feeding the attention forward and backward directly from its own outputs.
+
+Bars as in the forward and backward parity tests: O relative Frobenius
+<= 1e-2 and max-abs <= 3e-2 (plus the bf16 output spacing), lse max-abs
+<= 1e-4, dQ / dK / dV relative Frobenius <= 3e-2; quantized payloads and
+scales bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from mxfp8_block_scaled_fa_gb300 import inputs
+from tests.helpers import f64, host, to_dev
+from tests.test_gpu_bwd import check as grad_check
+from tests.test_gpu_bwd import gpu_bwd, oracle_fwd_out
+from tests.test_gpu_fwd import check as fwd_check
+from tests.test_gpu_fwd import gpu_fwd
+
+pytestmark = pytest.mark.gpu
+
+THR = 8.0
+D = 128
+SCALE = 1 / math.sqrt(D)
+
+
+def oracle_fwd_full(qf, kf, vf, cu_q, cu_k, causal):
+    """The oracle forward -> (O float64, lse, O as bf16 bits, O bf16 as float64)."""
+    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, SCALE, causal, True, 128, THR, True)
+    o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
+    return o, lse, o_bits, f64(o_bits)
+
+
+def fwd_check_envelope(o, lse, qd, kd, vd, causal, oo, lo, eps=1e-7, seeds=(0, 1, 2)):
+    """fwd_check, where every P code is unique, and an envelope elsewhere.
+
+    Rows dominated by a few keys (the outlier recipe's scores reach 1e5) put
+    single P elements within an fp32 ulp of an E4M3 rounding boundary; the
+    tensor core's fp32 summation order is unspecified, so such a row has more
+    than one correct O.  The oracle reruns with K (dequantized) scaled by
+    1 + eps * N(0,1) per element, an ulp-sized change of every score: rows
+    whose O moves by more than 1e-3 are the non-unique ones, must be rare (under
+    1% of rows), and are held to the bar plus the spread of those reruns; all
+    other rows and the whole-tensor relative Frobenius are held to the plain bar.
+    The lse bar adds the fp32 summation bound of the row's scores.
+    """
+    from tests.test_gpu_fwd import O_ABS, O_REL, _spacing
+    from tests.helpers import rel_fro
+    spread = np.zeros_like(oo)
+    for sd in seeds:
+        rng = np.random.default_rng(sd)
+        kp = kd * (1 + eps * rng.standard_normal(kd.shape))
+        ov, _ = oracle.attn_fwd(qd, kp, vd, None, None, SCALE, causal, True, 128, THR, True)
+        spread = np.maximum(spread, np.abs(ov - oo))
+    unstable = spread.max(axis=(1, 2)) > 1e-3
+    assert unstable.sum() <= 0.01 * len(unstable), unstable.sum()
+    assert rel_fro(o, oo) <= O_REL, rel_fro(o, oo)
+    excess = np.abs(o - oo) - 0.5 * _spacing(oo, 7) - np.where(unstable[:, None, None], spread, 0)
+    assert excess.max() <= O_ABS, excess.max()
+    # lse: each score is an fp32 sum over four 32-element K steps, so it may
+    # differ from the exactly rounded score by 8 * 2^-24 * sum_d |q_d k_d|;
+    # the outlier products (up to 1e7) make this the dominant term
+    acc = np.stack([(np.abs(qd[:, hh]) @ np.abs(kd[:, hh]).T).max(axis=1)
+                    for hh in range(qd.shape[1])]) * SCALE * 2.0 ** -21
+    lexcess = np.abs(lse - lo) - 4 * _spacing(lo, 23) - acc
+    assert lexcess.max() <= 1e-4, lexcess.max()
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import torch
+    from mxfp8_block_scaled_fa_gb300 import build, mxfa
+    build.build()
+    assert torch.cuda.is_available()
+    return mxfa
+
+
+@pytest.mark.parametrize("outliers_v,dq_mode,dq_static", [(False, 0, 1.0), (True, 0, 1.0),
+                                                          (True, 1, 1.0)])
+def test_bwd_outliers_small(mx, outliers_v, dq_mode, dq_static):
+    # the outlier recipe (1% of Q/K channels x20, 0.1% of elements x200)
+    # through the backward: square-block scales of Q, K and dO see the
+    # outliers, and the online dS quantization sees their large scores
+    import torch
+    B, H, S = 1, 4, 512
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=12, outliers=True, outliers_v=outliers_v)
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    o_bits, o_bf, lse = oracle_fwd_out(f(qb), f(kb), f(vb), None, None, SCALE, False)
+    seqs = mx.Seqs.dense(B, S)
+    lse_dev = torch.from_numpy(lse.reshape(H, B, S).transpose(1, 0, 2).astype(np.float32).copy())
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse_dev.cuda(), seqs, seqs, SCALE, False, dq_mode,
+                  dq_static)
+    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lse, None, None, SCALE, False,
+                            True, True)
+    grad_check(got, ref, "outliers")
+
+
+def test_outlier_config_sampled_heads(mx):
+    # the full non-causal outlier workload (B8 H32 S4096) forward and backward
+    # on the GPU; the oracle recomputes sampled (batch, head) pairs in full
+    import torch
+    B, H, S = 8, 32, 4096
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=2, outliers=True)
+    seqs = mx.Seqs.dense(B, S)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o, lse = mx.attention_fwd(q, k, v, seqs, seqs, SCALE, causal=False)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    del q, k, v
+    o_host = host(o.float()).astype(np.float64).reshape(B, S, H, D)
+    o_bits = host(o.view(torch.int16)).view(np.uint16).reshape(B, S, H, D).copy()
+    lse_host = host(lse).reshape(B, H, S)
+    sampled = ((0, 0), (5, 17), (7, 31))
+    sl = lambda x, b, h: f64(x[b, :, h:h + 1, :])
+    fwd_ref = {}
+    for b, h in sampled:
+        oo, lo, ob, obf = oracle_fwd_full(sl(qb, b, h), sl(kb, b, h), sl(vb, b, h), None, None,
+                                          False)
+        fwd_check_envelope(o_host[b, :, h:h + 1, :], lse_host[b, h:h + 1, :],
+                           oracle.qdq(sl(qb, b, h), 0), oracle.qdq(sl(kb, b, h), 0),
+                           oracle.qdq(sl(vb, b, h), 1), False, oo, lo)
+        fwd_ref[b, h] = (obf, lo)
+        # the backward of this head runs from the oracle's O and lse
+        o_bits[b, :, h, :] = ob.reshape(S, D)
+        lse.view(B, H, S)[b, h].copy_(torch.from_numpy(lo.reshape(S).astype(np.float32)).cuda())
+    del o
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, SCALE, False)
+    got = [g.reshape(B, S, H, D) for g in got]
+    for b, h in sampled:
+        obf, lo = fwd_ref[b, h]
+        ref = oracle.method_bwd(sl(qb, b, h), sl(kb, b, h), sl(vb, b, h), sl(dob, b, h), obf, lo,
+                                None, None, SCALE, False, True, True)
+        grad_check([g[b, :, h:h + 1, :] for g in got], ref, f"outlier b{b} h{h}")
+
+
+def test_jagged_config_sampled_sequences(mx):
+    # the jagged cross-attention batch on the GPU: 64 sequences, query lengths
+    # U[64, 2048], key lengths U[32, 1024], H8, non-causal; the oracle
+    # recomputes every head of eight sequences (the extremes of both length
+    # distributions and four drawn at random), and the backward of those
+    # sequences runs from the oracle's O and lse
+    import torch
+    qb, kb, vb, dob, cu_q, cu_k = inputs.jagged_attn()
+    lq, lk = cu_q[1:] - cu_q[:-1], cu_k[1:] - cu_k[:-1]
+    sq, sk = mx.Seqs.varlen(lq, "cuda"), mx.Seqs.varlen(lk, "cuda")
+    o, lse = gpu_fwd(mx, qb, kb, vb, sq, sk, SCALE, False)
+    picks = {int(np.argmax(lq)), int(np.argmin(lq)), int(np.argmax(lk)), int(np.argmin(lk))}
+    picks |= set(np.random.default_rng(5).choice(len(lq), 4, replace=False).tolist())
+    o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
+    lse_all = lse.copy()
+    fwd_ref = {}
+    for i in sorted(picks):
+        rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
+        oo, lo, ob, obf = oracle_fwd_full(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), None, None, False)
+        fwd_check(o[rq], lse[:, rq], oo, lo)
+        fwd_ref[i] = (obf, lo)
+        o_bits[rq] = ob
+        lse_all[:, rq] = lo
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse_all.astype(np.float32)).cuda(),
+                  sq, sk, SCALE, False)
+    for i in sorted(picks):
+        rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
+        obf, lo = fwd_ref[i]
+        ref = oracle.method_bwd(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), f64(dob[rq]), obf, lo, None,
+                                None, SCALE, False, True, True)
+        grad_check([got[0][rq], got[1][rk], got[2][rk]], ref, f"jagged seq {i}")
+
+
+def _fused_chain(mx, x, g, dob, B, S, H):
+    """RMSNorm+Quantize on the GPU, then causal self-attention forward and
+    backward on its outputs: the 1x32 row layout is Q and K of the forward
+    and V of the backward, the 32x1 column layout is V of the forward, the
+    32x32 square layout is Q and K of the backward."""
+    import torch
+    T, C = x.shape
+    res = mx.rmsnorm_quant(to_dev(x), torch.from_numpy(g).cuda(), 1e-6, S, H)
+    view = lambda m: mx.Mx(m.data.view(T, H, D), m.sf_compact, m.sf_packed, m.blk)
+    row, col, sqr = view(res["row"]), view(res["col"]), view(res["sq"])
+    seqs = mx.Seqs.dense(B, S)
+    o, lse = mx.attention_fwd(row, row, col, seqs, seqs, SCALE, causal=True)
+    do_t = to_dev(dob)
+    grads = mx.attention_bwd(sqr, sqr, row, mx.quantize(do_t, mx.SQ, seqs), o,
+                             do_t.reshape(T, H, D), lse, seqs, seqs, SCALE, causal=True)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    return res, o, lse, grads
+
+
+def _oracle_operands(x, g, S, H, rows=None):
+    """The oracle's RMSNorm+Quantize outputs, dequantized to [tokens, H, D]."""
+    T, C = x.shape
+    ref = oracle.rmsnorm_quant(inputs.bf16_bits_to_f32(x), g, 1e-6, 7, S)
+    cu = np.arange(0, T + S, S, dtype=np.int32)
+    deq = {}
+    for name, mode in (("row", 0), ("col", 1), ("sq", 2)):
+        full = oracle.dequantize(ref[name][0], ref[name][1], mode, cu).reshape(T, H, D)
+        deq[name] = full if rows is None else full[rows]
+    return ref, deq
+
+
+def test_fused_chain_small(mx):
+    # two 256-token sequences, H2: every element of O, lse, dQ, dK, dV
+    B, S, H = 2, 256, 2
+    T, C = B * S, H * D
+    x = inputs.normal_bf16((T, C), 41)
+    g = np.random.default_rng(42).uniform(0.5, 1.5, C).astype(np.float32)
+    dob = inputs.normal_bf16((B, S, H, D), 43)
+    res, o, lse, grads = _fused_chain(mx, x, g, dob, B, S, H)
+    ref, deq = _oracle_operands(x, g, S, H)
+    for name in ("row", "col", "sq"):
+        np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
+    cu = np.arange(0, T + S, S, dtype=np.int32)
+    oo, lo = oracle.attn_fwd(deq["row"], deq["row"], deq["col"], cu, cu, SCALE, True, True, 128,
+                             THR, True)
+    o_gpu = host(o.float()).astype(np.float64)
+    lse_gpu = host(lse).reshape(B, H, S).transpose(1, 0, 2).reshape(H, T)
+    fwd_check(o_gpu, lse_gpu, oo, lo)
+    o_bf = f64(inputs.f32_to_bf16_bits(oo.astype(np.float32)))
+    dof = f64(dob).reshape(T, H, D)
+    ref_g = oracle.attn_bwd(deq["sq"], deq["sq"], deq["row"], oracle.qdq(dof, 2, cu), o_bf, dof, lo,
+                            cu, cu, SCALE, True, True, True, True)
+    grad_check([host(t.float()).astype(np.float64) for t in grads], ref_g, "fused chain")
+
+
+def test_fused_config_sampled_head(mx):
+    # the fused producer workload (X [32768, 2048] -> B4 S8192 H16, causal);
+    # the oracle recomputes one (batch, head) pair from its own RMSNorm+Quantize
+    B, S, H = 4, 8192, 16
+    x, g, dob = inputs.fused_inputs()
+    res, o, lse, grads = _fused_chain(mx, x, g, dob, B, S, H)
+    b, h = 2, 9
+    rows = slice(b * S, (b + 1) * S)
+    ref, deq = _oracle_operands(x, g, S, H, rows)
+    for name in ("row", "col", "sq"):
+        np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
+    hs = slice(h, h + 1)
+    q, vc, qs = deq["row"][:, hs], deq["col"][:, hs], deq["sq"][:, hs]
+    oo, lo = oracle.attn_fwd(q, q, vc, None, None, SCALE, True, True, 128, THR, True)
+    o_gpu = host(o.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs]
+    fwd_check(o_gpu, host(lse).reshape(B, H, S)[b, hs], oo, lo)
+    o_bf = f64(inputs.f32_to_bf16_bits(oo.astype(np.float32)))
+    dof = f64(dob[b, :, hs, :])
+    ref_g = oracle.attn_bwd(qs, qs, q, oracle.qdq(dof, 2), o_bf, dof, lo, None, None, SCALE, True,
+                            True, True, True)
+    got = [host(t.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs] for t in grads]
+    grad_check(got, ref_g, "fused config")

@@ -284,11 +284,13 @@ def _f32_with_product(target):
 
 def test_fp32_mode_backward_exponent_rounded_once():
     # One query, one key, D = 1: S = 4097, fl(scale * log2 e) = 1 + 2^-20 and
-    # fl(lse * log2 e) = 4097 + 2^-8.  The exact argument S * c - l is 2^-20;
-    # rounding S * c to fp32 first (ulp 2^-11 there) would give 0.  With
-    # dO = 1 and no quantization, dV = P = fl32(2^(2^-20)) for one rounding.
+    # fl(lse * log2 e) = 4097 + 2^-8 + 2^-11.  The exact argument S * c - l is
+    # 2^-20 - 2^-11 = -511 * 2^-20 (an fp32 number); rounding S * c to fp32
+    # first (ulp 2^-11 there, S * c -> 4097 + 2^-8) would give -2^-11.  With
+    # dO = 1 and no quantization, dV = P = fl32(2^(-511 * 2^-20)) for one
+    # rounding.
     scale = _f32_with_product(1 + 2.0 ** -20)
-    lse = _f32_with_product(4097 + 2.0 ** -8)
+    lse = _f32_with_product(4097 + 2.0 ** -8 + 2.0 ** -11)
     q = np.full((1, 1, 1), 4097.0)
     k = np.ones((1, 1, 1))
     v = np.zeros((1, 1, 1))
@@ -296,5 +298,25 @@ def test_fp32_mode_backward_exponent_rounded_once():
     o = np.zeros((1, 1, 1))
     lse_a = np.full((1, 1), lse)
     dq, dk, dv = oracle.attn_bwd(q, k, v, do, o, do, lse_a, None, None, scale, False, False, False, True)
-    assert dv[0, 0, 0] == float(np.float32(2.0 ** (2.0 ** -20)))
-    assert dv[0, 0, 0] != 1.0
+    assert dv[0, 0, 0] == float(np.float32(2.0 ** (-511 * 2.0 ** -20)))
+    assert dv[0, 0, 0] != float(np.float32(2.0 ** (-(2.0 ** -11))))
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_backward_p_clamped_at_one(fp32):
+    # One query, three keys, D = 1, scale 1: S = (2, 0.5, -1) with lse = 1
+    # given (smaller than the first score, as a recompute from other operands
+    # can make it).  Exact attention never has P > 1, so the first key takes
+    # P = 1 (not e), the others exp(S - lse).  With dO = 1, O = 0 and no
+    # quantization, dV_j = P_j.
+    q = np.ones((1, 1, 1))
+    k = np.array([2.0, 0.5, -1.0]).reshape(3, 1, 1)
+    v = np.zeros((3, 1, 1))
+    do = np.ones((1, 1, 1))
+    o = np.zeros((1, 1, 1))
+    lse = np.ones((1, 1))
+    _, _, dv = oracle.attn_bwd(q, k, v, do, o, do, lse, None, None, 1.0, False, False, False, fp32)
+    assert dv[0, 0, 0] == 1.0
+    tol = 1e-6 if fp32 else 1e-15
+    assert abs(dv[1, 0, 0] - math.exp(-0.5)) <= tol
+    assert abs(dv[2, 0, 0] - math.exp(-2.0)) <= tol
