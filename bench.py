@@ -12,7 +12,9 @@ reduction.  value = algorithmic PFLOP/s of the step (forward 4*D and backward
   python bench.py --profile-op fwd|bwd|rmsnorm|quant_row|quant_col|quant_sq [--profile-seq S]
                    [--profile-batch B] [--steps K] [--warmup W]
 
-One JSON line on rank 0.  --profile-op runs W + K launches of one operation
+One JSON line on rank 0; at N=1 it also carries "accuracy": the SQNR of the
+step's O, dQ, dK, dV against fp64 attention without quantization on one
+(batch, head) of the workload.  --profile-op runs W + K launches of one operation
 on a causal case (B=--profile-batch, H=16, S=--profile-seq; for rmsnorm the
 fused producer's X[32768, 2048] with row and column outputs; for quant_* one
 quantization of the benchmark's Q tensor into packed scales) for kernel
@@ -65,6 +67,7 @@ def parse():
     p.add_argument("--impl", default="mxfa", choices=["mxfa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-components", action="store_true")
+    p.add_argument("--no-accuracy", action="store_true")
     p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm", "quant_row", "quant_col",
                                             "quant_sq"], default=None)
     p.add_argument("--profile-seq", type=int, default=4096)
@@ -189,12 +192,52 @@ class GpuStep:
         self.quant(self.v, "vR")
         self.bwd()
 
-    def step_e2e(self):
-        for dst, src in zip((self.q, self.k, self.v, self.do), self.host_in):
-            dst.copy_(src, non_blocking=True)
-        self.step()
-        for dst, src in zip(self.host_out, (self.o, self.dq, self.dk, self.dv)):
-            dst.copy_(src, non_blocking=True)
+    def e2e(self, steps):
+        """`steps` steps from pinned host inputs to pinned host outputs, every
+        step copying its Q, K, V, dO in and its O, dQ, dK, dV out.  Device
+        inputs and outputs are double-buffered: the copy-in of step i+1 and
+        the copy-out of step i-1 run on their own streams while step i
+        computes.  Returns the milliseconds per step, first copy-in to last
+        copy-out."""
+        torch = self.torch
+        names_in, names_out = ("q", "k", "v", "do"), ("o", "lse", "dq", "dk", "dv")
+        if not hasattr(self, "_bufs"):
+            own = {n: getattr(self, n) for n in names_in + names_out}
+            self._bufs = [own, {n: torch.empty_like(t) for n, t in own.items()}]
+        s_cmp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        in_done, cmp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_cmp)
+        s_in.wait_event(t0)
+        for i in range(steps):
+            b, buf = i % 2, self._bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(cmp_done[b])  # step i-2 no longer reads these inputs
+                for n, src in zip(names_in, self.host_in):
+                    buf[n].copy_(src, non_blocking=True)
+                in_done[b].record(s_in)
+            s_cmp.wait_event(in_done[b])
+            if i >= 2:
+                s_cmp.wait_event(out_done[b])  # step i-2's outputs have left the device
+            for n in names_in + names_out:
+                setattr(self, n, buf[n])
+            self.step()
+            cmp_done[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(cmp_done[b])
+                for dst, n in zip(self.host_out, ("o", "dq", "dk", "dv")):
+                    dst.copy_(buf[n], non_blocking=True)
+                out_done[b].record(s_out)
+        s_cmp.wait_event(out_done[(steps - 1) % 2])
+        t1.record(s_cmp)
+        torch.cuda.synchronize()
+        for n in names_in + names_out:
+            setattr(self, n, self._bufs[0][n])
+        return t0.elapsed_time(t1) / steps
 
 
 def time_loop(torch, fn, iters, warmup, flush=None):
@@ -326,6 +369,25 @@ def cpu_baseline(qb, kb, vb, dob, s_len=4096):
             "sample": f"fwd+bwd (quantize, forward, backward) of the causal {s_len}-token prefix of "
                       f"{n} (batch, head) pairs of the workload, heads in parallel, {dt:.1f} s",
             "seconds": dt}
+
+
+def accuracy(torch, st, qb, kb, vb, dob, b=1, h=5):
+    """Error of the GPU step's outputs against fp64 attention without any
+    quantization (the oracle with quantization off), on one (batch, head) of
+    the workload: SQNR in dB of O, dQ, dK and dV."""
+    import oracle
+    from mxfp8_block_scaled_fa_gb300 import inputs
+    take = lambda x: inputs.bf16_bits_to_f32(x[b, :, h:h + 1, :]).astype(np.float64)
+    q, k, v, do = take(qb), take(kb), take(vb), take(dob)
+    scale = 1.0 / math.sqrt(D)
+    o_x, lse_x = oracle.method_fwd(q, k, v, None, None, scale, CAUSAL, False)
+    g_x = oracle.method_bwd(q, k, v, do, o_x, lse_x, None, None, scale, CAUSAL, False)
+    pick = lambda t: t.view(B, S, H, D)[b, :, h:h + 1, :].float().cpu().numpy().astype(np.float64)
+    got = [pick(t) for t in (st.o, st.dq, st.dk, st.dv)]
+    sqnr = lambda g, r: float(10 * np.log10(np.sum(r * r) / max(np.sum((g - r) ** 2), 1e-300)))
+    return {"sample": f"(batch {b}, head {h}) of the workload, outputs of the last timed step",
+            "reference": "fp64 attention without quantization (oracle, quantization off)",
+            "sqnr_db": {n: sqnr(g, r) for n, g, r in zip(("O", "dQ", "dK", "dV"), got, (o_x,) + tuple(g_x))}}
 
 
 def reference_arm(args):
@@ -480,21 +542,19 @@ def main():
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     # end to end through the same C-ABI calls, host buffers in and out
-    for _ in range(2):
-        st.step_e2e()
+    st.e2e(2)
     barrier()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record()
-    for _ in range(args.steps):
-        st.step_e2e()
-    a1.record()
+    ms_e2e = st.e2e(args.steps)
     barrier()
-    ms_e2e = a0.elapsed_time(a1) / args.steps
     if world > 1:
         t = torch.tensor([ms, ms_e2e], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, ms_e2e = float(t[0]), float(t[1])
     assert mxfa.device_status() == 0, "device status after timing"
+    acc = None
+    if rank == 0 and world == 1 and not args.no_accuracy:
+        torch.cuda.synchronize()
+        acc = accuracy(torch, st, qb, kb, vb, dob)
     comp = None
     if not args.no_components:
         comp = components(torch, mxfa, st, args.steps, args.warmup, bf16_peak, hbm_peak)
@@ -517,6 +577,8 @@ def main():
             "frac_of_nominal_4.5": value / world * 1e3 / NOMINAL_FP8_TFLOPS,
             "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e15, "unit": "PFLOP/s",
                     "ms_per_step": ms_e2e, "h2d_bytes_per_step": bytes_io,
+                    "overlap": "copy-in of step i+1 and copy-out of step i-1 on their own "
+                               "streams during step i (double-buffered device tensors)",
                     "d2h_bytes_per_step": bytes_io},
             "gpu_launches": st.launches_per_step * args.steps,
             "clocks": clk}
@@ -537,6 +599,8 @@ def main():
         line["components"] = comp
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if acc is not None:
+        line["accuracy"] = acc
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -250,3 +250,35 @@ def test_fused_config_sampled_head(mx):
                             True, True, True)
     got = [host(t.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs] for t in grads]
     grad_check(got, ref_g, "fused config")
+
+
+def test_tiny_error_vs_unquantized_attention(mx):
+    # the tiny workload (B1 H2 S256, non-causal) through the GPU forward and
+    # backward, against fp64 attention without any quantization: the method
+    # itself keeps 23-25 dB here (the oracle's figure on the same inputs),
+    # and the GPU path must stay within 2 dB of the oracle's SQNR
+    import torch
+    from tests.helpers import sqnr_db
+    B, H, S = 1, 2, 256
+    qb, kb, vb, dob = inputs.dense_attn(B, H, S, D, seed=0)
+    seqs = mx.Seqs.dense(B, S)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o, lse = mx.attention_fwd(q, k, v, seqs, seqs, SCALE, causal=False)
+    do_t = to_dev(dob)
+    grads = mx.attention_bwd(mx.quantize(to_dev(qb), mx.SQ, seqs), mx.quantize(to_dev(kb), mx.SQ, seqs),
+                             mx.quantize(to_dev(vb), mx.ROW, seqs), mx.quantize(do_t, mx.SQ, seqs), o,
+                             do_t.reshape(B * S, H, D), lse, seqs, seqs, SCALE, causal=False)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    f = lambda b: f64(b).reshape(B * S, H, D)
+    o_x, lse_x = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, SCALE, False, False)
+    g_x = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_x, lse_x, None, None, SCALE, False, False)
+    oo, lo, _, o_bf = oracle_fwd_full(f(qb), f(kb), f(vb), None, None, False)
+    g_m = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lo, None, None, SCALE, False, True, True)
+    got = [host(t.float()).astype(np.float64) for t in (o,) + tuple(grads)]
+    for name, g, m, x in zip(("O", "dQ", "dK", "dV"), got, (oo,) + tuple(g_m), (o_x,) + tuple(g_x)):
+        s_gpu, s_method = sqnr_db(g, x), sqnr_db(m, x)
+        assert s_method > 20.0, (name, s_method)
+        assert s_gpu >= s_method - 2.0, (name, s_gpu, s_method)
