@@ -277,6 +277,26 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     t_fwd = time_loop(torch, st.fwd, iters, warmup)
     t_bwd = time_loop(torch, st.bwd, iters, warmup)
     t_bwd16 = time_loop(torch, lambda: st.bwd(1, 1.0), iters, warmup)
+    # forward that also writes O as MXFP8 (payload + compact and packed ROW scales)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    omx = [torch.empty((B * S, H, D), **u8), torch.empty((B * S, H * D // 32), **u8),
+           torch.empty(st.seqs.ptiles * H * 512, **u8)]
+    omx_s = mx.MxOut(*(t.data_ptr() for t in omx))
+    m = st.mx_out
+    fwd_mxo = lambda: mx.mxfa_fwd_mxo(m["qR"].mx_in(), m["kR"].mx_in(), m["vC"].mx_in(), B, S, H,
+                                      D, st.scale, CAUSAL, st.o, st.lse, omx_s)
+    t_fwd_mxo = time_loop(torch, fwd_mxo, iters, warmup)
+    del omx
+    # backward that also writes dQ, dK, dV as MXFP8 (payload + compact and packed ROW scales)
+    gmx = [[torch.empty((B * S, H, D), **u8), torch.empty((B * S, H * D // 32), **u8),
+            torch.empty(st.seqs.ptiles * H * 512, **u8)] for _ in range(3)]
+    gs = [mx.MxOut(*(t.data_ptr() for t in g)) for g in gmx]
+    bwd_mxg = lambda: mx.mxfa_bwd_mxg(m["qS"].mx_in(), m["kS"].mx_in(), m["vR"].mx_in(),
+                                      m["doS"].mx_in(), st.o, st.do, st.lse, B, S, H, D, st.scale,
+                                      CAUSAL, 0, 1.0, st.dq, st.dk, st.dv, st.ws, st.ws.numel(),
+                                      *gs)
+    t_bwd_mxg = time_loop(torch, bwd_mxg, iters, warmup)
+    del gmx
     st.bwd()
     t_q = time_loop(torch, lambda: st.quant(st.q, "qR"), iters, warmup, flush)
     t_qs = time_loop(torch, lambda: st.quant(st.q, "qS"), iters, warmup, flush)
@@ -284,6 +304,10 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     n = B * S * H * D
     res["fwd"] = {"ms": t_fwd, "pflops": FWD_FLOPS / t_fwd / 1e12,
                   "frac_of_4.5": FWD_FLOPS / t_fwd / 1e9 / NOMINAL_FP8_TFLOPS}
+    res["fwd_mxfp8_o"] = {"ms": t_fwd_mxo, "pflops": FWD_FLOPS / t_fwd_mxo / 1e12,
+                          "note": "forward with O also written as MXFP8 (ROW)"}
+    res["bwd_mxfp8_grads"] = {"ms": t_bwd_mxg, "pflops": BWD_FLOPS / t_bwd_mxg / 1e12,
+                              "note": "fp32-dQ backward with dQ, dK, dV also written as MXFP8 (ROW)"}
     res["bwd_fp32_dq"] = {"ms": t_bwd, "pflops": BWD_FLOPS / t_bwd / 1e12,
                           "frac_of_4.5": BWD_FLOPS / t_bwd / 1e9 / NOMINAL_FP8_TFLOPS}
     res["bwd_fp16_dq"] = {"ms": t_bwd16, "pflops": BWD_FLOPS / t_bwd16 / 1e12,

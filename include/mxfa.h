@@ -155,6 +155,27 @@ mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
                             int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
                             int causal, void* o, float* lse, mxfa_stream_t stream);
 
+/* mxfa_fwd_mxo, mxfa_varlen_fwd_mxo -- the forward passes above that also
+ * emit O as MXFP8 for the output projection ([KDIM] paragraph 4: fused
+ * producer and output epilogues).  The bf16 O they write is quantized in
+ * 1x32 blocks along D, byte for byte as mxfa_quantize(MXFA_BLK_ROW)
+ * quantizes that bf16 O:
+ *  o_mx->data        E4M3 [tokens][H][128] (required, 16-byte aligned)
+ *  o_mx->sf_compact  E8M0 [tokens][H * 4] (nullable, 4-byte aligned)
+ *  o_mx->sf_packed   packed ROW atoms, ptiles_q * H * 512 bytes, rows past
+ *                    a sequence's end 0x7F (nullable, 16-byte aligned)
+ * Other arguments and errors as mxfa_fwd / mxfa_varlen_fwd; o_mx NULL is
+ * MXFA_ERR_INVALID_ARG. */
+mxfa_status mxfa_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H,
+                         int D, float softmax_scale, int causal, void* o, float* lse,
+                         const mxfa_mx_out* o_mx, mxfa_stream_t stream);
+mxfa_status mxfa_varlen_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                                int max_seqlen_q, int max_seqlen_k, int64_t total_q,
+                                int64_t total_k, int64_t ptiles_q, int64_t ptiles_k, int H, int D,
+                                float softmax_scale, int causal, void* o, float* lse,
+                                const mxfa_mx_out* o_mx, mxfa_stream_t stream);
+
 /* Workspace of the backward pass for total_q query tokens in nseq sequences:
  * one 2560-byte record per (64-query tile, head) -- the tile's scale atoms,
  * lse * log2(e) and Delta = rowsum(dO * O) -- for at most
@@ -188,6 +209,37 @@ mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
                             int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
                             int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
                             void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
+
+/* mxfa_bwd_mxg, mxfa_varlen_bwd_mxg -- the backward passes above that also
+ * emit the gradients as MXFP8 ([TMEM] page, section "What the Benchmarks
+ * Show About Low-Precision Training": quantized gradients instead of bf16).
+ * Each bf16 gradient they write is quantized in 1x32 blocks along D, byte
+ * for byte as mxfa_quantize(MXFA_BLK_ROW) quantizes it.  dq_mx, dk_mx, dv_mx
+ * are each nullable; for each given one:
+ *  data        E4M3 [tokens][H][128] (required, 16-byte aligned)
+ *  sf_compact  E8M0 [tokens][H * 4] (nullable, 4-byte aligned; required for
+ *              dq_mx when its sf_packed is given)
+ *  sf_packed   packed ROW atoms, ptiles * H * 512 bytes, rows past a
+ *              sequence's end 0x7F (nullable, 16-byte aligned)
+ * dK and dV are quantized in the kernel's epilogue, dQ in its final pass
+ * (plus one scale-packing pass when dq_mx->sf_packed is given).  Other
+ * arguments and errors as mxfa_bwd / mxfa_varlen_bwd. */
+mxfa_status mxfa_bwd_mxg(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                         const mxfa_mx* dout_mx, const void* o, const void* dout, const float* lse,
+                         int B, int S, int H, int D, float softmax_scale, int causal, int dq_mode,
+                         float dq_static_scale, void* dq, void* dk, void* dv, void* ws,
+                         size_t ws_bytes, const mxfa_mx_out* dq_mx, const mxfa_mx_out* dk_mx,
+                         const mxfa_mx_out* dv_mx, mxfa_stream_t stream);
+mxfa_status mxfa_varlen_bwd_mxg(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                const mxfa_mx* dout_mx, const void* o, const void* dout,
+                                const float* lse, const int32_t* cu_seqlens_q,
+                                const int32_t* cu_seqlens_k, int nseq, int max_seqlen_q,
+                                int max_seqlen_k, int64_t total_q, int64_t total_k,
+                                int64_t ptiles_q, int64_t ptiles_k, int H, int D,
+                                float softmax_scale, int causal, int dq_mode, float dq_static_scale,
+                                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                const mxfa_mx_out* dq_mx, const mxfa_mx_out* dk_mx,
+                                const mxfa_mx_out* dv_mx, mxfa_stream_t stream);
 
 /* mxfa_rmsnorm_quant -- fused RMSNorm + MX quantization in one pass
  * ([TMEM] "fused producers", [ITEMS] item 7: FP8 out with dual scale layouts).

@@ -65,6 +65,7 @@ bool make_map_acc(CUtensorMap* m, const void* ptr, int64_t tokens, int H, bool h
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 mxfa_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return MXFA_OK;
@@ -97,10 +98,14 @@ mxfa_status check_mx(const mxfa_mx* x) {
 
 mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seqs sq, Seqs sk,
                        int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
-                       float scale, int causal, void* o, float* lse, bool dense, mxfa_stream_t stream) {
+                       float scale, int causal, void* o, float* lse, const mxfa_mx_out* omx, bool dense,
+                       mxfa_stream_t stream) {
   mxfa_status s;
   if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v))) return s;
   if (!o || !lse || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (omx && (!omx->data || !aligned16(omx->data) || (omx->sf_compact && !aligned4(omx->sf_compact)) ||
+              (omx->sf_packed && !aligned16(omx->sf_packed))))
+    return omx->data ? MXFA_ERR_MISALIGNED : MXFA_ERR_INVALID_ARG;
   if (D != 128) return MXFA_ERR_UNSUPPORTED;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return MXFA_ERR_INVALID_ARG;
   if (!aligned16(o)) return MXFA_ERR_MISALIGNED;
@@ -123,6 +128,11 @@ mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seq
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal ? 1 : 0;
   a.o = static_cast<uint16_t*>(o);
+  if (omx) {
+    a.omx = omx->data;
+    a.omx_sfc = omx->sf_compact;
+    a.omx_sfp = omx->sf_packed;
+  }
   a.lse = lse;
   a.dense_lse = dense ? 1 : 0;
   a.lse_hstride = dense ? sq.seqlen : total_q;
@@ -133,9 +143,19 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
                        const void* o, const void* dout, const float* lse, Seqs sq, Seqs sk,
                        int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
                        float scale, int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
-                       void* dv, void* ws, size_t ws_bytes, bool dense, mxfa_stream_t stream) {
+                       void* dv, void* ws, size_t ws_bytes, const mxfa_mx_out* gmx[3], bool dense,
+                       mxfa_stream_t stream) {
   mxfa_status s;
   if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v)) || (s = check_mx(dmx))) return s;
+  for (int i = 0; i < 3 && gmx; i++) {
+    const mxfa_mx_out* m = gmx[i];
+    if (!m) continue;
+    if (!m->data) return MXFA_ERR_INVALID_ARG;
+    if (i == 0 && m->sf_packed && !m->sf_compact) return MXFA_ERR_INVALID_ARG;
+    if (!aligned16(m->data) || (m->sf_compact && !aligned4(m->sf_compact)) ||
+        (m->sf_packed && !aligned16(m->sf_packed)))
+      return MXFA_ERR_MISALIGNED;
+  }
   if (!o || !dout || !lse || !dq || !dk || !dv || H <= 0) return MXFA_ERR_INVALID_ARG;
   if (D != 128) return MXFA_ERR_UNSUPPORTED;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return MXFA_ERR_INVALID_ARG;
@@ -180,6 +200,21 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   a.dq = static_cast<uint16_t*>(dq);
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
+  if (gmx && gmx[0]) {
+    a.dqmx = gmx[0]->data;
+    a.dqmx_sfc = gmx[0]->sf_compact;
+    a.dqmx_sfp = gmx[0]->sf_packed;
+  }
+  if (gmx && gmx[1]) {
+    a.dkmx = gmx[1]->data;
+    a.dkmx_sfc = gmx[1]->sf_compact;
+    a.dkmx_sfp = gmx[1]->sf_packed;
+  }
+  if (gmx && gmx[2]) {
+    a.dvmx = gmx[2]->data;
+    a.dvmx_sfc = gmx[2]->sf_compact;
+    a.dvmx_sfp = gmx[2]->sf_packed;
+  }
   a.rec = static_cast<uint8_t*>(ws);
   a.dq_acc = static_cast<uint8_t*>(ws) + bwd_records_bytes(total_q, sq.nseq, H);
   if (!make_map_acc(&a.tm_dqacc, a.dq_acc, total_q, H, dq_mode == 1)) return MXFA_ERR_CUDA;
@@ -279,7 +314,19 @@ mxfa_status mxfa_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B
   if (s) return s;
   const int64_t pt = int64_t(B) * ceil_div(S, 128);
   return fwd_common(q, k, v, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total, pt, pt, H, D,
-                    softmax_scale, causal, o, lse, true, stream);
+                    softmax_scale, causal, o, lse, nullptr, true, stream);
+}
+
+mxfa_status mxfa_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H,
+                         int D, float softmax_scale, int causal, void* o, float* lse,
+                         const mxfa_mx_out* o_mx, mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0 || !o_mx) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  return fwd_common(q, k, v, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total, pt, pt, H, D,
+                    softmax_scale, causal, o, lse, o_mx, true, stream);
 }
 
 mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const int32_t* cu_q,
@@ -292,7 +339,21 @@ mxfa_status mxfa_varlen_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
     return s;
   if (max_sk <= 0) return MXFA_ERR_INVALID_ARG;
   return fwd_common(q, k, v, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk}, total_q, total_k, ptq,
-                    ptk, H, D, softmax_scale, causal, o, lse, false, stream);
+                    ptk, H, D, softmax_scale, causal, o, lse, nullptr, false, stream);
+}
+
+mxfa_status mxfa_varlen_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                const int32_t* cu_q, const int32_t* cu_k, int nseq, int max_sq,
+                                int max_sk, int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk,
+                                int H, int D, float softmax_scale, int causal, void* o, float* lse,
+                                const mxfa_mx_out* o_mx, mxfa_stream_t stream) {
+  if (!cu_q || !cu_k || !o_mx) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  if (max_sk <= 0) return MXFA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk}, total_q, total_k, ptq,
+                    ptk, H, D, softmax_scale, causal, o, lse, o_mx, false, stream);
 }
 
 size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_mode) {
@@ -311,7 +372,23 @@ mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const
   const int64_t pt = int64_t(B) * ceil_div(S, 128);
   return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total,
                     pt, pt, H, D, softmax_scale, causal, dq_mode, dq_static_scale, dq, dk, dv, ws,
-                    ws_bytes, true, stream);
+                    ws_bytes, nullptr, true, stream);
+}
+
+mxfa_status mxfa_bwd_mxg(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                         const void* o, const void* dout, const float* lse, int B, int S, int H, int D,
+                         float softmax_scale, int causal, int dq_mode, float dq_static_scale, void* dq,
+                         void* dk, void* dv, void* ws, size_t ws_bytes, const mxfa_mx_out* dq_mx,
+                         const mxfa_mx_out* dk_mx, const mxfa_mx_out* dv_mx, mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  const mxfa_mx_out* gmx[3] = {dq_mx, dk_mx, dv_mx};
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total,
+                    pt, pt, H, D, softmax_scale, causal, dq_mode, dq_static_scale, dq, dk, dv, ws,
+                    ws_bytes, gmx, true, stream);
 }
 
 mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
@@ -326,7 +403,25 @@ mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
     return s;
   return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk},
                     total_q, total_k, ptq, ptk, H, D, softmax_scale, causal, dq_mode, dq_static_scale,
-                    dq, dk, dv, ws, ws_bytes, false, stream);
+                    dq, dk, dv, ws, ws_bytes, nullptr, false, stream);
+}
+
+mxfa_status mxfa_varlen_bwd_mxg(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                                const void* o, const void* dout, const float* lse, const int32_t* cu_q,
+                                const int32_t* cu_k, int nseq, int max_sq, int max_sk, int64_t total_q,
+                                int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
+                                float softmax_scale, int causal, int dq_mode, float dq_static_scale,
+                                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                const mxfa_mx_out* dq_mx, const mxfa_mx_out* dk_mx,
+                                const mxfa_mx_out* dv_mx, mxfa_stream_t stream) {
+  if (!cu_q || !cu_k) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  const mxfa_mx_out* gmx[3] = {dq_mx, dk_mx, dv_mx};
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk},
+                    total_q, total_k, ptq, ptk, H, D, softmax_scale, causal, dq_mode, dq_static_scale,
+                    dq, dk, dv, ws, ws_bytes, gmx, false, stream);
 }
 
 mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int64_t C, float eps,

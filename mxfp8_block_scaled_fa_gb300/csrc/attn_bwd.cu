@@ -150,6 +150,47 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   }
 }
 
+// dQ = bf16(acc * mult) as below, and the same bf16 dQ as MXFP8: one thread
+// per 1x32 block along D (the flat element index / 32 is the block's index
+// in the compact [tokens][H * 4] scale layout).
+__global__ void __launch_bounds__(256) bwd_post_mx_kernel(const void* __restrict__ acc,
+                                                          uint16_t* __restrict__ dq, int64_t n, int mode,
+                                                          float mult, uint8_t* __restrict__ dqmx,
+                                                          uint8_t* __restrict__ dqmx_sfc) {
+  const int64_t blk = int64_t(blockIdx.x) * 256 + threadIdx.x;
+  const int64_t i = blk * 32;
+  if (i >= n) return;
+  uint32_t w[16];
+#pragma unroll
+  for (int q8 = 0; q8 < 4; q8++) {
+    float v[8];
+    if (mode == 0) {
+      const float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i + 8 * q8);
+      const float4 y = *reinterpret_cast<const float4*>(static_cast<const float*>(acc) + i + 8 * q8 + 4);
+      v[0] = x.x * mult; v[1] = x.y * mult; v[2] = x.z * mult; v[3] = x.w * mult;
+      v[4] = y.x * mult; v[5] = y.y * mult; v[6] = y.z * mult; v[7] = y.w * mult;
+    } else {
+      const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __half*>(acc) + i + 8 * q8);
+      const uint32_t hw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+        v[2 * j] = f.x * mult;
+        v[2 * j + 1] = f.y * mult;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      w[4 * q8 + j] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    *reinterpret_cast<uint4*>(dq + i + 8 * q8) = make_uint4(w[4 * q8], w[4 * q8 + 1], w[4 * q8 + 2], w[4 * q8 + 3]);
+  }
+  const uint32_t sc = mx_block_e8m0(w);
+  mx_block_store(dqmx + i, w, sc);
+  if (dqmx_sfc != nullptr) dqmx_sfc[blk] = uint8_t(sc);
+}
+
 // dQ = bf16(acc * mult): acc is fp32 holding unscaled sums (mode 0, mult =
 // softmax scale) or fp16 holding scale * static_scale times them (mode 1,
 // mult = 1 / static_scale).
@@ -587,25 +628,46 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       tc_fence_after();
       const uint32_t col = hq == 0 ? COL_DV : COL_DK;
       const float mult = hq == 0 ? 1.0f : a.scale;
-      uint16_t* dst = (hq == 0 ? a.dv : a.dk) + ((sk0 + kpos) * a.H + h) * 128;
+      const int64_t tok = sk0 + kpos;
+      uint16_t* dst = (hq == 0 ? a.dv : a.dk) + (tok * a.H + h) * 128;
+      uint8_t* mxd = hq == 0 ? a.dvmx : a.dkmx;
+      uint32_t sfw = 0;  // E8M0 scales of the MXFP8 gradient row, one byte per 32 columns
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + col + 32 * c, v);
         tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+          const float x0 = ntile > 0 ? __uint_as_float(v[2 * e]) * mult : 0.0f;
+          const float x1 = ntile > 0 ? __uint_as_float(v[2 * e + 1]) * mult : 0.0f;
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(x0, x1);
+          w[e] = *reinterpret_cast<uint32_t*>(&p2);
+        }
         if (kvalid) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; v4++) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-              const float x0 = ntile > 0 ? __uint_as_float(v[8 * v4 + 2 * e]) * mult : 0.0f;
-              const float x1 = ntile > 0 ? __uint_as_float(v[8 * v4 + 2 * e + 1]) * mult : 0.0f;
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(x0, x1);
-              w[e] = *reinterpret_cast<uint32_t*>(&p2);
-            }
-            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v4) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int v4 = 0; v4 < 4; v4++)
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * v4) =
+                make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+        if (mxd != nullptr) {
+          // the 32 bf16 values of this chunk are one 1x32 block along D,
+          // quantized exactly as the ROW quantizer treats a bf16 tensor
+          const uint32_t sc = mx_block_e8m0(w);
+          sfw |= sc << (8 * c);
+          if (kvalid) mx_block_store(mxd + (tok * a.H + h) * 128 + 32 * c, w, sc);
+        }
+      }
+      if (mxd != nullptr) {
+        uint8_t* sfc = hq == 0 ? a.dvmx_sfc : a.dkmx_sfc;
+        uint8_t* sfp = hq == 0 ? a.dvmx_sfp : a.dkmx_sfp;
+        if (kvalid && sfc != nullptr) *reinterpret_cast<uint32_t*>(sfc + (tok * a.H + h) * 4) = sfw;
+        // packed ROW atom of this key tile; rows past the sequence hold 0x7F
+        if (sfp != nullptr) {
+          const int64_t tile = seq_units_before(a.sk, g, 128) + kt;
+          *reinterpret_cast<uint32_t*>(sfp + (tile * a.H + h) * 512 + (r & 31) * 16 + (r >> 5) * 4) =
+              kvalid ? sfw : 0x7F7F7F7Fu;
         }
       }
     }
@@ -696,8 +758,27 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
   if (grid.x > 0 && grid.y > 0 && grid.z > 0)
     attn_bwd_kernel<<<grid, bwd::NTHREADS, bwd::SMEM_BYTES, st>>>(a);
   const int64_t n = rows * 128;
-  bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(
-      a.dq_acc, a.dq, n, a.dq_mode, a.dq_mode == 1 ? 1.0f / a.dq_static_scale : a.scale);
+  const float mult = a.dq_mode == 1 ? 1.0f / a.dq_static_scale : a.scale;
+  if (a.dqmx == nullptr) {
+    bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode, mult);
+  } else {
+    bwd_post_mx_kernel<<<unsigned((n / 32 + 255) / 256), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode, mult,
+                                                                       a.dqmx, a.dqmx_sfc);
+    if (a.dqmx_sfp != nullptr) {
+      cudaError_t e = cudaPeekAtLastError();
+      if (e != cudaSuccess) return e;
+      PackArgs p;
+      p.sf_compact = a.dqmx_sfc;
+      p.tokens = rows / a.H;
+      p.H = a.H;
+      p.D = 128;
+      p.mode = 0;
+      p.seq = a.sq;
+      p.packed_tiles = a.ptiles_q;
+      p.sf_packed = a.dqmx_sfp;
+      return launch_sf_pack(p, st);
+    }
+  }
   return cudaPeekAtLastError();
 }
 

@@ -398,24 +398,43 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       tc_fence_after();
       const bool valid = qpos < lq;
       const float rl = 1.0f / l;
-      uint16_t* orow = a.o + ((sq0 + qpos) * a.H + h) * 128;
+      const int64_t tok = sq0 + qpos;
+      uint16_t* orow = a.o + (tok * a.H + h) * 128;
+      uint32_t sfw = 0;  // E8M0 scales of the MXFP8 O row, one byte per 32 columns
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
         tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * rl,
+                                                    __uint_as_float(o[2 * e + 1]) * rl);
+          w[e] = *reinterpret_cast<uint32_t*>(&p2);
+        }
         if (valid) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; v4++) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[8 * v4 + 2 * e]) * rl,
-                                                        __uint_as_float(o[8 * v4 + 2 * e + 1]) * rl);
-              w4[e] = *reinterpret_cast<uint32_t*>(&p2);
-            }
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+          for (int v4 = 0; v4 < 4; v4++)
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) =
+                make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+        if (a.omx != nullptr) {
+          // O as MXFP8: these 32 bf16 values form one 1x32 block along D,
+          // quantized exactly as the ROW quantizer treats a bf16 tensor
+          const uint32_t sc = mx_block_e8m0(w);
+          sfw |= sc << (8 * c);
+          if (valid) mx_block_store(a.omx + (tok * a.H + h) * 128 + 32 * c, w, sc);
+        }
+      }
+      if (a.omx != nullptr) {
+        if (valid && a.omx_sfc != nullptr)
+          *reinterpret_cast<uint32_t*>(a.omx_sfc + (tok * a.H + h) * 4) = sfw;
+        // packed ROW atom of this query tile; rows past the sequence hold 0x7F
+        if (a.omx_sfp != nullptr) {
+          const int64_t tile = seq_units_before(a.sq, g, TILE) + 2 * qp + x;
+          *reinterpret_cast<uint32_t*>(a.omx_sfp + (tile * a.H + h) * 512 + (row & 31) * 16 + (row >> 5) * 4) =
+              valid ? sfw : 0x7F7F7F7Fu;
         }
       }
       if (valid) {

@@ -419,4 +419,54 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
 }
 
+// |bf16| bit patterns of a packed pair, as an unsigned max-able pair.
+__device__ __forceinline__ uint32_t abs2(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t hmax2(uint32_t w) { return max(w & 0xFFFFu, w >> 16); }
+
+// E8M0 from the bit pattern of a bf16 magnitude (the block maximum):
+// exponent field - 8, clamped at 0; Inf or NaN in the block -> 0xFF.
+__device__ __forceinline__ uint32_t e8m0_from_bf16abs(uint32_t a) {
+  if (a >= 0x7F80u) return 0xFFu;
+  uint32_t e = a >> 7;
+  return e > 8u ? e - 8u : 0u;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Eight bf16 (as uint4) times inv[0..7] -> eight E4M3 bytes (uint2).
+__device__ __forceinline__ uint2 cvt8(uint4 v, const float* inv) {
+  uint2 r;
+  r.x = pack4_e4m3(bf_lo(v.x) * inv[0], bf_hi(v.x) * inv[1], bf_lo(v.y) * inv[2], bf_hi(v.y) * inv[3]);
+  r.y = pack4_e4m3(bf_lo(v.z) * inv[4], bf_hi(v.z) * inv[5], bf_lo(v.w) * inv[6], bf_hi(v.w) * inv[7]);
+  return r;
+}
+
+// One 1x32 block of bf16 values held as 16 packed words: its E8M0 scale
+// (from the block's largest magnitude), and its 32 E4M3 bytes stored at dst
+// (16-byte aligned); a block holding Inf or NaN gets scale 0xFF and 0x7F bytes.
+__device__ __forceinline__ uint32_t mx_block_e8m0(const uint32_t* w) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int e = 0; e < 16; e++) mx = max(mx, hmax2(abs2(w[e])));
+  return e8m0_from_bf16abs(mx);
+}
+__device__ __forceinline__ void mx_block_store(uint8_t* dst, const uint32_t* w, uint32_t sc) {
+  uint2 q[4];
+  if (sc == 0xFFu) {
+#pragma unroll
+    for (int v4 = 0; v4 < 4; v4++) q[v4] = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  } else {
+    float inv[8];
+    const float f = e8m0_inv_scale(sc);
+#pragma unroll
+    for (int i = 0; i < 8; i++) inv[i] = f;
+#pragma unroll
+    for (int v4 = 0; v4 < 4; v4++)
+      q[v4] = cvt8(make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]), inv);
+  }
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
+}
+
 }  // namespace mxfa

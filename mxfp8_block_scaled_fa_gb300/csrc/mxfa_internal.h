@@ -65,6 +65,9 @@ struct FwdArgs {
   float scale_log2;  // softmax scale * log2(e)
   int causal;
   uint16_t* o;       // bf16 [tokens][H][128]
+  uint8_t* omx;      // nullable: O quantized (ROW, 1x32 along D) E4M3 [tokens][H][128]
+  uint8_t* omx_sfc;  // nullable: its compact scales [tokens][H * 4]
+  uint8_t* omx_sfp;  // nullable: its packed ROW atoms (ptiles_q * H * 512 bytes)
   float* lse;
   int64_t lse_hstride;  // dense: S, varlen: total_q
   int dense_lse;        // 1: lse[(b*H + h) * S + s]; 0: lse[h * total_q + token]
@@ -90,6 +93,12 @@ struct BwdArgs {
   int dq_mode;        // 0 fp32 accumulation, 1 fp16 with static scale
   float dq_static_scale;
   uint16_t *dq, *dk, *dv;  // bf16 outputs
+  // nullable MXFP8 copies of the gradients (ROW, 1x32 along D): payload,
+  // compact scales [tokens][H * 4], packed ROW atoms (dK, dV only; dQ's are
+  // packed from its compact scales after the post pass)
+  uint8_t *dqmx, *dqmx_sfc, *dqmx_sfp;
+  uint8_t *dkmx, *dkmx_sfc, *dkmx_sfp;
+  uint8_t *dvmx, *dvmx_sfc, *dvmx_sfp;
   uint8_t* rec;            // workspace: one record per (64-query tile, head)
   void* dq_acc;            // workspace [total_q][H][128] fp32 or fp16
   int64_t lse_hstride;

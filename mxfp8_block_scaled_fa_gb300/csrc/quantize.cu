@@ -32,27 +32,6 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
   return v;
 }
 
-// |bf16| bit patterns of a packed pair, as an unsigned max-able pair.
-__device__ __forceinline__ uint32_t abs2(uint32_t w) { return w & 0x7FFF7FFFu; }
-__device__ __forceinline__ uint32_t hmax2(uint32_t w) { return max(w & 0xFFFFu, w >> 16); }
-
-// E8M0 from the bit pattern of a bf16 magnitude.
-__device__ __forceinline__ uint32_t e8m0_from_bf16abs(uint32_t a) {
-  if (a >= 0x7F80u) return 0xFFu;  // Inf or NaN in the block
-  uint32_t e = a >> 7;
-  return e > 8u ? e - 8u : 0u;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Eight bf16 (as uint4) times inv[0..7] -> eight E4M3 bytes (uint2).
-__device__ __forceinline__ uint2 cvt8(uint4 v, const float* inv) {
-  uint2 r;
-  r.x = pack4_e4m3(bf_lo(v.x) * inv[0], bf_hi(v.x) * inv[1], bf_lo(v.y) * inv[2], bf_hi(v.y) * inv[3]);
-  r.y = pack4_e4m3(bf_lo(v.z) * inv[4], bf_hi(v.z) * inv[5], bf_lo(v.w) * inv[6], bf_hi(v.w) * inv[7]);
-  return r;
-}
 
 // ------------------------------------------------------------------ quantize
 // grid (ceil(cols/1024), 4 * ceil(max_len/128), nseq), block 128.

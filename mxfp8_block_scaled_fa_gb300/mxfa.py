@@ -64,10 +64,17 @@ def lib() -> ctypes.CDLL:
             "mxfa_fwd": (I, [P, P, P, I, I, I, I, F, I, P, P, P]),
             "mxfa_varlen_fwd": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P, P,
                                     P]),
+            "mxfa_fwd_mxo": (I, [P, P, P, I, I, I, I, F, I, P, P, P, P]),
+            "mxfa_varlen_fwd_mxo": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P,
+                                        P, P, P]),
             "mxfa_bwd_workspace_size": (S, [I64, I, I, I, I]),
             "mxfa_bwd": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P, S, P]),
             "mxfa_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I,
                                     F, I, I, F, P, P, P, P, S, P]),
+            "mxfa_bwd_mxg": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P, S, P, P,
+                                 P, P]),
+            "mxfa_varlen_bwd_mxg": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I,
+                                        I, F, I, I, F, P, P, P, P, S, P, P, P, P]),
             "mxfa_rmsnorm_quant": (I, [P, P, I64, I64, F, I, I, P, P, P, P]),
             "mxfa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint)]),
             "mxfa_bwd_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P]),
@@ -130,6 +137,21 @@ def mxfa_varlen_fwd(q, k, v, cu_q, cu_k, nseq, max_sq, max_sk, total_q, total_k,
                                  _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H, D,
                                  float(scale), int(causal), _p(o), _p(lse), _stream(stream)),
            "mxfa_varlen_fwd")
+
+
+def mxfa_fwd_mxo(q: MxIn, k: MxIn, v: MxIn, B, S, H, D, scale, causal, o, lse, o_mx: MxOut,
+                 stream=None):
+    _check(lib().mxfa_fwd_mxo(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), B, S, H, D,
+                              float(scale), int(causal), _p(o), _p(lse), ctypes.byref(o_mx),
+                              _stream(stream)), "mxfa_fwd_mxo")
+
+
+def mxfa_varlen_fwd_mxo(q, k, v, cu_q, cu_k, nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H,
+                        D, scale, causal, o, lse, o_mx: MxOut, stream=None):
+    _check(lib().mxfa_varlen_fwd_mxo(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), _p(cu_q),
+                                     _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H,
+                                     D, float(scale), int(causal), _p(o), _p(lse),
+                                     ctypes.byref(o_mx), _stream(stream)), "mxfa_varlen_fwd_mxo")
 
 
 def mxfa_bwd_workspace_size(total_q, nseq, H, D, dq_mode) -> int:
@@ -252,30 +274,69 @@ def sf_pack(sf_compact: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 128
 
 
 def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,
-                  causal: bool = False, stream=None, out=None):
-    """Forward on quantized operands -> (O bf16 [tokens, H, D], lse fp32)."""
+                  causal: bool = False, stream=None, out=None, o_mx: bool = False):
+    """Forward on quantized operands -> (O bf16 [tokens, H, D], lse fp32), and with
+    o_mx=True also O as MXFP8 (Mx with ROW compact and packed scales) as a third item."""
     H, D = q.data.shape[-2], q.data.shape[-1]
     dev = q.data.device
     o = out[0] if out is not None else torch.empty(q.data.shape, dtype=torch.bfloat16, device=dev)
+    omx = omx_s = None
+    if o_mx:
+        u8 = dict(dtype=torch.uint8, device=dev)
+        omx = Mx(torch.empty(q.data.shape, **u8), torch.empty((seqs_q.total, H * D // 32), **u8),
+                 torch.empty(seqs_q.ptiles * H * 512, **u8), ROW)
+        omx_s = MxOut(omx.data.data_ptr(), omx.sf_compact.data_ptr(), omx.sf_packed.data_ptr())
     if seqs_q.cu_host is None and seqs_k.cu_host is None:
         lse = out[1] if out is not None else torch.empty((seqs_q.nseq, H, seqs_q.max_len),
                                                          dtype=torch.float32, device=dev)
-        mxfa_fwd(q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.nseq, seqs_q.max_len, H, D, scale,
-                 causal, o, lse, stream)
+        args = (q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.nseq, seqs_q.max_len, H, D, scale,
+                causal, o, lse)
+        if o_mx:
+            mxfa_fwd_mxo(*args, omx_s, stream)
+        else:
+            mxfa_fwd(*args, stream)
     else:
         lse = out[1] if out is not None else torch.empty((H, seqs_q.total), dtype=torch.float32,
                                                          device=dev)
-        mxfa_varlen_fwd(q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.cu_dev, seqs_k.cu_dev,
-                        seqs_q.nseq, seqs_q.max_len, seqs_k.max_len, seqs_q.total, seqs_k.total,
-                        seqs_q.ptiles, seqs_k.ptiles, H, D, scale, causal, o, lse, stream)
-    return o, lse
+        args = (q.mx_in(), k.mx_in(), v.mx_in(), seqs_q.cu_dev, seqs_k.cu_dev, seqs_q.nseq,
+                seqs_q.max_len, seqs_k.max_len, seqs_q.total, seqs_k.total, seqs_q.ptiles,
+                seqs_k.ptiles, H, D, scale, causal, o, lse)
+        if o_mx:
+            mxfa_varlen_fwd_mxo(*args, omx_s, stream)
+        else:
+            mxfa_varlen_fwd(*args, stream)
+    return (o, lse, omx) if o_mx else (o, lse)
+
+
+def mxfa_bwd_mxg(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, dq_mode, dq_static, dq,
+                 dk, dv, ws, ws_bytes, dq_mx, dk_mx, dv_mx, stream=None):
+    ref = lambda m: ctypes.byref(m) if m is not None else None
+    _check(lib().mxfa_bwd_mxg(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                              ctypes.byref(do_mx), _p(o), _p(do), _p(lse), B, S, H, D,
+                              float(scale), int(causal), dq_mode, float(dq_static), _p(dq), _p(dk),
+                              _p(dv), _p(ws), ws_bytes, ref(dq_mx), ref(dk_mx), ref(dv_mx),
+                              _stream(stream)), "mxfa_bwd_mxg")
+
+
+def mxfa_varlen_bwd_mxg(q, k, v, do_mx, o, do, lse, cu_q, cu_k, nseq, max_sq, max_sk, total_q,
+                        total_k, ptq, ptk, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
+                        ws_bytes, dq_mx, dk_mx, dv_mx, stream=None):
+    ref = lambda m: ctypes.byref(m) if m is not None else None
+    _check(lib().mxfa_varlen_bwd_mxg(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                     ctypes.byref(do_mx), _p(o), _p(do), _p(lse), _p(cu_q),
+                                     _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H,
+                                     D, float(scale), int(causal), dq_mode, float(dq_static),
+                                     _p(dq), _p(dk), _p(dv), _p(ws), ws_bytes, ref(dq_mx),
+                                     ref(dk_mx), ref(dv_mx), _stream(stream)),
+           "mxfa_varlen_bwd_mxg")
 
 
 def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Tensor,
                   lse: torch.Tensor, seqs_q: Seqs, seqs_k: Seqs, scale: float,
                   causal: bool = False, dq_mode: int = 0, dq_static: float = 1.0, stream=None,
-                  ws=None, out=None):
-    """Backward on quantized operands -> (dQ, dK, dV) bf16."""
+                  ws=None, out=None, grads_mx: bool = False):
+    """Backward on quantized operands -> (dQ, dK, dV) bf16; with grads_mx=True also the
+    three gradients as MXFP8 (Mx with ROW compact and packed scales), six items in all."""
     H, D = q.data.shape[-2], q.data.shape[-1]
     dev = q.data.device
     wsb = mxfa_bwd_workspace_size(seqs_q.total, seqs_q.nseq, H, D, dq_mode)
@@ -287,17 +348,32 @@ def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Ten
         dv = torch.empty(v.data.shape, dtype=torch.bfloat16, device=dev)
     else:
         dq, dk, dv = out
+    gmx = gs = None
+    if grads_mx:
+        u8 = dict(dtype=torch.uint8, device=dev)
+        gmx = [Mx(torch.empty(t.shape, **u8), torch.empty((sq.total, H * D // 32), **u8),
+                  torch.empty(sq.ptiles * H * 512, **u8), ROW)
+               for t, sq in ((dq, seqs_q), (dk, seqs_k), (dv, seqs_k))]
+        gs = [MxOut(m.data.data_ptr(), m.sf_compact.data_ptr(), m.sf_packed.data_ptr())
+              for m in gmx]
     if seqs_q.cu_host is None and seqs_k.cu_host is None:
-        mxfa_bwd(q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse, seqs_q.nseq,
-                 seqs_q.max_len, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
-                 ws.numel(), stream)
+        args = (q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse, seqs_q.nseq,
+                seqs_q.max_len, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
+                ws.numel())
+        if grads_mx:
+            mxfa_bwd_mxg(*args, *gs, stream)
+        else:
+            mxfa_bwd(*args, stream)
     else:
-        mxfa_varlen_bwd(q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse,
-                        seqs_q.cu_dev, seqs_k.cu_dev, seqs_q.nseq, seqs_q.max_len,
-                        seqs_k.max_len, seqs_q.total, seqs_k.total, seqs_q.ptiles,
-                        seqs_k.ptiles, H, D, scale, causal, dq_mode, dq_static, dq, dk, dv, ws,
-                        ws.numel(), stream)
-    return dq, dk, dv
+        args = (q.mx_in(), k.mx_in(), v.mx_in(), do_mx.mx_in(), o, do, lse, seqs_q.cu_dev,
+                seqs_k.cu_dev, seqs_q.nseq, seqs_q.max_len, seqs_k.max_len, seqs_q.total,
+                seqs_k.total, seqs_q.ptiles, seqs_k.ptiles, H, D, scale, causal, dq_mode,
+                dq_static, dq, dk, dv, ws, ws.numel())
+        if grads_mx:
+            mxfa_varlen_bwd_mxg(*args, *gs, stream)
+        else:
+            mxfa_varlen_bwd(*args, stream)
+    return (dq, dk, dv, *gmx) if grads_mx else (dq, dk, dv)
 
 
 def rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float, seg_len: int, H: int,

@@ -151,3 +151,59 @@ def test_bwd_llm_config_sampled_head(mx):
     ref = oracle.method_bwd(sl(qb), sl(kb), sl(vb), sl(dob), o_h_bf, lse_h, None, None, scale, True,
                             True, True)
     check(got, ref, "llm")
+
+
+@pytest.mark.parametrize("varlen,dq_mode", [(False, 0), (False, 1), (True, 0)])
+def test_bwd_mxfp8_gradients(mx, varlen, dq_mode):
+    # the backward that also emits dQ, dK, dV as MXFP8 (1x32 blocks along D):
+    # its bf16 dK and dV equal the plain backward's bit for bit (one CTA owns
+    # each key row), and every MXFP8 payload and scale equals the oracle's ROW
+    # quantization of the same call's bf16 gradient, byte for byte
+    import torch
+    from tests.helpers import unpack_packed
+    H, D = 2, 128
+    scale = 1 / math.sqrt(D)
+    if varlen:
+        lq = [64, 300, 7, 129, 1, 255]
+        lk = [32, 200, 1, 260, 77, 128]
+        qb, kb, vb, dob, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=51)
+        sq, sk = mx.Seqs.varlen(lq, "cuda"), mx.Seqs.varlen(lk, "cuda")
+        causal = False
+    else:
+        B, S = 2, 300
+        lq = lk = [S] * B
+        qb, kb, vb, dob = (b.reshape(B * S, H, D) for b in inputs.dense_attn(B, H, S, D, seed=52))
+        cu_q = cu_k = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+        sq = sk = mx.Seqs.dense(B, S)
+        causal = True
+    o_bits, o_bf, lse = oracle_fwd_out(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal)
+    lse_dev = (torch.from_numpy(lse.astype(np.float32)).cuda() if varlen else
+               torch.from_numpy(lse.reshape(H, len(lq), lq[0]).transpose(1, 0, 2).astype(np.float32)
+                                .copy()).cuda())
+    q = mx.quantize(to_dev(qb), mx.SQ, sq)
+    k = mx.quantize(to_dev(kb), mx.SQ, sk)
+    v = mx.quantize(to_dev(vb), mx.ROW, sk)
+    do_t = to_dev(dob)
+    dmx = mx.quantize(do_t, mx.SQ, sq)
+    o_t = to_dev(o_bits)
+    plain = mx.attention_bwd(q, k, v, dmx, o_t, do_t, lse_dev, sq, sk, scale, causal, dq_mode, 4.0)
+    dq, dk, dv, dq_mx, dk_mx, dv_mx = mx.attention_bwd(q, k, v, dmx, o_t, do_t, lse_dev, sq, sk,
+                                                       scale, causal, dq_mode, 4.0, grads_mx=True)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    bits = lambda t: host(t.view(torch.int16)).view(np.uint16)
+    np.testing.assert_array_equal(bits(dk), bits(plain[1]))
+    np.testing.assert_array_equal(bits(dv), bits(plain[2]))
+    for name, g, m, lens, cu in (("dQ", dq, dq_mx, lq, cu_q), ("dK", dk, dk_mx, lk, cu_k),
+                                 ("dV", dv, dv_mx, lk, cu_k)):
+        gb = bits(g)
+        tokens = gb.shape[0]
+        q_ref, s_ref = oracle.quantize(f64(gb).reshape(tokens, H * D), mx.ROW, cu)
+        np.testing.assert_array_equal(host(m.data).reshape(tokens, H * D), q_ref, err_msg=name)
+        np.testing.assert_array_equal(host(m.sf_compact), s_ref, err_msg=name)
+        comp, pad = unpack_packed(host(m.sf_packed), mx.ROW, lens, H)
+        np.testing.assert_array_equal(comp, s_ref, err_msg=name)
+        assert np.all(pad == 0x7F), name
+    ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale, causal,
+                            True, True)
+    check([host(t.float()).astype(np.float64) for t in (dq, dk, dv)], ref, "mxfp8 grads")

@@ -122,3 +122,47 @@ def test_fwd_llm_config_sampled_heads(mx):
         sl = lambda x: f64(x[b, :, h:h + 1, :])
         oo, lo = oracle.method_fwd(sl(qb), sl(kb), sl(vb), None, None, scale, True, True, 128, THR, True)
         check(o[b, :, h:h + 1, :], lse[b, h:h + 1, :], oo, lo)
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_fwd_mxfp8_output(mx, varlen):
+    # the forward that also emits O as MXFP8 (1x32 blocks along D): its bf16 O
+    # equals the plain forward's bit for bit, and its payload and scales equal
+    # the oracle's ROW quantization of that bf16 O, byte for byte
+    import torch
+    from tests.helpers import unpack_packed
+    H, D = 2, 128
+    if varlen:
+        lens = [64, 300, 7, 129, 1, 255]
+        qb, kb, vb, _, cu, _ = inputs.varlen_attn(lens, lens, H, D, seed=41)
+        seqs = mx.Seqs.varlen(lens, "cuda")
+    else:
+        B, S = 2, 300
+        lens = [S] * B
+        qb, kb, vb, _ = inputs.dense_attn(B, H, S, D, seed=42)
+        qb, kb, vb = (b.reshape(B * S, H, D) for b in (qb, kb, vb))
+        cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+        seqs = mx.Seqs.dense(B, S)
+    scale = 1 / math.sqrt(D)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o_plain, lse_plain = mx.attention_fwd(q, k, v, seqs, seqs, scale, True)
+    o, lse, omx = mx.attention_fwd(q, k, v, seqs, seqs, scale, True, o_mx=True)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    o_bits = host(o.view(torch.int16)).view(np.uint16)
+    np.testing.assert_array_equal(o_bits, host(o_plain.view(torch.int16)).view(np.uint16))
+    np.testing.assert_array_equal(host(lse), host(lse_plain))
+    tokens = o_bits.shape[0]
+    q_ref, s_ref = oracle.quantize(f64(o_bits).reshape(tokens, H * D), mx.ROW, cu)
+    np.testing.assert_array_equal(host(omx.data).reshape(tokens, H * D), q_ref)
+    np.testing.assert_array_equal(host(omx.sf_compact), s_ref)
+    comp, pad = unpack_packed(host(omx.sf_packed), mx.ROW, lens, H)
+    np.testing.assert_array_equal(comp, s_ref)
+    assert np.all(pad == 0x7F)
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu, cu, scale, True, True, 128, THR, True)
+    lse_h = host(lse)
+    if not varlen:  # dense lse is [B][H][S]; the oracle's is [H][tokens]
+        lse_h = lse_h.reshape(len(lens), H, lens[0]).transpose(1, 0, 2).reshape(H, tokens)
+    check(f64(o_bits).reshape(tokens, H, D), lse_h, oo, lo)
