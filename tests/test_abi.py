@@ -106,3 +106,34 @@ def test_rmsnorm_argument_checks(lib):
     assert f(0x1000, 0x2000, 64, 256, 1e-6, 48, 2, r(o), None, None, None) == 2    # seg_len
     assert f(0x1000, 0x2000, 64, 256, 1e-6, 64, 2, None, None, None, None) == 1    # no output
     assert f(0x1000, 0x2000, 64, 256, 1e-6, 64, 4, r(o), None, None, None) == 2    # C != H*128
+
+
+def test_mxfp8_output_argument_checks(lib):
+    # the calls with MXFP8 outputs validate those outputs before any launch
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    m = mxfa.MxIn(0x1000, 0x2000)
+    r = ctypes.byref
+    f = lib.mxfa_fwd_mxo
+    fargs = lambda omx, D=128: (r(m), r(m), r(m), 1, 256, 2, D, 0.1, 0, 0x4000, 0x5000, omx, None)
+    assert f(*fargs(None)) == 1                                  # o_mx required
+    assert f(*fargs(r(_out(data=None)))) == 1                    # o_mx->data required
+    assert f(*fargs(r(_out(data=0x1008)))) == 3                  # payload not 16-byte aligned
+    assert f(*fargs(r(_out(sfc=0x2001)))) == 3                   # compact scales not 4-byte aligned
+    assert f(*fargs(r(_out(sfp=0x3004)))) == 3                   # packed scales not 16-byte aligned
+    assert f(*fargs(r(_out()), D=96)) == 2                       # D still checked
+    v = lib.mxfa_varlen_fwd_mxo
+    assert v(r(m), r(m), r(m), None, None, 2, 10, 10, 20, 20, 2, 2, 2, 128, 0.1, 0, 0x4000, 0x5000,
+             r(_out()), None) == 1                               # varlen needs cu_seqlens
+    b = lib.mxfa_bwd_mxg
+    ws = mxfa.mxfa_bwd_workspace_size(256, 1, 2, 128, 0)
+    bargs = lambda dq, dk, dv, wsb=ws: (r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, 1, 256, 2,
+                                        128, 0.1, 0, 0, 1.0, 0x7000, 0x8000, 0x9000, 0xA000, wsb,
+                                        dq, dk, dv, None)
+    assert b(*bargs(r(_out(sfc=None)), None, None)) == 1         # dQ packed scales need compact
+    assert b(*bargs(None, r(_out(data=0x1004)), None)) == 3      # dK payload misaligned
+    assert b(*bargs(None, None, r(_out(data=None)))) == 1        # dV payload required
+    assert b(*bargs(None, None, None, ws - 1)) == 4              # workspace still checked
+    vb = lib.mxfa_varlen_bwd_mxg
+    assert vb(r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, None, None, 2, 10, 10, 20, 20, 2, 2,
+              2, 128, 0.1, 0, 0, 1.0, 0x7000, 0x8000, 0x9000, 0xA000, ws, None, None, None,
+              None) == 1                                         # varlen needs cu_seqlens
