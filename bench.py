@@ -518,6 +518,19 @@ def profile_op(args):
     return 0
 
 
+# ------------------------------------------------------------------ ranks
+def slowest_rank(torch, dist, times_ms, device):
+    """The largest of each per-rank time over all ranks (every rank gets it)."""
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_pflops(flops_per_rank, world, ms):
+    """Whole-job throughput: the work of all ranks over the slowest rank's step time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e15
+
+
 # ------------------------------------------------------------------ main
 def main():
     args = parse()
@@ -571,9 +584,7 @@ def main():
     ms_e2e = st.e2e(args.steps)
     barrier()
     if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+        ms, ms_e2e = slowest_rank(torch, dist, [ms, ms_e2e], dev)
     assert mxfa.device_status() == 0, "device status after timing"
     acc = None
     if rank == 0 and world == 1 and not args.no_accuracy:
@@ -587,7 +598,7 @@ def main():
             dist.destroy_process_group()
         return 0
     flops = (FWD_FLOPS + BWD_FLOPS) * world
-    value = flops / (ms * 1e-3) / 1e15
+    value = job_pflops(FWD_FLOPS + BWD_FLOPS, world, ms)
     bytes_io = B * S * H * D * 2 * 4
     line = {"metric": METRIC, "value": value, "unit": "PFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
