@@ -12,8 +12,10 @@
 // paragraph 3), 32x32 squares for the backward operands (andresseo.expert,
 // same section).  The fused producer follows brifing.si item 7.
 //
-// These kernels are HBM-bound: each thread owns an 8-column x 32-row slab in
-// registers (16-byte loads, 8-byte stores, every byte read once).
+// These kernels are HBM-bound.  Column and square blocks: each thread owns an
+// 8-column x 32-row slab in registers (16-byte loads, 8-byte stores).  Row
+// blocks: each thread owns whole 1x32 blocks (64 bytes in, 32 bytes out), so
+// no block maximum crosses threads.  Every input byte is read once.
 #include <cuda_bf16.h>
 
 #include "mx_ptx.cuh"
@@ -47,6 +49,60 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
   seq_info(a.seq, g, s0, L);
   const int nrb_real = (L + 31) / 32;
   const int nrb_pad = ((L + 127) / 128) * 4;
+  if (MODE == 0 && rb < nrb_real) {
+    // 1x32 blocks along columns: one thread per (row, 32-column block) with
+    // the block's 64 bytes in registers, so the block maximum needs no
+    // exchange between threads; warp w takes rows w, w + 4, ..., w + 28
+    const int cb = threadIdx.x & 31;
+    const int col = blockIdx.x * 1024 + cb * 32;
+    if (col >= cols) return;
+    const int hd = col / a.D, kb = (col % a.D) / 32;
+    const int kb4 = rb & 3;
+    uint8_t* pbase = nullptr;
+    if (a.sf_packed) {
+      const int64_t tg = seq_units_before(a.seq, g, 128) + (rb >> 2);
+      if (tg >= a.packed_tiles) {
+        atomicOr(&g_status_quant, DEV_BAD_INDEX);
+        return;
+      }
+      pbase = a.sf_packed + (tg * a.H + hd) * 512;
+    }
+    const int64_t r0 = s0 + int64_t(rb) * 32;
+    const int nr = min(32, L - rb * 32);
+    const int rw = threadIdx.x >> 5;
+#pragma unroll 1
+    for (int half = 0; half < 2; half++) {
+      uint4 v[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const int r = rw + 4 * (4 * half + i);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          v[i][k] = r < nr ? ldg16(a.x + (r0 + r) * cols + col + 8 * k) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const int r = rw + 4 * (4 * half + i);
+        if (r < nr) {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 4; k++) {
+            w[4 * k] = v[i][k].x;
+            w[4 * k + 1] = v[i][k].y;
+            w[4 * k + 2] = v[i][k].z;
+            w[4 * k + 3] = v[i][k].w;
+          }
+          const uint32_t sc = mx_block_e8m0(w);
+          mx_block_store(a.data + (r0 + r) * cols + col, w, sc);
+          if (a.sf_compact) a.sf_compact[(r0 + r) * (cols / 32) + col / 32] = uint8_t(sc);
+          if (pbase) pbase[atom_off(kb4 * 32 + r, kb)] = uint8_t(sc);
+        } else if (pbase) {
+          pbase[atom_off(kb4 * 32 + r, kb)] = 0x7F;
+        }
+      }
+    }
+    return;
+  }
   if (rb >= nrb_pad || col0 >= cols) return;
   const int h = col0 / a.D, dcol = col0 % a.D;
   const int tile = rb >> 2, kb4 = rb & 3;
@@ -73,6 +129,7 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
     return;
   }
 
+  if (MODE == 0) return;  // real row blocks were handled above
   const int64_t r0 = s0 + int64_t(rb) * 32;
   const int nr = min(32, L - rb * 32);
   uint4 v[32];
@@ -80,37 +137,7 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
   for (int r = 0; r < 32; r++)
     v[r] = r < nr ? ldg16(a.x + (r0 + r) * cols + col0) : make_uint4(0, 0, 0, 0);
 
-  if (MODE == 0) {  // 1x32 along columns: 4 threads per block, per row
-    const int ncb = cols / 32;
-    uint8_t* pbase = a.sf_packed ? a.sf_packed + (tile_g * a.H + h) * 512 : nullptr;
-#pragma unroll
-    for (int r = 0; r < 32; r++) {
-      uint32_t m = max(max(hmax2(abs2(v[r].x)), hmax2(abs2(v[r].y))),
-                       max(hmax2(abs2(v[r].z)), hmax2(abs2(v[r].w))));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      if (r < nr) {
-        uint32_t s = e8m0_from_bf16abs(m);
-        uint2 out;
-        if (s == 0xFFu) {
-          out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-          float inv[8];
-          float f = e8m0_inv_scale(s);
-#pragma unroll
-          for (int i = 0; i < 8; i++) inv[i] = f;
-          out = cvt8(v[r], inv);
-        }
-        *reinterpret_cast<uint2*>(a.data + (r0 + r) * cols + col0) = out;
-        if (lead) {
-          if (a.sf_compact) a.sf_compact[(r0 + r) * ncb + col0 / 32] = uint8_t(s);
-          if (pbase) pbase[atom_off(kb4 * 32 + r, dcol / 32)] = uint8_t(s);
-        }
-      } else if (lead && pbase) {
-        pbase[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
-      }
-    }
-  } else {
+  {
     // per-column maxima over the 32 rows (pairs of columns per word)
     uint32_t cm[4] = {0, 0, 0, 0};
 #pragma unroll
