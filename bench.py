@@ -385,14 +385,40 @@ def cpu_baseline(qb, kb, vb, dob, s_len=4096):
     import oracle
     cores = oracle.num_threads()
     q, k, v, do, n = oracle_sample(qb, kb, vb, dob, s_len, cores)
+    scale = 1.0 / math.sqrt(D)
     t0 = time.perf_counter()
-    run_oracle_step(oracle, q, k, v, do, 1.0 / math.sqrt(D))
-    dt = time.perf_counter() - t0
-    flops = 14 * D * (s_len * s_len / 2) * n
-    return {"value": flops / dt / 1e15, "unit": "PFLOP/s", "cores": cores, "kind": "oracle",
+    o, lse = oracle.method_fwd(q, k, v, None, None, scale, True, True, 128, 8.0, True)
+    t1 = time.perf_counter()
+    o_bf = np.asarray(o, np.float32).astype(np.float64)
+    oracle.method_bwd(q, k, v, do, o_bf, lse, None, None, scale, True, True, True)
+    t2 = time.perf_counter()
+    dt = t2 - t0
+    pairs = (s_len * s_len / 2) * n
+    # the tiny workload (B1 H2 S256, non-causal) on one host thread, forward + backward
+    from mxfp8_block_scaled_fa_gb300 import inputs
+    tq, tk, tv, tdo = (inputs.bf16_bits_to_f32(x).astype(np.float64).reshape(256, 2, D)
+                       for x in inputs.dense_attn(1, 2, 256, D, seed=0))
+    oracle.set_num_threads(1)
+    try:
+        u0 = time.perf_counter()
+        to, tl = oracle.method_fwd(tq, tk, tv, None, None, scale, False, True, 128, 8.0, True)
+        u1 = time.perf_counter()
+        oracle.method_bwd(tq, tk, tv, tdo, np.asarray(to, np.float32).astype(np.float64), tl, None,
+                          None, scale, False, True, True)
+        u2 = time.perf_counter()
+    finally:
+        oracle.set_num_threads(cores)
+    tiny_pairs = 2 * 256 * 256
+    return {"value": 14 * D * pairs / dt / 1e15, "unit": "PFLOP/s", "cores": cores,
+            "kind": "oracle",
             "sample": f"fwd+bwd (quantize, forward, backward) of the causal {s_len}-token prefix of "
                       f"{n} (batch, head) pairs of the workload, heads in parallel, {dt:.1f} s",
-            "seconds": dt}
+            "seconds": dt,
+            "fwd": {"seconds": t1 - t0, "PFLOP/s": 4 * D * pairs / (t1 - t0) / 1e15},
+            "bwd": {"seconds": t2 - t1, "PFLOP/s": 10 * D * pairs / (t2 - t1) / 1e15},
+            "tiny_1_thread": {"workload": "B1 H2 S256 D128 non-causal", "cores": 1,
+                              "fwd_seconds": u1 - u0, "bwd_seconds": u2 - u1,
+                              "PFLOP/s": 14 * D * tiny_pairs / (u2 - u0) / 1e15}}
 
 
 def accuracy(torch, st, qb, kb, vb, dob, b=1, h=5):
@@ -633,7 +659,8 @@ def main():
                                            f"nominal ratio)"}
         line["components"] = comp
     if cpu is not None:
-        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                     "fwd", "bwd", "tiny_1_thread")}
     if acc is not None:
         line["accuracy"] = acc
     print(json.dumps(line), flush=True)

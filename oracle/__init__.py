@@ -73,6 +73,8 @@ def _load():
                                               ctypes.c_int32, P, P, P, P, P, P, P]
             lib.mxo_num_threads.restype = I32
             lib.mxo_num_threads.argtypes = []
+            lib.mxo_set_num_threads.restype = None
+            lib.mxo_set_num_threads.argtypes = [I32]
             _lib = lib
     return _lib
 
@@ -87,6 +89,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().mxo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Host threads for later calls (results do not depend on the count)."""
+    _load().mxo_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- codecs

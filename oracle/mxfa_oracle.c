@@ -583,3 +583,13 @@ int mxo_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Host threads the oracle uses from now on (timing runs; results do not
+ * depend on it: every output element keeps its own summation order). */
+void mxo_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -320,3 +320,20 @@ def test_backward_p_clamped_at_one(fp32):
     tol = 1e-6 if fp32 else 1e-15
     assert abs(dv[1, 0, 0] - math.exp(-0.5)) <= tol
     assert abs(dv[2, 0, 0] - math.exp(-2.0)) <= tol
+
+
+def test_results_do_not_depend_on_thread_count():
+    # every output element keeps its own summation order, so the oracle's
+    # results are bit-identical on one host thread and on all of them
+    q, k, v, do = (_rand((96, 2, 128), s) for s in (70, 71, 72, 73))
+    scale = 1 / math.sqrt(128)
+    cores = oracle.num_threads()
+    runs = []
+    for n in (1, cores):
+        oracle.set_num_threads(n)
+        o, lse = oracle.method_fwd(q, k, v, None, None, scale, True, True, 128, 8.0, True)
+        g = oracle.method_bwd(q, k, v, do, o, lse, None, None, scale, True, True, True)
+        runs.append((o, lse) + tuple(g))
+    oracle.set_num_threads(cores)
+    for a, b in zip(*runs):
+        np.testing.assert_array_equal(a, b)
