@@ -355,6 +355,29 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     pairs = float(np.sum(lq.astype(np.float64) * lk)) * Hj
     res["jagged_fwd"] = {"ms": t_jf, "pflops": 4 * D * pairs / t_jf / 1e12}
     res["jagged_bwd"] = {"ms": t_jb, "pflops": 10 * D * pairs / t_jb / 1e12}
+    del qR, kR, vC, qS, kS, vR, do_t, doS, o, lse, out, ws, grads
+    # the outlier workload: B8 H32 S4096 non-causal, outlier recipe on Q and K
+    Bo, Ho, So = 8, 32, 4096
+    qb, kb, vb, dob = inputs.dense_attn(Bo, Ho, So, D, seed=2, outliers=True)
+    so = mx.Seqs.dense(Bo, So)
+    to = lambda b: torch.from_numpy(b.view("int16")).view(torch.bfloat16).reshape(Bo * So, Ho, D).to(dev)
+    qo, ko, vo, doo = to(qb), to(kb), to(vb), to(dob)
+    del qb, kb, vb, dob
+    fq = [mx.quantize(qo, 0, so), mx.quantize(ko, 0, so), mx.quantize(vo, 1, so)]
+    bq = [mx.quantize(qo, 2, so), mx.quantize(ko, 2, so), mx.quantize(vo, 0, so),
+          mx.quantize(doo, 2, so)]
+    oo, lo = mx.attention_fwd(*fq, so, so, 1 / math.sqrt(D), False)
+    t_of = time_loop(torch, lambda: mx.attention_fwd(*fq, so, so, 1 / math.sqrt(D), False,
+                                                     out=(oo, lo)), iters, warmup)
+    wso = torch.empty(mx.mxfa_bwd_workspace_size(Bo * So, Bo, Ho, D, 0), dtype=torch.uint8, device=dev)
+    go = tuple(torch.empty_like(oo) for _ in range(3))
+    t_ob = time_loop(torch, lambda: mx.attention_bwd(*bq, oo, doo, lo, so, so, 1 / math.sqrt(D),
+                                                     False, ws=wso, out=go), iters, warmup)
+    of = attn_flops(Bo, Ho, So, D, False, 4)
+    res["outlier_fwd"] = {"ms": t_of, "pflops": of / t_of / 1e12,
+                          "workload": "B8 H32 S4096 D128 non-causal, outlier recipe"}
+    res["outlier_bwd"] = {"ms": t_ob, "pflops": 2.5 * of / t_ob / 1e12}
+    del qo, ko, vo, doo, fq, bq, oo, lo, wso, go
     step_q = (4 * t_q + 2 * t_qs + t_qc) / 7 * 7
     res["step_share"] = {"fwd": t_fwd, "bwd": t_bwd, "quantize_x7": step_q}
     del flush_buf
