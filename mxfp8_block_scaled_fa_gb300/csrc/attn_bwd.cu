@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           for (int c = 0; c < 32; c++) sv[c] = fminf(sv[c], 0.0f);
           tmax = 0.0f;
         }
-        float dmax = 0.0f, dmin = 0.0f;
+        float damax = 0.0f;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           // P = 2^t, dS = P * (dP - Delta)
@@ -581,15 +581,14 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           sv[c + 1] = p1;
           dp[c] = ds.x;
           dp[c + 1] = ds.y;
-          dmax = fmax3(dmax, ds.x, ds.y);
-          dmin = fmin3(dmin, ds.x, ds.y);
+          damax = fmax3(damax, fabsf(ds.x), fabsf(ds.y));
         }
         // the largest P of this thread's block (2^t is monotone in t)
         pmax = bex2(tmax);
         // P^T: one 1x32 block along queries per thread; dS: one 32x32 block
         // per warp, its maximum by a warp-wide absolute-maximum reduction
         float wmax;
-        asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(fmaxf(dmax, -dmin)));
+        asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(damax));
         sp = e8m0_from_amax(pmax);
         sd = e8m0_from_amax(wmax);
         const float2 ip = make_float2(e8m0_inv_scale(sp), e8m0_inv_scale(sp));
