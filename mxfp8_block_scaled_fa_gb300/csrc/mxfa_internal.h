@@ -103,6 +103,7 @@ struct BwdArgs {
   void* dq_acc;            // workspace [total_q][H][128] fp32 or fp16
   int64_t lse_hstride;
   int dense_lse;
+  int head_group;  // dense: heads whose key tiles are scheduled together (set by launch_bwd)
 };
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 
