@@ -53,7 +53,7 @@ def attn_flops(b, h, s, d, causal, per_pair):
 
 # DRAM bytes of one attn_bwd_kernel launch at this workload, from one ncu capture
 # (profiles/attn_bwd_kernel_llm_traffic.md); null once the kernel changes.
-BWD_TRAFFIC_BYTES = 1328065536 + 921119488
+BWD_TRAFFIC_BYTES = 1328746752 + 922691328
 
 FWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 4)
 BWD_FLOPS = attn_flops(B, H, S, D, CAUSAL, 10)
