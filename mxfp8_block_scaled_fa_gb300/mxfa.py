@@ -6,6 +6,19 @@ stream -> ``cudaStream_t``).  The helpers below them (``quantize``,
 ``attention_fwd`` ...) allocate outputs with torch and call those entry points;
 every arithmetic step runs in the library's CUDA kernels.  Nothing here falls
 back to the CPU: a missing library or a CUDA-less process raises.
+
+A training step on bf16 q, k, v, do of shape [B * S, H, 128] (dense, causal):
+
+    seqs = Seqs.dense(B, S)
+    scale = 1 / math.sqrt(128)
+    o, lse = attention_fwd(quantize(q, ROW, seqs), quantize(k, ROW, seqs),
+                           quantize(v, COL, seqs), seqs, seqs, scale, causal=True)
+    dq, dk, dv = attention_bwd(quantize(q, SQ, seqs), quantize(k, SQ, seqs),
+                               quantize(v, ROW, seqs), quantize(do, SQ, seqs),
+                               o, do, lse, seqs, seqs, scale, causal=True)
+
+Jagged batches use ``Seqs.varlen(lengths, device)`` for queries and keys;
+``o_mx=True`` / ``grads_mx=True`` also return O / the gradients as MXFP8.
 """
 from __future__ import annotations
 
