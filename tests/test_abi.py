@@ -137,3 +137,12 @@ def test_mxfp8_output_argument_checks(lib):
     assert vb(r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, None, None, 2, 10, 10, 20, 20, 2, 2,
               2, 128, 0.1, 0, 0, 1.0, 0x7000, 0x8000, 0x9000, 0xA000, ws, None, None, None,
               None) == 1                                         # varlen needs cu_seqlens
+
+
+def test_package_exposes_the_public_api():
+    # the package forwards the binding's public names without loading the library
+    import mxfp8_block_scaled_fa_gb300 as pkg
+    for n in ("Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ", "quantize", "sf_pack",
+              "attention_fwd", "attention_bwd", "rmsnorm_quant", "device_status", "lib",
+              "MxfaError", "mxfa_fwd", "mxfa_bwd", "mxfa_fwd_mxo", "mxfa_bwd_mxg"):
+        assert getattr(pkg, n) is not None, n
