@@ -8,14 +8,17 @@
 //   five GEMMs with recompute -- S^T = K Q^T, dP^T = V dO^T, dV += P^T dO,
 //   dK += dS^T Q, dQ^T = K^T dS^T -- on MXFP8 operands.  Q, K and dO carry
 //   32x32 square scales, so one E4M3 payload serves both GEMM orientations;
-//   V carries 1x32 scales along D.  P = exp(S tau - lse) is quantized in 1x32
-//   blocks along queries (the dV contraction), dS = P (dP - Delta) once per
-//   32x32 block with a warp-wide absolute-maximum reduction.  dQ partials are
-//   reduced into a global accumulator in FP32, or in FP16 after multiplying by
-//   a static power-of-two scale.
+//   V carries 1x32 scales along D.  P = exp(min(S tau - lse, 0)) is quantized
+//   in 1x32 blocks along queries (the dV contraction); the min keeps P <= 1
+//   when the square-block scores exceed the forward's lse.  dS = P (dP - Delta)
+//   is quantized once per 32x32 block with a warp-wide absolute-maximum
+//   reduction.  dQ partials are reduced into a global accumulator in FP32, or
+//   in FP16 after multiplying by a static power-of-two scale.  dQ, dK, dV are
+//   written as bf16 and, on request, also as MXFP8 (1x32 along D).
 //
 // Structure: one CTA = one 128-key tile of one head, looping over 64-query
-// tiles (16 warps, 1 CTA per SM):
+// tiles (16 warps, 1 CTA per SM; dense non-causal grids run heads in groups
+// so that their fp32 dQ rows stay in L2):
 //   warp 0       TMA producer: K, V (+ V scale atom) once; ring of Q_i, dO_i
 //                and the tile records made by the preparation kernel
 //   warp 1       TMEM owner + MMA issuer for S^T and dP^T
