@@ -25,7 +25,9 @@
 // PV_X(j)), and the Q / K scales of the other tile's next S GEMM [40,48).
 // The running max moves only when it grows by more than kRescaleThr (log2
 // units); P~ then stays below 2^kRescaleThr, which the E8M0 block scale
-// absorbs, and O and l carry the stale max exactly.
+// absorbs, and O and l carry the stale max exactly.  The epilogue writes O as
+// bf16 and, on request, also as MXFP8 (the bf16 row quantized in 1x32 blocks
+// along D, with compact and packed scales).
 #include <cuda_bf16.h>
 
 #include "mx_ptx.cuh"
