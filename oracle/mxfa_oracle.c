@@ -8,9 +8,12 @@
  * header, table or constant generator with the CUDA path.
  *
  * Arithmetic is fp64 throughout, except mxo_rmsnorm_quant, which follows the
- * fp32 operation order that the fused kernel documents: its results decide
- * integer codes (E8M0 scales, E4M3 payloads), and such decisions are taken in
- * the same precision on both sides.
+ * fp32 operation order that the fused kernel documents, and the attention
+ * functions' score_fp32 mode, which rounds the values that decide P's and
+ * dS's codes to fp32: those results decide integer codes (E8M0 scales, E4M3
+ * payloads), and such decisions are taken in the same precision on both
+ * sides.  With score_fp32 = 0 the attention functions are the plain fp64
+ * definitions that the pins check.
  *
  * Sources (each function cites the passage it follows):
  *  [MX]  "Low-Precision FlashAttention-4: End-to-End Block-Scaled Attention on
@@ -40,7 +43,9 @@
  *  - P below 2^-126 is flushed to zero (fp32 flush-to-zero of the exponential);
  *  - fp32 row sum of the unquantized P;
  *  - backward P quantized in 1x32 blocks along queries (the dV contraction),
- *    dS in 32x32 blocks; tau applied after the contraction.
+ *    dS in 32x32 blocks; tau applied after the contraction;
+ *  - backward P = exp(min(S tau - lse, 0)): exact attention never exceeds 1,
+ *    and the square-block scores can exceed the forward's lse.
  */
 #include <math.h>
 #include <stdint.h>
