@@ -132,6 +132,15 @@ mxfa_status mxfa_sf_pack(const uint8_t* sf_compact, int64_t tokens, int H, int D
                          const int32_t* cu_seqlens, int nseq, int max_seqlen,
                          int64_t packed_tiles, uint8_t* sf_packed, mxfa_stream_t stream);
 
+/* mxfa_sf_unpack -- packed scales -> compact scales: the inverse of
+ * mxfa_sf_pack for every real row / block (padding bytes are not read).
+ * It gives tests and tools a C-ABI round trip of the packed layout that the
+ * tensor core reads; it is not on the training path.  Arguments as
+ * mxfa_sf_pack with the roles of the two scale buffers exchanged. */
+mxfa_status mxfa_sf_unpack(const uint8_t* sf_packed, int64_t tokens, int H, int D, mxfa_block blk,
+                           const int32_t* cu_seqlens, int nseq, int max_seqlen,
+                           int64_t packed_tiles, uint8_t* sf_compact, mxfa_stream_t stream);
+
 /* mxfa_fwd -- dense forward ([KDIM] paragraphs 1-2, [TMEM]).
  *  q, k       ROW-quantized payload [B][S][H][128] + packed ROW scales
  *  v          COL-quantized payload + packed COL scales
@@ -145,7 +154,10 @@ mxfa_status mxfa_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B
 
 /* mxfa_varlen_fwd -- jagged forward ([TMEM] split addressing, [ITEMS] 5).
  *  cu_seqlens_q/k  DEVICE int32[nseq+1]; q/o/lse follow cu_seqlens_q,
- *                  k/v follow cu_seqlens_k; every key length >= 1
+ *                  k/v follow cu_seqlens_k.  Lengths may be 0: a query
+ *                  sequence whose key sequence is empty gets O = 0 and
+ *                  lse = -inf (the empty softmax sum); an empty query
+ *                  sequence writes nothing.  max_seqlen_k must be >= 1.
  *  ptiles_q/k      mxfa_packed_tiles() of the query / key sequences
  *  lse             fp32 [H][total_q]
  *  causal          top-left aligned (key index > query index masked) */
@@ -201,7 +213,8 @@ mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const
                      void* dk, void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
 
 /* mxfa_varlen_bwd -- jagged backward; arguments as mxfa_varlen_fwd and
- * mxfa_bwd (lse [H][total_q]). */
+ * mxfa_bwd (lse [H][total_q]).  Keys of a sequence with no queries get
+ * dK = dV = 0; queries of a sequence with no keys get dQ = 0. */
 mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
                             const mxfa_mx* dout_mx, const void* o, const void* dout, const float* lse,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,

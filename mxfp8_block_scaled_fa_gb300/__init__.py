@@ -12,7 +12,7 @@ from . import inputs  # noqa: F401  (seeded synthetic workloads; no arithmetic)
 def __getattr__(name):
     if name.startswith("mxfa_") or name in ("lib", "MxfaError",
                                             "Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ",
-                                            "quantize", "sf_pack", "attention_fwd",
+                                            "quantize", "sf_pack", "sf_unpack", "attention_fwd",
                                             "attention_bwd", "rmsnorm_quant",
                                             "device_status"):
         from . import mxfa as _m

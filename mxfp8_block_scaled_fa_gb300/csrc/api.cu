@@ -13,6 +13,24 @@
 
 using namespace mxfa;
 
+namespace mxfa {
+
+int sm_count_current_device() {
+  static std::atomic<int> count[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = count[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  if (dev >= 0 && dev < kMaxDevices) count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace mxfa
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -304,6 +322,27 @@ mxfa_status mxfa_sf_pack(const uint8_t* sf_compact, int64_t tokens, int H, int D
   a.sf_packed = sf_packed;
   if (tokens == 0) return MXFA_OK;
   return from_cuda(launch_sf_pack(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_sf_unpack(const uint8_t* sf_packed, int64_t tokens, int H, int D, mxfa_block blk,
+                           const int32_t* cu, int nseq, int max_seqlen, int64_t packed_tiles,
+                           uint8_t* sf_compact, mxfa_stream_t stream) {
+  if (!sf_compact || !sf_packed || H <= 0 || packed_tiles <= 0) return MXFA_ERR_INVALID_ARG;
+  if (blk < MXFA_BLK_ROW || blk > MXFA_BLK_SQ) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  mxfa_status s = check_seqs(cu, nseq, max_seqlen, tokens);
+  if (s) return s;
+  PackArgs a;
+  a.sf_compact = nullptr;
+  a.tokens = tokens;
+  a.H = H;
+  a.D = D;
+  a.mode = int(blk);
+  a.seq = Seqs{cu, nseq, max_seqlen};
+  a.packed_tiles = packed_tiles;
+  a.sf_packed = const_cast<uint8_t*>(sf_packed);
+  if (tokens == 0) return MXFA_OK;
+  return from_cuda(launch_sf_unpack(a, sf_compact, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mxfa_status mxfa_fwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H, int D,

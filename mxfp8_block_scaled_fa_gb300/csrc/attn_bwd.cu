@@ -743,20 +743,21 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         bwd::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  clear_stale_error();
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bwd::SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   const int64_t rows = a.total_q * a.H;
   const size_t esz = a.dq_mode == 1 ? 2 : 4;
-  cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, size_t(rows) * 128 * esz, st);
+  e = cudaMemsetAsync(a.dq_acc, 0, size_t(rows) * 128 * esz, st);
   if (e != cudaSuccess) return e;
   {
     dim3 pg(unsigned((a.sq.seqlen + bwd::QT - 1) / bwd::QT), unsigned(a.H), unsigned(a.sq.nseq));
     if (pg.x > 0) bwd_prep_kernel<<<pg, 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   dim3 grid;
   BwdArgs args = a;
@@ -769,20 +770,17 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     // S4096).  Causal: one group of all heads (key tile major), which keeps
     // concurrent CTAs on different heads' dQ rows -- grouping measured 5%
     // slower there, its CTAs' reduce-adds contending for the same rows.
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        sms = 148;
-    }
+    int sms = sm_count_current_device();
+    if (sms <= 0) sms = 148;
     args.head_group = (a.causal || nkt <= 0) ? max(per, 1) : min(per, max(1, (2 * sms + nkt - 1) / nkt));
     grid = dim3(unsigned(nkt * per), 1, 1);
   } else {
     grid = dim3(unsigned((a.sk.seqlen + bwd::KT - 1) / bwd::KT), unsigned(a.H), unsigned(a.sk.nseq));
   }
-  if (grid.x > 0 && grid.y > 0 && grid.z > 0)
+  if (grid.x > 0 && grid.y > 0 && grid.z > 0) {
     attn_bwd_kernel<<<grid, bwd::NTHREADS, bwd::SMEM_BYTES, st>>>(args);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const int64_t n = rows * 128;
   const float mult = a.dq_mode == 1 ? 1.0f / a.dq_static_scale : a.scale;
   if (a.dqmx == nullptr) {
@@ -791,8 +789,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     bwd_post_mx_kernel<<<unsigned((n / 32 + 255) / 256), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode, mult,
                                                                        a.dqmx, a.dqmx_sfc);
     if (a.dqmx_sfp != nullptr) {
-      cudaError_t e = cudaPeekAtLastError();
-      if (e != cudaSuccess) return e;
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
       PackArgs p;
       p.sf_compact = a.dqmx_sfc;
       p.tokens = rows / a.H;
@@ -805,7 +802,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
       return launch_sf_pack(p, st);
     }
   }
-  return cudaPeekAtLastError();
+  return cudaGetLastError();
 }
 
 unsigned read_status_bwd(cudaStream_t st) {

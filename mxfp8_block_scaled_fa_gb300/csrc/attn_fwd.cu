@@ -394,11 +394,15 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       fwd_warp_arrive(BAR(B_PFULL + x), lane);
       m = mu;
     }
-    // ---- epilogue: O / l -> bf16, LSE
-    if (ok && nkv_x > 0 &&
-        __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE + x), (nkv_x - 1) & 1, abort_flag, &g_status_fwd))) {
+    // ---- epilogue: O / l -> bf16, LSE.  A tile with no key to visit (an
+    // empty key sequence) writes O = 0 and lse = -inf, the empty softmax sum.
+    const bool tile_exists = x == 0 || has_b;
+    if (ok && tile_exists &&
+        (nkv_x == 0 ||
+         __all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ODONE + x), (nkv_x - 1) & 1, abort_flag, &g_status_fwd)))) {
       tc_fence_after();
       const bool valid = qpos < lq;
+      const bool any_key = nkv_x > 0;
       const float rl = 1.0f / l;
       const int64_t tok = sq0 + qpos;
       uint16_t* orow = a.o + (tok * a.H + h) * 128;
@@ -406,13 +410,19 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
 #pragma unroll
       for (int c = 0; c < 4; c++) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
-        tmem_wait_ld();
+        if (any_key) {
+          tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e++) o[e] = 0u;
+        }
+        const float r = any_key ? rl : 0.0f;
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * rl,
-                                                    __uint_as_float(o[2 * e + 1]) * rl);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * r,
+                                                    __uint_as_float(o[2 * e + 1]) * r);
           w[e] = *reinterpret_cast<uint32_t*>(&p2);
         }
         if (valid) {
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         }
       }
       if (valid) {
-        const float lse = (m + log2f(l)) * 0.69314718055994530942f;
+        const float lse = any_key ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         if (a.dense_lse)
           a.lse[(int64_t(g) * a.H + h) * a.lse_hstride + qpos] = lse;
         else
@@ -457,13 +467,13 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         fwd::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  clear_stale_error();
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fwd::SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid;
   if (a.sq.cu == nullptr) {
     const int npair = (a.sq.seqlen + 2 * fwd::TILE - 1) / (2 * fwd::TILE);
@@ -474,7 +484,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   attn_fwd_kernel<<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
-  return cudaPeekAtLastError();
+  return cudaGetLastError();
 }
 
 unsigned read_status_fwd(cudaStream_t st) {

@@ -17,6 +17,7 @@
 // lookup, so make that first call before any stream capture.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <mutex>
 
 #include "../../include/mxfa.h"
@@ -29,6 +30,8 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_bwd_scratch on the current device (nullptr on error).
@@ -38,7 +41,10 @@ void* scratch_on_current_device() {
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();  // leave no stale error for the caller's next runtime call
+      return nullptr;
+    }
     g_scratch_ptr[dev] = p;
   }
   return g_scratch_ptr[dev];
@@ -55,6 +61,16 @@ extern "C" mxfa_status mxfa_bwd_noalloc(const mxfa_mx* q, const mxfa_mx* k, cons
                                         float dq_static_scale, void* dq, void* dk, void* dv,
                                         mxfa_stream_t stream) {
   if (B <= 0 || S <= 0 || H <= 0 || D <= 0) return MXFA_ERR_INVALID_ARG;
+  // the argument checks that need no workspace come first, so that a bad
+  // call is reported the same way mxfa_bwd reports it
+  for (const mxfa_mx* m : {q, k, v, dout_mx}) {
+    if (!m || !m->data || !m->sf) return MXFA_ERR_INVALID_ARG;
+    if (!aligned16(m->data) || !aligned16(m->sf)) return MXFA_ERR_MISALIGNED;
+  }
+  if (!o || !dout || !lse || !dq || !dk || !dv) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return MXFA_ERR_MISALIGNED;
   const size_t need = mxfa_bwd_workspace_size(int64_t(B) * S, B, H, D, dq_mode);
   if (need == 0) return MXFA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return MXFA_ERR_WORKSPACE_TOO_SMALL;

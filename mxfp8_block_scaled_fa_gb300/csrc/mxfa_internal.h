@@ -5,7 +5,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mxfa {
+
+// ---------------------------------------------------------- per-device state
+// Launch attributes (the opt-in to large dynamic shared memory) and device
+// properties belong to one device's context, so they are set and cached per
+// device: bit d of `done` records that `fn` has succeeded on device d.
+// Concurrent first calls may both run `fn`, which is idempotent.
+constexpr int kMaxDevices = 64;
+template <class F>
+cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return fn();
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Number of SMs of the current device (0 on error), cached per device.
+int sm_count_current_device();
+
+// Clears an error left by earlier runtime calls of this thread, so that the
+// check after this call's launches reports only this call's own failures.
+inline void clear_stale_error() { (void)cudaGetLastError(); }
 
 // Sequence geometry.  When cu == nullptr every sequence has length `seqlen`
 // and sequence g starts at token g * seqlen.
@@ -38,6 +66,8 @@ struct PackArgs {
   uint8_t* sf_packed;
 };
 cudaError_t launch_sf_pack(const PackArgs& a, cudaStream_t s);
+// Inverse of launch_sf_pack: reads a.sf_packed, writes the compact scales.
+cudaError_t launch_sf_unpack(const PackArgs& a, uint8_t* sf_compact, cudaStream_t s);
 
 struct RmsArgs {
   const uint16_t* x;

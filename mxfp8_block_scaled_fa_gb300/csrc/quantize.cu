@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  clear_stale_error();
   const int cols = a.H * a.D;
   dim3 grid((cols + 1023) / 1024, 4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
@@ -209,7 +210,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
     case 1: quant_kernel<1><<<grid, 128, 0, st>>>(a); break;
     default: quant_kernel<2><<<grid, 128, 0, st>>>(a); break;
   }
-  return cudaPeekAtLastError();
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ sf pack
@@ -257,11 +258,60 @@ __global__ void __launch_bounds__(256) sf_pack_kernel(PackArgs a) {
   }
 }
 
+// Packed (MMA atom) scales -> compact scales: the inverse of sf_pack_kernel
+// for every real row / block (padding bytes are not read).  Same grid.
+__global__ void __launch_bounds__(256) sf_unpack_kernel(PackArgs a, uint8_t* __restrict__ sf_compact) {
+  const int cols = a.H * a.D;
+  const int ncb = cols / 32;
+  const int g = blockIdx.y, rb = blockIdx.x;
+  int64_t s0;
+  int L;
+  seq_info(a.seq, g, s0, L);
+  if (rb >= (L + 31) / 32) return;
+  const int tile = rb >> 2, kb4 = rb & 3;
+  const int64_t tile_g = seq_units_before(a.seq, g, 128) + tile;
+  if (tile_g >= a.packed_tiles) {
+    atomicOr(&g_status_quant, DEV_BAD_INDEX);
+    return;
+  }
+  const uint8_t* pk = a.sf_packed;
+  if (a.mode == 0) {
+    const int nr = min(32, L - rb * 32);
+    for (int i = threadIdx.x; i < nr * ncb; i += blockDim.x) {
+      const int r = i / ncb, cb = i % ncb;
+      const int h = cb / (a.D / 32), kb = cb % (a.D / 32);
+      sf_compact[(s0 + rb * 32 + r) * ncb + cb] = pk[(tile_g * a.H + h) * 512 + atom_off(kb4 * 32 + r, kb)];
+    }
+  } else {
+    const int64_t b32 = seq_units_before(a.seq, g, 32) + rb;
+    if (a.mode == 1) {
+      for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+        const int h = c / a.D, d = c % a.D;
+        sf_compact[b32 * cols + c] = pk[(tile_g * a.H + h) * 512 + atom_off(d, kb4)];
+      }
+    } else {
+      for (int cb = threadIdx.x; cb < ncb; cb += blockDim.x) {
+        const int h = cb / (a.D / 32), kb = cb % (a.D / 32);
+        sf_compact[b32 * ncb + cb] = pk[(tile_g * a.H + h) * 16 + kb4 * 4 + kb];
+      }
+    }
+  }
+}
+
+cudaError_t launch_sf_unpack(const PackArgs& a, uint8_t* sf_compact, cudaStream_t st) {
+  clear_stale_error();
+  dim3 grid(4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  sf_unpack_kernel<<<grid, 256, 0, st>>>(a, sf_compact);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sf_pack(const PackArgs& a, cudaStream_t st) {
+  clear_stale_error();
   dim3 grid(4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   sf_pack_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaPeekAtLastError();
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------- RMSNorm+Quantize
@@ -499,23 +549,19 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
 
 template <int NK>
 cudaError_t launch_rms_nk(const RmsArgs& a, cudaStream_t st) {
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rms_quant_kernel<NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               rms::smem_bytes(NK * 256));
-    if (e != cudaSuccess) {
-      nsm = 0;
-      return e;
-    }
-  }
+  static std::atomic<unsigned long long> attr{0};
+  clear_stale_error();
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(rms_quant_kernel<NK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                rms::smem_bytes(NK * 256));
+  });
+  if (e != cudaSuccess) return e;
+  const int nsm = sm_count_current_device();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
   const int64_t nblk = (a.T + 31) / 32;
   const unsigned grid = unsigned(nblk < nsm ? nblk : int64_t(nsm));
   rms_quant_kernel<NK><<<grid, rms::NTHREADS, rms::smem_bytes(NK * 256), st>>>(a);
-  return cudaPeekAtLastError();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_quant(const RmsArgs& a, cudaStream_t st) {

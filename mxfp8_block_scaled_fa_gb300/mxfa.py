@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "mxfa_sf_packed_bytes": (S, [I, I64, I]),
             "mxfa_quantize": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
             "mxfa_sf_pack": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
+            "mxfa_sf_unpack": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
             "mxfa_fwd": (I, [P, P, P, I, I, I, I, F, I, P, P, P]),
             "mxfa_varlen_fwd": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P, P,
                                     P]),
@@ -137,6 +138,13 @@ def mxfa_sf_pack(sf_compact, tokens, H, D, blk, cu_seqlens, nseq, max_seqlen, pa
                  sf_packed, stream=None):
     _check(lib().mxfa_sf_pack(_p(sf_compact), tokens, H, D, blk, _p(cu_seqlens), nseq, max_seqlen,
                               packed_tiles, _p(sf_packed), _stream(stream)), "mxfa_sf_pack")
+
+
+def mxfa_sf_unpack(sf_packed, tokens, H, D, blk, cu_seqlens, nseq, max_seqlen, packed_tiles,
+                   sf_compact, stream=None):
+    _check(lib().mxfa_sf_unpack(_p(sf_packed), tokens, H, D, blk, _p(cu_seqlens), nseq,
+                                max_seqlen, packed_tiles, _p(sf_compact), _stream(stream)),
+           "mxfa_sf_unpack")
 
 
 def mxfa_fwd(q: MxIn, k: MxIn, v: MxIn, B, S, H, D, scale, causal, o, lse, stream=None):
@@ -284,6 +292,16 @@ def sf_pack(sf_compact: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 128
     mxfa_sf_pack(sf_compact, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len,
                  seqs.ptiles, sfp, stream)
     return sfp
+
+
+def sf_unpack(sf_packed: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 128,
+              stream=None) -> torch.Tensor:
+    """Packed scales -> compact scales (the inverse of sf_pack)."""
+    comp_shape, _ = _sf_shapes(blk, seqs, H, D)
+    sfc = torch.empty(comp_shape, dtype=torch.uint8, device=sf_packed.device)
+    mxfa_sf_unpack(sf_packed, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len,
+                   seqs.ptiles, sfc, stream)
+    return sfc
 
 
 def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,

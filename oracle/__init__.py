@@ -64,10 +64,10 @@ def _load():
             lib.mxo_dequantize.argtypes = [P, P, I64, I64, I32, P, I32, P]
             lib.mxo_attn_fwd.restype = None
             lib.mxo_attn_fwd.argtypes = [P, P, P, P, P, I32, I32, I32, D, I32, I32,
-                                         I32, D, P, P, I64, I32]
+                                         I32, D, P, P, I64]
             lib.mxo_attn_bwd.restype = None
             lib.mxo_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, D,
-                                         I32, I32, I32, P, P, P, I64, I32]
+                                         I32, I32, I32, P, P, P, I64]
             lib.mxo_rmsnorm_quant.restype = None
             lib.mxo_rmsnorm_quant.argtypes = [P, P, I64, I64, ctypes.c_float, I32,
                                               ctypes.c_int32, P, P, P, P, P, P, P]
@@ -169,11 +169,8 @@ def qdq(x3d, mode: int, cu=None) -> np.ndarray:
 
 # ------------------------------------------------------------- attention
 def attn_fwd(q, k, v, cu_q, cu_k, scale, causal=False, quant_p=True, tile_n=128,
-             lazy_thr=0.0, score_fp32=False):
-    """Forward on dequantized operands [tokens, H, D] -> (O float64, lse [H, tokens]).
-
-    score_fp32 takes the values that decide P's quantization codes in fp32
-    (the kernel's precision) instead of fp64."""
+             lazy_thr=0.0):
+    """Forward on dequantized operands [tokens, H, D] -> (O float64, lse [H, tokens])."""
     lib = _load()
     q, k, v = (_c(a, np.float64) for a in (q, k, v))
     tq, H, D = q.shape
@@ -183,12 +180,12 @@ def attn_fwd(q, k, v, cu_q, cu_k, scale, causal=False, quant_p=True, tile_n=128,
     lse = np.zeros((H, tq), np.float64)
     lib.mxo_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), n, H, D,
                      float(scale), int(causal), int(quant_p), int(tile_n),
-                     float(lazy_thr), _ptr(o), _ptr(lse), tq, int(score_fp32))
+                     float(lazy_thr), _ptr(o), _ptr(lse), tq)
     return o, lse
 
 
 def attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal=False,
-             quant_p=True, quant_ds=True, score_fp32=False):
+             quant_p=True, quant_ds=True):
     """Backward on dequantized operands -> (dQ, dK, dV) float64 [tokens, H, D]."""
     lib = _load()
     q, k, v, do, o_bf, do_bf = (_c(a, np.float64) for a in (q, k, v, do, o_bf, do_bf))
@@ -201,14 +198,13 @@ def attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal=False,
     dv = np.zeros_like(v)
     lib.mxo_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(o_bf), _ptr(do_bf),
                      _ptr(lse), _ptr(cq), _ptr(ck), n, H, D, float(scale), int(causal),
-                     int(quant_p), int(quant_ds), _ptr(dq), _ptr(dk), _ptr(dv), tq,
-                     int(score_fp32))
+                     int(quant_p), int(quant_ds), _ptr(dq), _ptr(dk), _ptr(dv), tq)
     return dq, dk, dv
 
 
 # --------------------------------------------------- the method, end to end
 def method_fwd(q_bf, k_bf, v_bf, cu_q, cu_k, scale, causal=False, quant=True,
-               tile_n=128, lazy_thr=0.0, score_fp32=False):
+               tile_n=128, lazy_thr=0.0):
     """Quantize Q, K (1x32 along D) and V (32x1 along keys), then attention."""
     if quant:
         q = qdq(q_bf, ROW, cu_q)
@@ -216,11 +212,11 @@ def method_fwd(q_bf, k_bf, v_bf, cu_q, cu_k, scale, causal=False, quant=True,
         v = qdq(v_bf, COL, cu_k)
     else:
         q, k, v = q_bf, k_bf, v_bf
-    return attn_fwd(q, k, v, cu_q, cu_k, scale, causal, quant, tile_n, lazy_thr, score_fp32)
+    return attn_fwd(q, k, v, cu_q, cu_k, scale, causal, quant, tile_n, lazy_thr)
 
 
 def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=False,
-               quant=True, score_fp32=False):
+               quant=True):
     """Square-block Q, K, dO and row-block V, then the five-GEMM backward."""
     if quant:
         q = qdq(q_bf, SQ, cu_q)
@@ -230,7 +226,7 @@ def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=Fal
     else:
         q, k, do, v = q_bf, k_bf, do_bf, v_bf
     return attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal,
-                    quant, quant, score_fp32)
+                    quant, quant)
 
 
 # ------------------------------------------------------ RMSNorm+Quantize

@@ -8,12 +8,9 @@
  * header, table or constant generator with the CUDA path.
  *
  * Arithmetic is fp64 throughout, except mxo_rmsnorm_quant, which follows the
- * fp32 operation order that the fused kernel documents, and the attention
- * functions' score_fp32 mode, which rounds the values that decide P's and
- * dS's codes to fp32: those results decide integer codes (E8M0 scales, E4M3
- * payloads), and such decisions are taken in the same precision on both
- * sides.  With score_fp32 = 0 the attention functions are the plain fp64
- * definitions that the pins check.
+ * fp32 operation order that the fused kernel documents (there the fp32 result
+ * y decides every code, and the pages fix no other precision for it).  The
+ * attention functions are the plain fp64 definitions of the method.
  *
  * Sources (each function cites the passage it follows):
  *  [MX]  "Low-Precision FlashAttention-4: End-to-End Block-Scaled Attention on
@@ -243,36 +240,8 @@ static void qdq_block(double* v, int64_t n, int64_t vs) {
     v[i * vs] = mxo_e4m3_decode(mxo_e4m3_encode(ldexp(v[i * vs], -X))) * ldexp(1.0, X);
 }
 
-/* 2^x; with fp32 set, the argument is the fp32 difference of fp32 operands
- * (callers pass fp32-representable values) and the result is rounded to fp32,
- * the precision in which the kernel takes its quantization decisions. */
-static double exp2_prec(double x, int fp32) {
-  if (!fp32) return exp2(x);
-  volatile float xf = (float)x;
-  volatile float r = (float)exp2((double)xf);
-  return (double)r;
-}
-
 static double flush_fp32_subnormal(double p) {
   return p < ldexp(1.0, -126) ? 0.0 : p;
-}
-
-/* Quantize-dequantize one 32-key block of P in the kernel's fp32 steps: the
- * shared exponent X comes from the block maximum of p (the unscaled fp32
- * P~), and each element enters E4M3 as fl(2^fma(S, sl2, -fl(m + X))), which
- * is P~ * 2^-X computed with one rounding of the exponent argument. */
-static void qdq_block_fp32(double* p, const float* s32, float m, float sl2f) {
-  double amax = 0.0;
-  for (int i = 0; i < 32; i++)
-    if (p[i] > amax) amax = p[i];
-  int X = (int)mxo_e8m0_from_amax(amax) - 127;
-  volatile float mX = m + (float)X;
-  for (int i = 0; i < 32; i++) {
-    volatile float arg = fmaf(s32[i], sl2f, -mX);
-    volatile float pq = (float)exp2((double)arg);
-    double v = flush_fp32_subnormal((double)pq);
-    p[i] = mxo_e4m3_decode(mxo_e4m3_encode(v)) * ldexp(1.0, X);
-  }
 }
 
 /* ------------------------------------------------------------------ */
@@ -290,23 +259,16 @@ static void qdq_block_fp32(double* p, const float* s32, float m, float sl2f) {
  *   (lazy_thr = 0: exact rescale at every increase)
  *   O, l *= 2^(m_old - m);  P~ = 2^(s' - m);  l += sum P~ (unquantized)
  *   P~ quantized per 32-key block of the tile (when quant_p), then O += P^ V.
- * End: O /= l;  lse = (m + log2 l) * ln 2 (natural log).
+ * End: O /= l;  lse = (m + log2 l) * ln 2 (natural log); with no visible key
+ * (an empty key sequence) O = 0 and lse = -inf.
  * causal masks key index > query index within a sequence (equal lengths).
- * lse layout: lse[head][query token].
- * score_fp32 = 0 is the fp64 definition.  score_fp32 = 1 takes the values
- * that decide quantization codes in fp32, the kernel's precision: S rounded
- * to fp32 (the MMA accumulator), s' = fl(S * fl(scale * log2 e)), the running
- * maximum test in fp32, P~ = fl(2^fl(s' - m)) for the row sum and the block
- * maxima, and, for each 32-key block with shared exponent X taken from its
- * maximum, the value put on the E4M3 scale as fl(2^fma(S, fl(scale * log2 e),
- * -fl(m + X))) -- one fused multiply-add, no separate scaling multiply. */
+ * lse layout: lse[head][query token]. */
 void mxo_attn_fwd(const double* q, const double* k, const double* v,
                   const int32_t* cu_q, const int32_t* cu_k, int nseq, int H,
                   int D, double scale, int causal, int quant_p, int tile_n,
-                  double lazy_thr, double* o, double* lse, int64_t total_q, int score_fp32) {
+                  double lazy_thr, double* o, double* lse, int64_t total_q) {
   const double log2e = 1.4426950408889634074;
   const double ln2 = 0.69314718055994530942;
-  const float sl2f = (float)scale * 1.4426950408889634f;
   /* rows (query token, head) are independent: one parallel loop over them */
   int32_t* seq_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1));
   for (int g = 0; g < nseq; g++)
@@ -314,7 +276,6 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
 #pragma omp parallel
   {
     double* sp = (double*)malloc(sizeof(double) * (size_t)tile_n);
-    float* s32 = (float*)malloc(sizeof(float) * (size_t)tile_n);
     double* acc = (double*)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 16)
     for (int64_t w = 0; w < total_q * H; w++) {
@@ -337,50 +298,38 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
               const double* kj = k + ((k0 + t0 + j) * H + h) * D;
               double s = 0.0;
               for (int d = 0; d < D; d++) s += qi[d] * kj[d];
-              if (score_fp32) { /* S, s' rounded to fp32 like the MMA and kernel */
-                s32[j] = (float)s;
-                volatile float t = s32[j] * sl2f;
-                sp[j] = t;
-              } else {
-                sp[j] = s * scale * log2e;
-              }
+              sp[j] = s * scale * log2e;
               if (sp[j] > mt) mt = sp[j];
             } else {
               sp[j] = -INFINITY;
-              s32[j] = -INFINITY;
             }
           }
           double mn = mt > m ? mt : m;
-          double growth = score_fp32 ? (double)((float)mn - (float)m) : mn - m;
-          double mu = (m == -INFINITY || growth > lazy_thr) ? mn : m;
-          double alpha = (m == -INFINITY) ? 0.0 : exp2_prec(m - mu, score_fp32);
+          double mu = (m == -INFINITY || mn - m > lazy_thr) ? mn : m;
+          double alpha = (m == -INFINITY) ? 0.0 : exp2(m - mu);
           for (int d = 0; d < D; d++) acc[d] *= alpha;
           l *= alpha;
           m = mu;
           for (int64_t j = 0; j < tile_n; j++) {
-            sp[j] = sp[j] == -INFINITY ? 0.0 : flush_fp32_subnormal(exp2_prec(sp[j] - m, score_fp32));
+            sp[j] = sp[j] == -INFINITY ? 0.0 : flush_fp32_subnormal(exp2(sp[j] - m));
             l += sp[j];
           }
           if (quant_p)
-            for (int64_t b = 0; b < tile_n; b += 32) {
-              if (score_fp32)
-                qdq_block_fp32(sp + b, s32 + b, (float)m, sl2f);
-              else
-                qdq_block(sp + b, 32, 1);
-            }
+            for (int64_t b = 0; b < tile_n; b += 32) qdq_block(sp + b, 32, 1);
           for (int64_t j = 0; j < nt; j++) {
             if (sp[j] == 0.0) continue;
             const double* vj = v + ((k0 + t0 + j) * H + h) * D;
             for (int d = 0; d < D; d++) acc[d] += sp[j] * vj[d];
           }
         }
+        /* a query with no key to attend to (an empty key sequence): the
+         * softmax sum is empty, so O = 0 and lse = log 0 = -inf */
         double* oi = o + ((q0 + i) * H + h) * D;
-        for (int d = 0; d < D; d++) oi[d] = acc[d] / l;
-        lse[(int64_t)h * total_q + q0 + i] = (m + log2(l)) * ln2;
+        for (int d = 0; d < D; d++) oi[d] = l > 0.0 ? acc[d] / l : 0.0;
+        lse[(int64_t)h * total_q + q0 + i] = l > 0.0 ? (m + log2(l)) * ln2 : -INFINITY;
       }
     }
     free(sp);
-    free(s32);
     free(acc);
   }
   free(seq_of);
@@ -404,17 +353,13 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  *   (blocks anchored at the sequence start in both dimensions)
  *   dV_j = sum_i P^_ij dO_i;  dK_j = scale sum_i dS^_ij q_i;
  *   dQ_i = scale sum_j dS^_ij k_j.
- * score_fp32 = 1: S, dP, Delta rounded to fp32 and
- *   P = fl(2^min(fma(S, fl(scale * log2 e), -fl(lse * log2 e)), 0)) (one
- *   rounding of the exponent argument), dS = fl(P * fl(dP - Delta)): the fp32 steps of a
- *   kernel that evaluates the exponent with a fused multiply-add. */
+ */
 void mxo_attn_bwd(const double* q, const double* k, const double* v,
                   const double* dO, const double* o_bf, const double* do_bf,
                   const double* lse, const int32_t* cu_q, const int32_t* cu_k,
                   int nseq, int H, int D, double scale, int causal, int quant_p,
                   int quant_ds, double* dq, double* dk, double* dv,
-                  int64_t total_q, int score_fp32) {
-  const float sl2f = (float)scale * 1.4426950408889634f;
+                  int64_t total_q) {
   /* heads in turn; inside a head, independent rows / columns / blocks run in
    * parallel (every element keeps its own summation order) */
   for (int g = 0; g < nseq; g++) {
@@ -440,20 +385,9 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
             s += qi[d] * kj[d];
             dp += doi[d] * vj[d];
           }
-          if (score_fp32) { /* fp32 S, dP (MMA outputs) and fp32 elementwise steps */
-            volatile float l2 = (float)li * 1.4426950408889634f;
-            volatile float arg = fminf(fmaf((float)s, sl2f, -l2), 0.0f);
-            volatile float pf = (float)exp2((double)arg);
-            double p = flush_fp32_subnormal((double)pf);
-            volatile float diff = (float)dp - (float)delta;
-            volatile float dsf = (float)p * diff;
-            P[i * lk + j] = p;
-            dS[i * lk + j] = dsf;
-          } else {
-            double p = flush_fp32_subnormal(exp(fmin(s * scale - li, 0.0)));
-            P[i * lk + j] = p;
-            dS[i * lk + j] = p * (dp - delta);
-          }
+          double p = flush_fp32_subnormal(exp(fmin(s * scale - li, 0.0)));
+          P[i * lk + j] = p;
+          dS[i * lk + j] = p * (dp - delta);
         }
       }
       if (quant_p) /* 1x32 along queries, for every key column */

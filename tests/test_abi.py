@@ -75,6 +75,33 @@ def test_quantize_argument_checks(lib):
     assert q(0x1000, 256, 2, 128, 0, None, 1, 256, 0, ref(o), None) == 1     # packed w/o tiles
 
 
+def test_sf_unpack_argument_checks(lib):
+    u = lib.mxfa_sf_unpack
+    assert u(None, 256, 2, 128, 0, None, 1, 256, 2, 0x2000, None) == 1      # null packed
+    assert u(0x3000, 256, 2, 128, 0, None, 1, 256, 2, None, None) == 1      # null compact
+    assert u(0x3000, 256, 2, 64, 0, None, 1, 256, 2, 0x2000, None) == 2     # D != 128
+    assert u(0x3000, 256, 2, 128, 5, None, 1, 256, 2, 0x2000, None) == 1    # bad block kind
+    assert u(0x3000, 256, 2, 128, 0, None, 1, 256, 0, 0x2000, None) == 1    # no packed tiles
+    assert u(0x3000, 255, 2, 128, 0, None, 1, 256, 2, 0x2000, None) == 1    # tokens != nseq*len
+
+
+def test_noalloc_argument_checks(lib):
+    # the no-allocation backward validates like mxfa_bwd before it looks at
+    # the size of its scratch array or touches a device
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    m = mxfa.MxIn(0x1000, 0x2000)
+    bad = mxfa.MxIn(0x1000, 0x2004)
+    r = ctypes.byref
+    n = lib.mxfa_bwd_noalloc
+    args = lambda qm, D, o, B=2, S=8192: (r(qm), r(m), r(m), r(m), o, 0x5000, 0x6000, B, S, 16, D,
+                                           0.088, 1, 0, 1.0, 0x7000, 0x8000, 0x9000, None)
+    assert n(*args(m, 64, 0x4000)) == 2            # D != 128 before the size check
+    assert n(*args(m, 128, None)) == 1             # null O
+    assert n(*args(bad, 128, 0x4000)) == 3         # misaligned scales
+    assert n(*args(m, 128, 0x4000)) == 4           # ~129 MiB of workspace: beyond the array
+    assert n(*args(m, 128, 0x4000, B=0)) == 1      # empty batch
+
+
 def test_attention_argument_checks(lib):
     from mxfp8_block_scaled_fa_gb300 import mxfa
     m = mxfa.MxIn(0x1000, 0x2000)
@@ -142,7 +169,7 @@ def test_mxfp8_output_argument_checks(lib):
 def test_package_exposes_the_public_api():
     # the package forwards the binding's public names without loading the library
     import mxfp8_block_scaled_fa_gb300 as pkg
-    for n in ("Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ", "quantize", "sf_pack",
+    for n in ("Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ", "quantize", "sf_pack", "sf_unpack",
               "attention_fwd", "attention_bwd", "rmsnorm_quant", "device_status", "lib",
               "MxfaError", "mxfa_fwd", "mxfa_bwd", "mxfa_fwd_mxo", "mxfa_bwd_mxg"):
         assert getattr(pkg, n) is not None, n

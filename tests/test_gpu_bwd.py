@@ -46,14 +46,18 @@ def gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse_dev, sq, sk, scale, causal, dq_mode
 
 
 def oracle_fwd_out(qf, kf, vf, cu_q, cu_k, scale, causal):
-    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, scale, causal, True, 128, THR, True)
+    """The oracle forward's O and lse as the backward's interface carries them
+    (O in bf16, lse in fp32): (O bits, O as float64, lse as float64).  Both
+    backward implementations then receive exactly the same input values."""
+    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, scale, causal, True, 128, THR)
     o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
-    return o_bits, inputs.bf16_bits_to_f32(o_bits).astype(np.float64), lse
+    return o_bits, inputs.bf16_bits_to_f32(o_bits).astype(np.float64), lse.astype(np.float32).astype(np.float64)
 
 
 def check(got, ref, tag=""):
-    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
-        e = rel_fro(g.reshape(r.shape), r)
+    errs = [rel_fro(g.reshape(r.shape), r) for g, r in zip(got, ref)]
+    print(f"[bwd parity] {tag} rel-Fro dQ {errs[0]:.3e} dK {errs[1]:.3e} dV {errs[2]:.3e}")
+    for name, e in zip(("dQ", "dK", "dV"), errs):
         assert e <= G_REL, f"{tag} {name} rel {e}"
 
 
@@ -78,7 +82,7 @@ def test_bwd_dense(mx, B, H, S, causal, dq_mode, dq_static):
     seqs = mx.Seqs.dense(B, S)
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse_dense.copy()).cuda(), seqs,
                   seqs, scale, causal, dq_mode, dq_static)
-    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lse, cu, cu, scale, causal, True, True)
+    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lse, cu, cu, scale, causal, True)
     check(got, ref)
 
 
@@ -96,7 +100,33 @@ def test_bwd_varlen(mx, causal):
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse.astype(np.float32)).cuda(),
                   sq, sk, scale, causal)
     ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale,
-                            causal, True, True)
+                            causal, True)
+    check(got, ref)
+
+
+def test_bwd_varlen_empty_sequences(mx):
+    # keys of a sequence with no queries get dK = dV = 0; queries of a
+    # sequence with no keys get dQ = 0 (their O is 0 and lse -inf)
+    import torch
+    H, D = 2, 128
+    lq = [0, 70, 5, 130]
+    lk = [40, 70, 0, 130]
+    qb, kb, vb, dob, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=33)
+    scale = 1 / math.sqrt(D)
+    o_bits, o_bf, lse = oracle_fwd_out(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, False)
+    sq = mx.Seqs.varlen(lq, "cuda")
+    sk = mx.Seqs.varlen(lk, "cuda")
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse.astype(np.float32)).cuda(),
+                  sq, sk, scale, False)
+    ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale,
+                            False, True)
+    for g, r in zip(got, ref):
+        assert np.isfinite(g).all()
+    no_key = np.repeat(np.asarray(lk) == 0, lq)
+    no_query = np.repeat(np.asarray(lq) == 0, lk)
+    assert np.all(got[0].reshape(-1, H, D)[no_key] == 0)
+    assert np.all(got[1].reshape(-1, H, D)[no_query] == 0)
+    assert np.all(got[2].reshape(-1, H, D)[no_query] == 0)
     check(got, ref)
 
 
@@ -120,8 +150,16 @@ def test_fwd_then_bwd_on_gpu(mx):
     torch.cuda.synchronize()
     assert mx.device_status() == 0
     f = lambda b: f64(b).reshape(B * S, H, D)
-    o_bits, o_bf, lo = oracle_fwd_out(f(qb), f(kb), f(vb), None, None, scale, True)
-    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lo, None, None, scale, True, True, True)
+    # the forward against the oracle's forward, the backward against the
+    # oracle's backward on the same O (bf16) and lse (fp32) that the GPU
+    # backward received from the GPU forward
+    from tests.test_gpu_fwd import check as fwd_check
+    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, scale, True, True, 128, THR)
+    o_gpu = host(o.float()).astype(np.float64)
+    lse_gpu = host(lse).reshape(H, B * S).astype(np.float64)
+    fwd_check(o_gpu, lse_gpu, oo, lo)
+    ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_gpu, lse_gpu, None, None, scale, True,
+                            True)
     check([host(t.float()).astype(np.float64) for t in (dq, dk, dv)], ref, "chained")
 
 
@@ -144,12 +182,12 @@ def test_bwd_llm_config_sampled_head(mx):
     torch.cuda.synchronize()
     o_bits = host(o.view(torch.int16)).view(np.uint16).reshape(B, S, H, D).copy()
     o_bits[b, :, h, :] = o_h_bits.reshape(S, D)
-    lse_h32 = torch.from_numpy(lse_h.reshape(S).astype(np.float32)).cuda()
+    lse_h32 = torch.from_numpy(lse_h.reshape(S).astype(np.float32)).cuda()  # already fp32 values
     lse.view(B, H, S)[b, h].copy_(lse_h32)
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, scale, True)
     got = [g.reshape(B, S, H, D)[b, :, h:h + 1, :] for g in got]
     ref = oracle.method_bwd(sl(qb), sl(kb), sl(vb), sl(dob), o_h_bf, lse_h, None, None, scale, True,
-                            True, True)
+                            True)
     check(got, ref, "llm")
 
 
@@ -205,5 +243,5 @@ def test_bwd_mxfp8_gradients(mx, varlen, dq_mode):
         np.testing.assert_array_equal(comp, s_ref, err_msg=name)
         assert np.all(pad == 0x7F), name
     ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale, causal,
-                            True, True)
+                            True)
     check([host(t.float()).astype(np.float64) for t in (dq, dk, dv)], ref, "mxfp8 grads")

@@ -29,24 +29,29 @@ SCALE = 1 / math.sqrt(D)
 
 
 def oracle_fwd_full(qf, kf, vf, cu_q, cu_k, causal):
-    """The oracle forward -> (O float64, lse, O as bf16 bits, O bf16 as float64)."""
-    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, SCALE, causal, True, 128, THR, True)
+    """The oracle forward -> (O float64, lse float64, O as bf16 bits, O bf16 as
+    float64, lse rounded to fp32 as float64): the last two are O and lse as the
+    backward's interface carries them, the same values on both sides."""
+    o, lse = oracle.method_fwd(qf, kf, vf, cu_q, cu_k, SCALE, causal, True, 128, THR)
     o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
-    return o, lse, o_bits, f64(o_bits)
+    return o, lse, o_bits, f64(o_bits), lse.astype(np.float32).astype(np.float64)
 
 
-def fwd_check_envelope(o, lse, qd, kd, vd, causal, oo, lo, eps=1e-7, seeds=(0, 1, 2)):
+def fwd_check_envelope(o, lse, qd, kd, vd, causal, oo, lo, eps=2.0 ** -21, seeds=(0, 1, 2)):
     """fwd_check, where every P code is unique, and an envelope elsewhere.
 
     Rows dominated by a few keys (the outlier recipe's scores reach 1e5) put
-    single P elements within an fp32 ulp of an E4M3 rounding boundary; the
-    tensor core's fp32 summation order is unspecified, so such a row has more
-    than one correct O.  The oracle reruns with K (dequantized) scaled by
-    1 + eps * N(0,1) per element, an ulp-sized change of every score: rows
-    whose O moves by more than 1e-3 are the non-unique ones, must be rare (under
-    1% of rows), and are held to the bar plus the spread of those reruns; all
-    other rows and the whole-tensor relative Frobenius are held to the plain bar.
-    The lse bar adds the fp32 summation bound of the row's scores.
+    single P elements within the fp32 accuracy of a score from an E4M3
+    rounding boundary.  Softmax runs in FP32 (the pages), and an fp32 score
+    summed from 128 products may differ from the exact one by up to
+    8 * 2^-24 * sum_d |q_d k_d| in an unspecified tensor-core order, so such a
+    row has more than one correct O.  The fp64 oracle reruns with K
+    (dequantized) scaled by 1 + 2^-21 N(0,1) per element, which moves each
+    score by about that bound: rows whose O moves by more than 1e-3 are the
+    non-unique ones, must be rare (under 2% of rows), and are held to the bar
+    plus the spread of those reruns; all other rows and the whole-tensor
+    relative Frobenius are held to the plain bar.  The lse bar adds the same
+    fp32 summation bound.
     """
     from tests.test_gpu_fwd import O_ABS, O_REL, _spacing
     from tests.helpers import rel_fro
@@ -54,10 +59,12 @@ def fwd_check_envelope(o, lse, qd, kd, vd, causal, oo, lo, eps=1e-7, seeds=(0, 1
     for sd in seeds:
         rng = np.random.default_rng(sd)
         kp = kd * (1 + eps * rng.standard_normal(kd.shape))
-        ov, _ = oracle.attn_fwd(qd, kp, vd, None, None, SCALE, causal, True, 128, THR, True)
+        ov, _ = oracle.attn_fwd(qd, kp, vd, None, None, SCALE, causal, True, 128, THR)
         spread = np.maximum(spread, np.abs(ov - oo))
     unstable = spread.max(axis=(1, 2)) > 1e-3
-    assert unstable.sum() <= 0.01 * len(unstable), unstable.sum()
+    print(f"[fwd envelope] unstable rows {int(unstable.sum())} of {len(unstable)}; "
+          f"O rel-Fro {rel_fro(o, oo):.3e}; max |O - O_oracle| {np.max(np.abs(o - oo)):.3e}")
+    assert unstable.sum() <= 0.02 * len(unstable), unstable.sum()
     assert rel_fro(o, oo) <= O_REL, rel_fro(o, oo)
     excess = np.abs(o - oo) - 0.5 * _spacing(oo, 7) - np.where(unstable[:, None, None], spread, 0)
     assert excess.max() <= O_ABS, excess.max()
@@ -95,7 +102,7 @@ def test_bwd_outliers_small(mx, outliers_v, dq_mode, dq_static):
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse_dev.cuda(), seqs, seqs, SCALE, False, dq_mode,
                   dq_static)
     ref = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lse, None, None, SCALE, False,
-                            True, True)
+                            True)
     grad_check(got, ref, "outliers")
 
 
@@ -120,22 +127,22 @@ def test_outlier_config_sampled_heads(mx):
     sl = lambda x, b, h: f64(x[b, :, h:h + 1, :])
     fwd_ref = {}
     for b, h in sampled:
-        oo, lo, ob, obf = oracle_fwd_full(sl(qb, b, h), sl(kb, b, h), sl(vb, b, h), None, None,
-                                          False)
+        oo, lo, ob, obf, lo32 = oracle_fwd_full(sl(qb, b, h), sl(kb, b, h), sl(vb, b, h), None,
+                                                None, False)
         fwd_check_envelope(o_host[b, :, h:h + 1, :], lse_host[b, h:h + 1, :],
                            oracle.qdq(sl(qb, b, h), 0), oracle.qdq(sl(kb, b, h), 0),
                            oracle.qdq(sl(vb, b, h), 1), False, oo, lo)
-        fwd_ref[b, h] = (obf, lo)
+        fwd_ref[b, h] = (obf, lo32)
         # the backward of this head runs from the oracle's O and lse
         o_bits[b, :, h, :] = ob.reshape(S, D)
-        lse.view(B, H, S)[b, h].copy_(torch.from_numpy(lo.reshape(S).astype(np.float32)).cuda())
+        lse.view(B, H, S)[b, h].copy_(torch.from_numpy(lo32.reshape(S).astype(np.float32)).cuda())
     del o
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, SCALE, False)
     got = [g.reshape(B, S, H, D) for g in got]
     for b, h in sampled:
         obf, lo = fwd_ref[b, h]
         ref = oracle.method_bwd(sl(qb, b, h), sl(kb, b, h), sl(vb, b, h), sl(dob, b, h), obf, lo,
-                                None, None, SCALE, False, True, True)
+                                None, None, SCALE, False, True)
         grad_check([g[b, :, h:h + 1, :] for g in got], ref, f"outlier b{b} h{h}")
 
 
@@ -157,18 +164,19 @@ def test_jagged_config_sampled_sequences(mx):
     fwd_ref = {}
     for i in sorted(picks):
         rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
-        oo, lo, ob, obf = oracle_fwd_full(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), None, None, False)
+        oo, lo, ob, obf, lo32 = oracle_fwd_full(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), None, None,
+                                                False)
         fwd_check(o[rq], lse[:, rq], oo, lo)
-        fwd_ref[i] = (obf, lo)
+        fwd_ref[i] = (obf, lo32)
         o_bits[rq] = ob
-        lse_all[:, rq] = lo
+        lse_all[:, rq] = lo32
     got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse_all.astype(np.float32)).cuda(),
                   sq, sk, SCALE, False)
     for i in sorted(picks):
         rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
         obf, lo = fwd_ref[i]
         ref = oracle.method_bwd(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), f64(dob[rq]), obf, lo, None,
-                                None, SCALE, False, True, True)
+                                None, SCALE, False, True)
         grad_check([got[0][rq], got[1][rk], got[2][rk]], ref, f"jagged seq {i}")
 
 
@@ -217,14 +225,15 @@ def test_fused_chain_small(mx):
         np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
     cu = np.arange(0, T + S, S, dtype=np.int32)
     oo, lo = oracle.attn_fwd(deq["row"], deq["row"], deq["col"], cu, cu, SCALE, True, True, 128,
-                             THR, True)
+                             THR)
     o_gpu = host(o.float()).astype(np.float64)
-    lse_gpu = host(lse).reshape(B, H, S).transpose(1, 0, 2).reshape(H, T)
+    lse_gpu = host(lse).reshape(B, H, S).transpose(1, 0, 2).reshape(H, T).astype(np.float64)
     fwd_check(o_gpu, lse_gpu, oo, lo)
-    o_bf = f64(inputs.f32_to_bf16_bits(oo.astype(np.float32)))
+    # the backward against the oracle's backward on the O (bf16) and lse
+    # (fp32) that the GPU backward received
     dof = f64(dob).reshape(T, H, D)
-    ref_g = oracle.attn_bwd(deq["sq"], deq["sq"], deq["row"], oracle.qdq(dof, 2, cu), o_bf, dof, lo,
-                            cu, cu, SCALE, True, True, True, True)
+    ref_g = oracle.attn_bwd(deq["sq"], deq["sq"], deq["row"], oracle.qdq(dof, 2, cu), o_gpu, dof,
+                            lse_gpu, cu, cu, SCALE, True, True, True)
     grad_check([host(t.float()).astype(np.float64) for t in grads], ref_g, "fused chain")
 
 
@@ -241,12 +250,12 @@ def test_fused_config_sampled_head(mx):
         np.testing.assert_array_equal(host(res[name].data), ref[name][0], err_msg=name)
     hs = slice(h, h + 1)
     q, vc, qs = deq["row"][:, hs], deq["col"][:, hs], deq["sq"][:, hs]
-    oo, lo = oracle.attn_fwd(q, q, vc, None, None, SCALE, True, True, 128, THR, True)
+    oo, lo = oracle.attn_fwd(q, q, vc, None, None, SCALE, True, True, 128, THR)
     o_gpu = host(o.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs]
-    fwd_check(o_gpu, host(lse).reshape(B, H, S)[b, hs], oo, lo)
-    o_bf = f64(inputs.f32_to_bf16_bits(oo.astype(np.float32)))
+    lse_gpu = host(lse).reshape(B, H, S)[b, hs].astype(np.float64)
+    fwd_check(o_gpu, lse_gpu, oo, lo)
     dof = f64(dob[b, :, hs, :])
-    ref_g = oracle.attn_bwd(qs, qs, q, oracle.qdq(dof, 2), o_bf, dof, lo, None, None, SCALE, True,
+    ref_g = oracle.attn_bwd(qs, qs, q, oracle.qdq(dof, 2), o_gpu, dof, lse_gpu, None, None, SCALE,
                             True, True, True)
     got = [host(t.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs] for t in grads]
     grad_check(got, ref_g, "fused config")
@@ -275,8 +284,8 @@ def test_tiny_error_vs_unquantized_attention(mx):
     f = lambda b: f64(b).reshape(B * S, H, D)
     o_x, lse_x = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, SCALE, False, False)
     g_x = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_x, lse_x, None, None, SCALE, False, False)
-    oo, lo, _, o_bf = oracle_fwd_full(f(qb), f(kb), f(vb), None, None, False)
-    g_m = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lo, None, None, SCALE, False, True, True)
+    oo, lo, _, o_bf, lo32 = oracle_fwd_full(f(qb), f(kb), f(vb), None, None, False)
+    g_m = oracle.method_bwd(f(qb), f(kb), f(vb), f(dob), o_bf, lo32, None, None, SCALE, False, True)
     got = [host(t.float()).astype(np.float64) for t in (o,) + tuple(grads)]
     for name, g, m, x in zip(("O", "dQ", "dK", "dV"), got, (oo,) + tuple(g_m), (o_x,) + tuple(g_x)):
         s_gpu, s_method = sqnr_db(g, x), sqnr_db(m, x)

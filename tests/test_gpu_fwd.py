@@ -2,10 +2,9 @@
 
 Bar: O relative Frobenius <= 1e-2 and max-abs <= 3e-2; LSE max-abs <= 1e-4;
 each max-abs bar plus the rounding of the output format (bf16 O, fp32 lse).
-The oracle runs the method with the kernel's declared schedule: 128-key
-tiles in ascending order, running max moved when it grows by more than 8
-(log2 units), and takes the values that decide P's quantization codes in
-fp32, the kernel's precision.
+The oracle is the method's fp64 definition over the dequantized MXFP8
+operands, with the kernel's declared schedule: 128-key tiles in ascending
+order, running max moved when it grows by more than 8 (log2 units).
 """
 import math
 
@@ -52,6 +51,8 @@ def check(o, lse, oo, lo):
     # O is returned in bf16 and lse in fp32: the max-abs bars add the output
     # format's own rounding (half a bf16 spacing of O, four fp32 spacings of
     # lse), which only matters where |O| > 8 or |lse| > 100
+    print(f"[fwd parity] O rel-Fro {rel_fro(o, oo):.3e} max-abs {max_abs(o, oo):.3e} "
+          f"lse max-abs {max_abs(lse, lo):.3e}")
     assert rel_fro(o, oo) <= O_REL, rel_fro(o, oo)
     excess = np.abs(o - oo) - 0.5 * _spacing(oo, 7)
     assert excess.max() <= O_ABS, (max_abs(o, oo), excess.max())
@@ -76,7 +77,7 @@ def test_fwd_dense(mx, B, H, S, causal):
     o, lse = gpu_fwd(mx, qb, kb, vb, seqs, seqs, scale, causal)
     cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
     f = lambda b: f64(b).reshape(B * S, H, D)
-    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), cu, cu, scale, causal, True, 128, THR, True)
+    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), cu, cu, scale, causal, True, 128, THR)
     check(o.reshape(B * S, H, D), lse.reshape(B, H, S).transpose(1, 0, 2).reshape(H, B * S), oo, lo)
 
 
@@ -90,8 +91,28 @@ def test_fwd_varlen(mx, causal):
     sk = mx.Seqs.varlen(lk, "cuda")
     scale = 1 / math.sqrt(D)
     o, lse = gpu_fwd(mx, qb, kb, vb, sq, sk, scale, causal)
-    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal, True, 128, THR, True)
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal, True, 128, THR)
     check(o, lse, oo, lo)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_varlen_empty_sequences(mx, causal):
+    # zero-length query and key sequences: a query whose key sequence is empty
+    # gets O = 0 and lse = -inf; an empty query sequence writes nothing
+    H, D = 2, 128
+    lq = [0, 70, 5, 0, 130]
+    lk = [0, 70, 0, 9, 130] if not causal else [0, 70, 0, 0, 130]
+    qb, kb, vb, _, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=23)
+    sq = mx.Seqs.varlen(lq, "cuda")
+    sk = mx.Seqs.varlen(lk, "cuda")
+    scale = 1 / math.sqrt(D)
+    o, lse = gpu_fwd(mx, qb, kb, vb, sq, sk, scale, causal)
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal, True, 128, THR)
+    empty = np.repeat(np.asarray(lk) == 0, lq)       # query tokens with no key
+    assert empty.sum() == 5
+    assert np.all(o[empty] == 0) and np.all(oo[empty] == 0)
+    assert np.all(np.isneginf(lse[:, empty])) and np.all(np.isneginf(lo[:, empty]))
+    check(o[~empty], lse[:, ~empty], oo[~empty], lo[:, ~empty])
 
 
 @pytest.mark.parametrize("outliers_v", [False, True])
@@ -104,7 +125,7 @@ def test_fwd_outliers_small(mx, outliers_v):
     scale = 1 / math.sqrt(D)
     o, lse = gpu_fwd(mx, qb, kb, vb, seqs, seqs, scale, False)
     f = lambda b: f64(b).reshape(B * S, H, D)
-    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, scale, False, True, 128, THR, True)
+    oo, lo = oracle.method_fwd(f(qb), f(kb), f(vb), None, None, scale, False, True, 128, THR)
     check(o.reshape(B * S, H, D), lse.reshape(H, S), oo, lo)
 
 
@@ -120,7 +141,7 @@ def test_fwd_llm_config_sampled_heads(mx):
     lse = lse.reshape(B, H, S)
     for b, h in ((0, 3), (1, 14)):
         sl = lambda x: f64(x[b, :, h:h + 1, :])
-        oo, lo = oracle.method_fwd(sl(qb), sl(kb), sl(vb), None, None, scale, True, True, 128, THR, True)
+        oo, lo = oracle.method_fwd(sl(qb), sl(kb), sl(vb), None, None, scale, True, True, 128, THR)
         check(o[b, :, h:h + 1, :], lse[b, h:h + 1, :], oo, lo)
 
 
@@ -161,7 +182,7 @@ def test_fwd_mxfp8_output(mx, varlen):
     comp, pad = unpack_packed(host(omx.sf_packed), mx.ROW, lens, H)
     np.testing.assert_array_equal(comp, s_ref)
     assert np.all(pad == 0x7F)
-    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu, cu, scale, True, True, 128, THR, True)
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu, cu, scale, True, True, 128, THR)
     lse_h = host(lse)
     if not varlen:  # dense lse is [B][H][S]; the oracle's is [H][tokens]
         lse_h = lse_h.reshape(len(lens), H, lens[0]).transpose(1, 0, 2).reshape(H, tokens)

@@ -42,8 +42,12 @@ def _check_quant(mx, bits3, lens, H, blk):
     np.testing.assert_array_equal(comp, s_ref)
     assert np.all(pad == 0x7F)
     packed2 = mx.sf_pack(m.sf_compact, blk, seqs, H)
+    # the C-ABI round trip of the packed layout: unpack gives the compact scales back
+    comp2 = mx.sf_unpack(m.sf_packed, blk, seqs, H)
     torch.cuda.synchronize()
+    assert mx.device_status() == 0
     np.testing.assert_array_equal(host(packed2), host(m.sf_packed))
+    np.testing.assert_array_equal(host(comp2), s_ref)
 
 
 @pytest.mark.parametrize("blk,name", MODES)
@@ -57,6 +61,14 @@ def test_quantize_ragged_varlen(mx, blk, name):
     lens = [5, 130, 64, 33, 1, 257]
     q, _, _, _, _, _ = inputs.varlen_attn(lens, lens, 3, 128, seed=5)
     _check_quant(mx, q, lens, 3, blk)
+
+
+@pytest.mark.parametrize("blk,name", MODES)
+def test_quantize_varlen_with_empty_sequences(mx, blk, name):
+    # zero-length sequences own no payload row, no scale row and no packed tile
+    lens = [0, 40, 0, 0, 129, 0]
+    q, _, _, _, _, _ = inputs.varlen_attn(lens, lens, 2, 128, seed=6)
+    _check_quant(mx, q, lens, 2, blk)
 
 
 @pytest.mark.parametrize("blk,name", MODES)

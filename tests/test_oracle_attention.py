@@ -129,6 +129,27 @@ def test_fwd_varlen_equals_per_sequence():
         np.testing.assert_array_equal(lse[:, sq], lg)
 
 
+def test_empty_key_sequence_gives_zero_output_and_neg_inf_lse():
+    # a query whose key sequence is empty attends to nothing: O = 0, lse = -inf
+    # (the empty softmax sum); the other sequences are unaffected, and the
+    # backward gives dQ = 0 for such queries and dK = dV = 0 for keys of a
+    # sequence without queries
+    H, D = 2, 32
+    lq, lk = [3, 0, 40], [0, 9, 33]
+    q, k, v, do, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, 17)
+    f = lambda b: inputs.bf16_bits_to_f32(b).astype(np.float64)
+    q, k, v, do = f(q), f(k), f(v), f(do)
+    o, lse = oracle.method_fwd(q, k, v, cu_q, cu_k, 0.2, False, True)
+    assert np.all(o[:3] == 0.0) and np.all(np.isneginf(lse[:, :3]))
+    og, lg = oracle.method_fwd(q[3:], k[9:], v[9:], None, None, 0.2, False, True)
+    np.testing.assert_array_equal(o[3:], og)
+    np.testing.assert_array_equal(lse[:, 3:], lg)
+    dq, dk, dv = oracle.method_bwd(q, k, v, do, o, lse, cu_q, cu_k, 0.2, False, True)
+    assert np.all(dq[:3] == 0.0)
+    assert np.all(dk[:9] == 0.0) and np.all(dv[:9] == 0.0)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
 # ---------------------------------------------------------------- backward
 def _loss_grads_fd(q, k, v, do, scale, causal, h=1e-6):
     def loss(q_, k_, v_):
@@ -240,70 +261,7 @@ def test_bwd_quantized_close_to_exact():
         assert 1e-3 < rel < 0.15
 
 
-# ----------------------------------------------- fp32 decision-precision mode
-def test_fp32_mode_rounds_scores_to_fp32():
-    # q.k0 = 2^24 + 1 and q.k1 = 2^24: fp64 keeps the difference of 1 (times
-    # tau * log2 e = 2 with tau = 2 ln 2, so P~ = (1/4, 1) -> O = 1/(1 + 1/4) * v1
-    # = 0.8 for v0 = 0, v1 = 1), fp32 scores round both to 2^24 (P~ = (1, 1) -> O = 0.5).
-    q = np.zeros((1, 1, 4)); q[0, 0, 0] = 2.0 ** 12
-    k = np.zeros((2, 1, 4)); k[0, 0, 0] = 2.0 ** 12; k[1, 0, 0] = 2.0 ** 12 + 2.0 ** -12
-    v = np.zeros((2, 1, 4)); v[1] = 1.0
-    cu = np.array([0, 1], np.int32); ck = np.array([0, 2], np.int32)
-    tau = 2 * math.log(2.0)
-    o64, _ = oracle.attn_fwd(q, k, v, cu, ck, tau, False, True, 128, 0.0, False)
-    o32, _ = oracle.attn_fwd(q, k, v, cu, ck, tau, False, True, 128, 0.0, True)
-    np.testing.assert_allclose(o64, 0.8, rtol=1e-12)
-    np.testing.assert_allclose(o32, 0.5, rtol=0)
-
-
-@pytest.mark.parametrize("causal", [False, True])
-def test_fp32_mode_close_to_definition(causal):
-    S, H, D = 300, 2, 64
-    q, k, v, do = (_rand((S, H, D), s) for s in (60, 61, 62, 63))
-    scale = 1 / math.sqrt(D)
-    o64, l64 = oracle.attn_fwd(q, k, v, None, None, scale, causal, False, 128, 8.0, False)
-    o32, l32 = oracle.attn_fwd(q, k, v, None, None, scale, causal, False, 128, 8.0, True)
-    np.testing.assert_allclose(o32, o64, rtol=0, atol=2e-6)
-    np.testing.assert_allclose(l32, l64, rtol=0, atol=2e-6)
-    g64 = oracle.attn_bwd(q, k, v, do, o64, do, l64, None, None, scale, causal, False, False, False)
-    g32 = oracle.attn_bwd(q, k, v, do, o64, do, l64, None, None, scale, causal, False, False, True)
-    for a, b in zip(g32, g64):
-        assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-5
-
-
-def _f32_with_product(target):
-    """An fp32 x with fl32(x * fl32(log2 e)) == target (searched near target / log2 e)."""
-    l2e = np.float32(1.4426950408889634)
-    x = np.float32(float(target) / float(l2e))
-    for step in range(64):
-        for y in (x, np.float32(x + step * np.spacing(x)), np.float32(x - step * np.spacing(x))):
-            if np.float32(y * l2e) == np.float32(target):
-                return float(y)
-    raise AssertionError("no fp32 input found")
-
-
-def test_fp32_mode_backward_exponent_rounded_once():
-    # One query, one key, D = 1: S = 4097, fl(scale * log2 e) = 1 + 2^-20 and
-    # fl(lse * log2 e) = 4097 + 2^-8 + 2^-11.  The exact argument S * c - l is
-    # 2^-20 - 2^-11 = -511 * 2^-20 (an fp32 number); rounding S * c to fp32
-    # first (ulp 2^-11 there, S * c -> 4097 + 2^-8) would give -2^-11.  With
-    # dO = 1 and no quantization, dV = P = fl32(2^(-511 * 2^-20)) for one
-    # rounding.
-    scale = _f32_with_product(1 + 2.0 ** -20)
-    lse = _f32_with_product(4097 + 2.0 ** -8 + 2.0 ** -11)
-    q = np.full((1, 1, 1), 4097.0)
-    k = np.ones((1, 1, 1))
-    v = np.zeros((1, 1, 1))
-    do = np.ones((1, 1, 1))
-    o = np.zeros((1, 1, 1))
-    lse_a = np.full((1, 1), lse)
-    dq, dk, dv = oracle.attn_bwd(q, k, v, do, o, do, lse_a, None, None, scale, False, False, False, True)
-    assert dv[0, 0, 0] == float(np.float32(2.0 ** (-511 * 2.0 ** -20)))
-    assert dv[0, 0, 0] != float(np.float32(2.0 ** (-(2.0 ** -11))))
-
-
-@pytest.mark.parametrize("fp32", [False, True])
-def test_backward_p_clamped_at_one(fp32):
+def test_backward_p_clamped_at_one():
     # One query, three keys, D = 1, scale 1: S = (2, 0.5, -1) with lse = 1
     # given (smaller than the first score, as a recompute from other operands
     # can make it).  Exact attention never has P > 1, so the first key takes
@@ -315,11 +273,10 @@ def test_backward_p_clamped_at_one(fp32):
     do = np.ones((1, 1, 1))
     o = np.zeros((1, 1, 1))
     lse = np.ones((1, 1))
-    _, _, dv = oracle.attn_bwd(q, k, v, do, o, do, lse, None, None, 1.0, False, False, False, fp32)
+    _, _, dv = oracle.attn_bwd(q, k, v, do, o, do, lse, None, None, 1.0, False, False, False)
     assert dv[0, 0, 0] == 1.0
-    tol = 1e-6 if fp32 else 1e-15
-    assert abs(dv[1, 0, 0] - math.exp(-0.5)) <= tol
-    assert abs(dv[2, 0, 0] - math.exp(-2.0)) <= tol
+    assert abs(dv[1, 0, 0] - math.exp(-0.5)) <= 1e-15
+    assert abs(dv[2, 0, 0] - math.exp(-2.0)) <= 1e-15
 
 
 def test_results_do_not_depend_on_thread_count():
@@ -331,8 +288,8 @@ def test_results_do_not_depend_on_thread_count():
     runs = []
     for n in (1, cores):
         oracle.set_num_threads(n)
-        o, lse = oracle.method_fwd(q, k, v, None, None, scale, True, True, 128, 8.0, True)
-        g = oracle.method_bwd(q, k, v, do, o, lse, None, None, scale, True, True, True)
+        o, lse = oracle.method_fwd(q, k, v, None, None, scale, True, True, 128, 8.0)
+        g = oracle.method_bwd(q, k, v, do, o, lse, None, None, scale, True, True)
         runs.append((o, lse) + tuple(g))
     oracle.set_num_threads(cores)
     for a, b in zip(*runs):
