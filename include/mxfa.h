@@ -98,6 +98,25 @@ typedef struct {
  * more than this many log2 units (O and l keep the stale maximum exactly). */
 #define MXFA_FWD_RESCALE_THRESHOLD 8.0f
 
+/* Options of the *_opts attention calls (the plain calls use the defaults).
+ *  rescale_threshold  forward only: the running row maximum moves when it
+ *          grows by more than this (log2 units, 0 <= t <= 8); 0 rescales at
+ *          every increase.  P~ = 2^(s' - m) then stays below 2^t.  Default
+ *          MXFA_FWD_RESCALE_THRESHOLD.
+ *  p_scale MXFA_P_SCALE_BLOCK (default): each 32-element block of P gets the
+ *          E8M0 scale of its own maximum (OCP rule).  MXFA_P_SCALE_CONST: one
+ *          constant scale for every block ([ITEMS] item 4: constant scaling
+ *          of softmax outputs, which lie in a known range): forward
+ *          2^(ceil(t) - 8), so the largest possible P~, 2^ceil(t), maps to
+ *          256 <= 448; backward 2^-8 (P <= 1 maps to <= 256).  Values below
+ *          2^-9 of the scale round to zero. */
+#define MXFA_P_SCALE_BLOCK 0
+#define MXFA_P_SCALE_CONST 1
+typedef struct {
+  float rescale_threshold;
+  int p_scale;
+} mxfa_attn_opts;
+
 const char* mxfa_status_string(mxfa_status s);
 int mxfa_version(void);
 
@@ -188,6 +207,19 @@ mxfa_status mxfa_varlen_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_m
                                 float softmax_scale, int causal, void* o, float* lse,
                                 const mxfa_mx_out* o_mx, mxfa_stream_t stream);
 
+/* mxfa_fwd_opts, mxfa_varlen_fwd_opts -- mxfa_fwd / mxfa_varlen_fwd with
+ * options (see mxfa_attn_opts; NULL = defaults).  A threshold outside
+ * [0, 8] or an unknown p_scale is MXFA_ERR_INVALID_ARG. */
+mxfa_status mxfa_fwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H,
+                          int D, float softmax_scale, int causal, const mxfa_attn_opts* opts,
+                          void* o, float* lse, mxfa_stream_t stream);
+mxfa_status mxfa_varlen_fwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                                 int max_seqlen_q, int max_seqlen_k, int64_t total_q,
+                                 int64_t total_k, int64_t ptiles_q, int64_t ptiles_k, int H, int D,
+                                 float softmax_scale, int causal, const mxfa_attn_opts* opts,
+                                 void* o, float* lse, mxfa_stream_t stream);
+
 /* Workspace of the backward pass for total_q query tokens in nseq sequences:
  * one 2560-byte record per (64-query tile, head) -- the tile's scale atoms,
  * lse * log2(e) and Delta = rowsum(dO * O) -- for at most
@@ -222,6 +254,24 @@ mxfa_status mxfa_varlen_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v
                             int64_t ptiles_q, int64_t ptiles_k, int H, int D, float softmax_scale,
                             int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
                             void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
+
+/* mxfa_bwd_opts, mxfa_varlen_bwd_opts -- mxfa_bwd / mxfa_varlen_bwd with
+ * options (see mxfa_attn_opts; NULL = defaults; the backward reads only
+ * p_scale, which selects the block or constant scale of its P^T). */
+mxfa_status mxfa_bwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                          const mxfa_mx* dout_mx, const void* o, const void* dout, const float* lse,
+                          int B, int S, int H, int D, float softmax_scale, int causal,
+                          const mxfa_attn_opts* opts, int dq_mode, float dq_static_scale, void* dq,
+                          void* dk, void* dv, void* ws, size_t ws_bytes, mxfa_stream_t stream);
+mxfa_status mxfa_varlen_bwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                 const mxfa_mx* dout_mx, const void* o, const void* dout,
+                                 const float* lse, const int32_t* cu_seqlens_q,
+                                 const int32_t* cu_seqlens_k, int nseq, int max_seqlen_q,
+                                 int max_seqlen_k, int64_t total_q, int64_t total_k,
+                                 int64_t ptiles_q, int64_t ptiles_k, int H, int D,
+                                 float softmax_scale, int causal, const mxfa_attn_opts* opts,
+                                 int dq_mode, float dq_static_scale, void* dq, void* dk, void* dv,
+                                 void* ws, size_t ws_bytes, mxfa_stream_t stream);
 
 /* mxfa_bwd_mxg, mxfa_varlen_bwd_mxg -- the backward passes above that also
  * emit the gradients as MXFP8 ([TMEM] page, section "What the Benchmarks
@@ -295,6 +345,36 @@ mxfa_status mxfa_bwd_noalloc(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* 
                              int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
                              void* dv, mxfa_stream_t stream);
 size_t mxfa_bwd_noalloc_scratch_bytes(void);
+
+/* mxfa_gemm_quant -- projection GEMM with the quantization fused into its
+ * epilogue ([TMEM] "fused producers": projection GEMM epilogues emit FP8;
+ * [ITEMS] item 7: GEMM+Quantize with dual scale-factor layouts in one pass).
+ *  a   ROW-quantized A [M][K] (payload, and packed ROW scales with K / 128
+ *      column groups, i.e. mxfa_quantize(MXFA_BLK_ROW) of a bf16 [M][K/128][128])
+ *  b   ROW-quantized B [N][K] likewise (a weight stored [out][in])
+ *  Y = A B^T (dequantized operands, fp32 accumulation), written as
+ *  y_bf16  bf16 [M][N] (nullable)
+ *  y_row   MXFP8 of Y in 1x32 blocks along N: payload [M][N], compact scales
+ *          [M][N / 32], packed ROW atoms of (128-row tile, 128-column group),
+ *          as mxfa_quantize(MXFA_BLK_ROW) lays them out for Y seen as
+ *          [M][N / 128][128] (nullable; its scale pointers nullable)
+ *  y_col   MXFP8 of Y in 32x1 blocks along M (blocks start at multiples of
+ *          32 rows): payload [M][N], compact scales [M / 32][N], packed COL
+ *          atoms (nullable; its scale pointers nullable)
+ *  At least one output must be given.  M, N, K multiples of 128
+ *  (else MXFA_ERR_UNSUPPORTED).  Each output block is quantized with the OCP
+ *  rule of mxfa_quantize from the fp32 value of Y (not from its bf16 copy). */
+mxfa_status mxfa_gemm_quant(const mxfa_mx* a, const mxfa_mx* b, int64_t M, int64_t N, int64_t K,
+                            void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
+                            mxfa_stream_t stream);
+
+/* mxfa_tensor_peak_probe -- `ctas` CTAs (one per SM at most) each issue
+ * `iters` x 4 back-to-back block-scaled MMAs (M = 128, N = 256, K = 32, E4M3,
+ * operands resident in shared memory) and write the SM clock cycles they took
+ * to cycles[ctas] (DEVICE, 8-byte aligned).  The pages have no counterpart: it
+ * measures this GPU's dense MXFP8 tensor-pipe peak, the denominator of the
+ * benchmark's roofline fractions (MACs per CTA = iters * 4 * 128 * 256 * 32). */
+mxfa_status mxfa_tensor_peak_probe(int iters, int ctas, unsigned long long* cycles, mxfa_stream_t stream);
 
 /* Synchronise `stream`, then return and clear the device status words:
  * MXFA_OK, MXFA_ERR_TIMEOUT or MXFA_ERR_DEVICE_INDEX (bit flags also in

@@ -12,8 +12,10 @@ from . import inputs  # noqa: F401  (seeded synthetic workloads; no arithmetic)
 def __getattr__(name):
     if name.startswith("mxfa_") or name in ("lib", "MxfaError",
                                             "Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ",
+                                            "AttnOpts", "P_SCALE_BLOCK", "P_SCALE_CONST",
+                                            "RESCALE_THRESHOLD",
                                             "quantize", "sf_pack", "sf_unpack", "attention_fwd",
-                                            "attention_bwd", "rmsnorm_quant",
+                                            "attention_bwd", "rmsnorm_quant", "gemm_quant",
                                             "device_status"):
         from . import mxfa as _m
         return getattr(_m, name)

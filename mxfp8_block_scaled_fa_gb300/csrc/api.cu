@@ -114,11 +114,26 @@ mxfa_status check_mx(const mxfa_mx* x) {
   return MXFA_OK;
 }
 
+// Options: NULL = defaults; otherwise checked.
+mxfa_status read_opts(const mxfa_attn_opts* opts, float& thr, int& p_scale) {
+  thr = MXFA_FWD_RESCALE_THRESHOLD;
+  p_scale = MXFA_P_SCALE_BLOCK;
+  if (!opts) return MXFA_OK;
+  if (!(opts->rescale_threshold >= 0.0f && opts->rescale_threshold <= 8.0f)) return MXFA_ERR_INVALID_ARG;
+  if (opts->p_scale != MXFA_P_SCALE_BLOCK && opts->p_scale != MXFA_P_SCALE_CONST) return MXFA_ERR_INVALID_ARG;
+  thr = opts->rescale_threshold;
+  p_scale = opts->p_scale;
+  return MXFA_OK;
+}
+
 mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seqs sq, Seqs sk,
                        int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
                        float scale, int causal, void* o, float* lse, const mxfa_mx_out* omx, bool dense,
-                       mxfa_stream_t stream) {
+                       mxfa_stream_t stream, const mxfa_attn_opts* opts = nullptr) {
   mxfa_status s;
+  float thr;
+  int p_scale;
+  if ((s = read_opts(opts, thr, p_scale))) return s;
   if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v))) return s;
   if (!o || !lse || H <= 0) return MXFA_ERR_INVALID_ARG;
   if (omx && (!omx->data || !aligned16(omx->data) || (omx->sf_compact && !aligned4(omx->sf_compact)) ||
@@ -144,6 +159,9 @@ mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seq
   a.ptiles_k = ptk;
   a.H = H;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.rescale_thr = thr;
+  // constant P scale: 2^(ceil(thr) - 8), the largest possible P~ = 2^ceil(thr) -> 256
+  a.p_sc_const = p_scale == MXFA_P_SCALE_CONST ? uint32_t(127 + int(std::ceil(thr)) - 8) : 0u;
   a.causal = causal ? 1 : 0;
   a.o = static_cast<uint16_t*>(o);
   if (omx) {
@@ -162,8 +180,11 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
                        int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
                        float scale, int causal, int dq_mode, float dq_static_scale, void* dq, void* dk,
                        void* dv, void* ws, size_t ws_bytes, const mxfa_mx_out* gmx[3], bool dense,
-                       mxfa_stream_t stream) {
+                       mxfa_stream_t stream, const mxfa_attn_opts* opts = nullptr) {
   mxfa_status s;
+  float thr_unused;
+  int p_scale;
+  if ((s = read_opts(opts, thr_unused, p_scale))) return s;
   if ((s = check_mx(q)) || (s = check_mx(k)) || (s = check_mx(v)) || (s = check_mx(dmx))) return s;
   for (int i = 0; i < 3 && gmx; i++) {
     const mxfa_mx_out* m = gmx[i];
@@ -212,6 +233,8 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   a.ptiles_k = ptk;
   a.H = H;
   a.scale = scale;
+  // constant P^T scale 2^-8: P <= 1 maps to <= 256
+  a.p_sc_const = p_scale == MXFA_P_SCALE_CONST ? 119u : 0u;
   a.causal = causal ? 1 : 0;
   a.dq_mode = dq_mode;
   a.dq_static_scale = dq_mode == 1 ? dq_static_scale : 1.0f;
@@ -395,6 +418,32 @@ mxfa_status mxfa_varlen_fwd_mxo(const mxfa_mx* q, const mxfa_mx* k, const mxfa_m
                     ptk, H, D, softmax_scale, causal, o, lse, o_mx, false, stream);
 }
 
+mxfa_status mxfa_fwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, int B, int S, int H,
+                          int D, float softmax_scale, int causal, const mxfa_attn_opts* opts, void* o,
+                          float* lse, mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  return fwd_common(q, k, v, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total, pt, pt, H, D,
+                    softmax_scale, causal, o, lse, nullptr, true, stream, opts);
+}
+
+mxfa_status mxfa_varlen_fwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                 const int32_t* cu_q, const int32_t* cu_k, int nseq, int max_sq,
+                                 int max_sk, int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk,
+                                 int H, int D, float softmax_scale, int causal,
+                                 const mxfa_attn_opts* opts, void* o, float* lse, mxfa_stream_t stream) {
+  if (!cu_q || !cu_k) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  if (max_sk <= 0) return MXFA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk}, total_q, total_k, ptq,
+                    ptk, H, D, softmax_scale, causal, o, lse, nullptr, false, stream, opts);
+}
+
 size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_mode) {
   if (total_q < 0 || nseq <= 0 || H <= 0 || D <= 0) return 0;
   return bwd_records_bytes(total_q, nseq, H) + size_t(total_q) * H * D * (dq_mode == 1 ? 2u : 4u);
@@ -412,6 +461,38 @@ mxfa_status mxfa_bwd(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const
   return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total,
                     pt, pt, H, D, softmax_scale, causal, dq_mode, dq_static_scale, dq, dk, dv, ws,
                     ws_bytes, nullptr, true, stream);
+}
+
+mxfa_status mxfa_bwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
+                          const void* o, const void* dout, const float* lse, int B, int S, int H, int D,
+                          float softmax_scale, int causal, const mxfa_attn_opts* opts, int dq_mode,
+                          float dq_static_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                          mxfa_stream_t stream) {
+  if (B <= 0 || S <= 0) return MXFA_ERR_INVALID_ARG;
+  const int64_t total = int64_t(B) * S;
+  mxfa_status s = check_seqs(nullptr, B, S, total);
+  if (s) return s;
+  const int64_t pt = int64_t(B) * ceil_div(S, 128);
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{nullptr, B, S}, Seqs{nullptr, B, S}, total, total,
+                    pt, pt, H, D, softmax_scale, causal, dq_mode, dq_static_scale, dq, dk, dv, ws,
+                    ws_bytes, nullptr, true, stream, opts);
+}
+
+mxfa_status mxfa_varlen_bwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v,
+                                 const mxfa_mx* dmx, const void* o, const void* dout, const float* lse,
+                                 const int32_t* cu_q, const int32_t* cu_k, int nseq, int max_sq,
+                                 int max_sk, int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk,
+                                 int H, int D, float softmax_scale, int causal,
+                                 const mxfa_attn_opts* opts, int dq_mode, float dq_static_scale,
+                                 void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                 mxfa_stream_t stream) {
+  if (!cu_q || !cu_k) return MXFA_ERR_INVALID_ARG;
+  mxfa_status s;
+  if ((s = check_seqs(cu_q, nseq, max_sq, total_q)) || (s = check_seqs(cu_k, nseq, max_sk, total_k)))
+    return s;
+  return bwd_common(q, k, v, dmx, o, dout, lse, Seqs{cu_q, nseq, max_sq}, Seqs{cu_k, nseq, max_sk},
+                    total_q, total_k, ptq, ptk, H, D, softmax_scale, causal, dq_mode, dq_static_scale,
+                    dq, dk, dv, ws, ws_bytes, nullptr, false, stream, opts);
 }
 
 mxfa_status mxfa_bwd_mxg(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, const mxfa_mx* dmx,
@@ -499,10 +580,50 @@ mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int
   return from_cuda(launch_rmsnorm_quant(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mxfa_status mxfa_gemm_quant(const mxfa_mx* a, const mxfa_mx* b, int64_t M, int64_t N, int64_t K,
+                            void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
+                            mxfa_stream_t stream) {
+  mxfa_status s;
+  if ((s = check_mx(a)) || (s = check_mx(b))) return s;
+  if (M < 0 || N < 0 || K < 0) return MXFA_ERR_INVALID_ARG;
+  if (M % 128 || N % 128 || K % 128) return MXFA_ERR_UNSUPPORTED;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 24) || K >= (int64_t(1) << 24)) return MXFA_ERR_UNSUPPORTED;
+  if (!y_bf16 && !y_row && !y_col) return MXFA_ERR_INVALID_ARG;
+  if (y_bf16 && !aligned16(y_bf16)) return MXFA_ERR_MISALIGNED;
+  for (const mxfa_mx_out* m : {y_row, y_col}) {
+    if (!m) continue;
+    if (!m->data) return MXFA_ERR_INVALID_ARG;
+    if (!aligned16(m->data) || (m->sf_compact && !aligned4(m->sf_compact)) ||
+        (m->sf_packed && !aligned16(m->sf_packed)))
+      return MXFA_ERR_MISALIGNED;
+  }
+  if (M == 0 || N == 0) return MXFA_OK;
+  if (K == 0) return MXFA_ERR_UNSUPPORTED;
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  if (!make_map_u8(&g.tm_a, a->data, M, int(K / 128), 128) || !make_map_u8(&g.tm_b, b->data, N, int(K / 128), 128))
+    return MXFA_ERR_CUDA;
+  g.sfa = a->sf;
+  g.sfb = b->sf;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.y_bf16 = static_cast<uint16_t*>(y_bf16);
+  if (y_row) { g.row_data = y_row->data; g.row_sfc = y_row->sf_compact; g.row_sfp = y_row->sf_packed; }
+  if (y_col) { g.col_data = y_col->data; g.col_sfc = y_col->sf_compact; g.col_sfp = y_col->sf_packed; }
+  return from_cuda(launch_gemm_quant(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_tensor_peak_probe(int iters, int ctas, unsigned long long* cycles, mxfa_stream_t stream) {
+  if (iters <= 0 || ctas <= 0 || !cycles) return MXFA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cycles) & 7u) return MXFA_ERR_MISALIGNED;
+  return from_cuda(launch_mma_peak(iters, ctas, cycles, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mxfa_status mxfa_get_device_status(mxfa_stream_t stream, unsigned* flags) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return MXFA_ERR_CUDA;
-  unsigned f = read_status_quant(st) | read_status_fwd(st) | read_status_bwd(st);
+  unsigned f = read_status_quant(st) | read_status_fwd(st) | read_status_bwd(st) | read_status_gemm(st);
   if (flags) *flags = f;
   if (f & 1u) return MXFA_ERR_TIMEOUT;
   if (f & 2u) return MXFA_ERR_DEVICE_INDEX;

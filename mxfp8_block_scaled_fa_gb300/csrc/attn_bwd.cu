@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         // per warp, its maximum by a warp-wide absolute-maximum reduction
         float wmax;
         asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(wmax) : "f"(damax));
-        sp = e8m0_from_amax(pmax);
+        sp = a.p_sc_const ? a.p_sc_const : e8m0_from_amax(pmax);
         sd = e8m0_from_amax(wmax);
         const float2 ip = make_float2(e8m0_inv_scale(sp), e8m0_inv_scale(sp));
         const float2 id = make_float2(e8m0_inv_scale(sd), e8m0_inv_scale(sd));

@@ -23,9 +23,12 @@
 // O_B [384,512).  Once a tile's softmax has loaded S_X(j), the columns of S_X
 // carry P_X(j) [0,32), its scales [32,36), the V scales [36,40) (read by
 // PV_X(j)), and the Q / K scales of the other tile's next S GEMM [40,48).
-// The running max moves only when it grows by more than kRescaleThr (log2
-// units); P~ then stays below 2^kRescaleThr, which the E8M0 block scale
-// absorbs, and O and l carry the stale max exactly.  The epilogue writes O as
+// The running max moves only when it grows by more than a threshold (log2
+// units, 8 by default, 0 = at every increase); P~ then stays below
+// 2^threshold, which the E8M0 block scale absorbs, and O and l carry the
+// stale max exactly.  P's block scales come from the block maxima, or, in the
+// constant-scale mode, are one fixed E8M0 byte for every block (the pages'
+// constant scaling of softmax outputs, which lie in a known range).  The epilogue writes O as
 // bf16 and, on request, also as MXFP8 (the bf16 row quantized in 1x32 blocks
 // along D, with compact and packed scales).
 #include <cuda_bf16.h>
@@ -42,7 +45,6 @@ namespace fwd {
 constexpr int NS = 4;  // K/V pipeline stages
 constexpr int TILE = 128;
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows x 128 E4M3
-constexpr float kRescaleThr = 8.0f;
 
 constexpr int OFF_Q = 0;                               // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;          // NS stages
@@ -89,6 +91,8 @@ __device__ __forceinline__ void fwd_warp_arrive(uint32_t bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
+// PCONST: every P block takes the scale a.p_sc_const (the constant-scale mode)
+template <bool PCONST>
 __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using namespace fwd;
   extern __shared__ uint8_t smem_raw[];
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       // fl(max S * sl2) = max fl(S * sl2) since sl2 > 0
       const float mt = __fmul_rn(pm, sl2);
       const float mn = fmaxf(m, mt);
-      const float mu = (m == -INFINITY || __fsub_rn(mn, m) > kRescaleThr) ? mn : m;
+      const float mu = (m == -INFINITY || __fsub_rn(mn, m) > a.rescale_thr) ? mn : m;
       const float mref = mu == -INFINITY ? 0.0f : mu;
       const float alpha = ex2(__fsub_rn(m, mref));
       const bool rescale = (m != -INFINITY) && (mu > m);
@@ -348,7 +352,8 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       float lt = 0.0f;
 #pragma unroll
       for (int kb = 0; kb < 4; kb++) {
-        const uint32_t sc = e8m0_from_amax(ex2(__fsub_rn(__fmul_rn(bm[kb], sl2), mref)));
+        const uint32_t sc =
+            PCONST ? a.p_sc_const : e8m0_from_amax(ex2(__fsub_rn(__fmul_rn(bm[kb], sl2), mref)));
         sfw |= sc << (8 * kb);
         const float nmx = -__fadd_rn(mref, float(int(sc) - 127));
         float2 rs = make_float2(0.0f, 0.0f);
@@ -470,7 +475,10 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> attr{0};
   clear_stale_error();
   cudaError_t e = once_per_device(attr, [] {
-    return cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t r = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         fwd::SMEM_BYTES);
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fwd::SMEM_BYTES);
   });
   if (e != cudaSuccess) return e;
@@ -483,7 +491,10 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
                 unsigned(a.sq.nseq));
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  attn_fwd_kernel<<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
+  if (a.p_sc_const)
+    attn_fwd_kernel<true><<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
+  else
+    attn_fwd_kernel<false><<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(a);
   return cudaGetLastError();
 }
 

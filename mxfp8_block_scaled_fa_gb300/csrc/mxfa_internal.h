@@ -93,6 +93,8 @@ struct FwdArgs {
   int64_t ptiles_q, ptiles_k;  // packed tile counts (bounds of sfq / sfk, sfv)
   int H;
   float scale_log2;  // softmax scale * log2(e)
+  float rescale_thr; // running max moves when it grows by more than this (log2 units)
+  uint32_t p_sc_const;  // 0: P block scales from the block maxima; else this E8M0 byte for every block
   int causal;
   uint16_t* o;       // bf16 [tokens][H][128]
   uint8_t* omx;      // nullable: O quantized (ROW, 1x32 along D) E4M3 [tokens][H][128]
@@ -119,6 +121,7 @@ struct BwdArgs {
   int64_t ptiles_q, ptiles_k;
   int H;
   float scale;        // softmax scale
+  uint32_t p_sc_const; // 0: P^T block scales from the block maxima; else this E8M0 byte for every block
   int causal;
   int dq_mode;        // 0 fp32 accumulation, 1 fp16 with static scale
   float dq_static_scale;
@@ -137,8 +140,22 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 
+struct GemmArgs {
+  CUtensorMap tm_a, tm_b;  // u8 [M][K/128][128] and [N][K/128][128], box 128 x 1 x 128, 128B swizzle
+  const uint8_t* sfa;      // packed ROW atoms of A: entry (m / 128) * (K / 128) + k / 128
+  const uint8_t* sfb;      // packed ROW atoms of B: entry (n / 128) * (K / 128) + k / 128
+  int64_t M, N, K;         // multiples of 128
+  uint16_t* y_bf16;        // nullable: Y bf16 [M][N]
+  uint8_t *row_data, *row_sfc, *row_sfp;  // nullable: Y MXFP8, 1x32 along N
+  uint8_t *col_data, *col_sfc, *col_sfp;  // nullable: Y MXFP8, 32x1 along M
+};
+cudaError_t launch_gemm_quant(const GemmArgs& a, cudaStream_t s);
+// Tensor-pipe peak probe: `ctas` CTAs of back-to-back MMAs, cycles per CTA.
+cudaError_t launch_mma_peak(int iters, int ctas, unsigned long long* cycles, cudaStream_t s);
+
 // Read (and clear) the device status words of every kernel module.
 unsigned read_status_quant(cudaStream_t s);
+unsigned read_status_gemm(cudaStream_t s);
 unsigned read_status_fwd(cudaStream_t s);
 unsigned read_status_bwd(cudaStream_t s);
 

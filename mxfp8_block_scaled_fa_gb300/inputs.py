@@ -19,6 +19,11 @@ rounded to bf16 unless stated):
   packed token-major with ``cu_seqlens``, seed 3
 * ``fused``     X[32768, 2048] normal, gamma ``uniform(0.5, 1.5)`` float32,
   dO[4, 8192, 16, 128] normal, eps 1e-6, attention causal, seed 4
+* ``long_kv``   long-key jagged batches (key lengths up to 16384), H=8 D=128,
+  16 sequences, seed 5: ``jagged`` cross-attention with 1024 queries per
+  sequence and key lengths ``integers(1024, 16384, endpoint)``;
+  ``uniform`` the same with every key length 16384; ``causal`` self-attention
+  with lengths ``integers(1024, 16384, endpoint)``, causal
 """
 from __future__ import annotations
 
@@ -32,6 +37,7 @@ CONFIGS = {
                    lq=(64, 2048), lk=(32, 1024)),
     "fused": dict(T=32768, C=2048, B=4, S=8192, H=16, D=128, causal=True, seed=4,
                   eps=1e-6),
+    "long_kv": dict(nseq=16, H=8, D=128, seed=5, lq_cross=1024, lk=(1024, 16384)),
 }
 
 
@@ -116,3 +122,25 @@ def fused_inputs(T=32768, C=2048, B=4, S=8192, H=16, D=128, seed=4):
 def normal_bf16(shape, seed):
     """Generic seeded N(0,1) bf16 bits of any shape."""
     return _normal_bf16(np.random.Generator(np.random.PCG64(seed)), shape)
+
+
+def long_kv_lengths(kind, nseq=16, seed=5, lq_cross=1024, lk=(1024, 16384)):
+    """(query lengths, key lengths, causal) of a long-key batch: kind is
+    'jagged' (cross, jagged keys), 'uniform' (cross, every key length lk[1])
+    or 'causal' (self-attention, jagged lengths)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = rng.integers(lk[0], lk[1], size=nseq, endpoint=True).astype(np.int64)
+    if kind == "jagged":
+        return np.full(nseq, lq_cross, np.int64), lens, False
+    if kind == "uniform":
+        return np.full(nseq, lq_cross, np.int64), np.full(nseq, lk[1], np.int64), False
+    if kind == "causal":
+        return lens, lens.copy(), True
+    raise ValueError(kind)
+
+
+def long_kv_attn(kind, nseq=16, H=8, D=128, seed=5):
+    """Q, K, V, dO bf16 bits (packed token-major) + cu_seqlens + causal flag."""
+    lq, lk, causal = long_kv_lengths(kind, nseq, seed)
+    q, k, v, do, cu_q, cu_k = varlen_attn(lq, lk, H, D, seed + 100)
+    return q, k, v, do, cu_q, cu_k, causal

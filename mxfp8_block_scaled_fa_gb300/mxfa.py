@@ -54,6 +54,15 @@ class MxIn(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
 
 
+P_SCALE_BLOCK, P_SCALE_CONST = 0, 1
+RESCALE_THRESHOLD = 8.0
+
+
+class AttnOpts(ctypes.Structure):
+    """mxfa_attn_opts: forward rescale threshold (log2 units) and the P scale mode."""
+    _fields_ = [("rescale_threshold", ctypes.c_float), ("p_scale", ctypes.c_int)]
+
+
 _lib = None
 
 
@@ -81,6 +90,13 @@ def lib() -> ctypes.CDLL:
             "mxfa_fwd_mxo": (I, [P, P, P, I, I, I, I, F, I, P, P, P, P]),
             "mxfa_varlen_fwd_mxo": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P,
                                         P, P, P]),
+            "mxfa_fwd_opts": (I, [P, P, P, I, I, I, I, F, I, P, P, P, P]),
+            "mxfa_varlen_fwd_opts": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I,
+                                         P, P, P, P]),
+            "mxfa_bwd_opts": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, P, I, F, P, P, P, P, S,
+                                  P]),
+            "mxfa_varlen_bwd_opts": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64,
+                                         I, I, F, I, P, I, F, P, P, P, P, S, P]),
             "mxfa_bwd_workspace_size": (S, [I64, I, I, I, I]),
             "mxfa_bwd": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P, S, P]),
             "mxfa_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I,
@@ -91,6 +107,8 @@ def lib() -> ctypes.CDLL:
                                         I, F, I, I, F, P, P, P, P, S, P, P, P, P]),
             "mxfa_rmsnorm_quant": (I, [P, P, I64, I64, F, I, I, P, P, P, P]),
             "mxfa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint)]),
+            "mxfa_gemm_quant": (I, [P, P, I64, I64, I64, P, P, P, P]),
+            "mxfa_tensor_peak_probe": (I, [I, I, P, P]),
             "mxfa_bwd_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P]),
             "mxfa_bwd_noalloc_scratch_bytes": (S, []),
         }
@@ -304,10 +322,52 @@ def sf_unpack(sf_packed: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 12
     return sfc
 
 
+def _opts_ref(opts):
+    return None if opts is None else ctypes.byref(opts)
+
+
+def mxfa_fwd_opts(q, k, v, B, S, H, D, scale, causal, opts, o, lse, stream=None):
+    _check(lib().mxfa_fwd_opts(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), B, S, H, D,
+                               float(scale), int(causal), _opts_ref(opts), _p(o), _p(lse),
+                               _stream(stream)), "mxfa_fwd_opts")
+
+
+def mxfa_varlen_fwd_opts(q, k, v, cu_q, cu_k, nseq, max_sq, max_sk, total_q, total_k, ptq, ptk, H,
+                         D, scale, causal, opts, o, lse, stream=None):
+    _check(lib().mxfa_varlen_fwd_opts(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), _p(cu_q),
+                                      _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk,
+                                      H, D, float(scale), int(causal), _opts_ref(opts), _p(o),
+                                      _p(lse), _stream(stream)), "mxfa_varlen_fwd_opts")
+
+
+def mxfa_bwd_opts(q, k, v, do_mx, o, do, lse, B, S, H, D, scale, causal, opts, dq_mode, dq_static,
+                  dq, dk, dv, ws, ws_bytes, stream=None):
+    _check(lib().mxfa_bwd_opts(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                               ctypes.byref(do_mx), _p(o), _p(do), _p(lse), B, S, H, D,
+                               float(scale), int(causal), _opts_ref(opts), dq_mode,
+                               float(dq_static), _p(dq), _p(dk), _p(dv), _p(ws), ws_bytes,
+                               _stream(stream)), "mxfa_bwd_opts")
+
+
+def mxfa_varlen_bwd_opts(q, k, v, do_mx, o, do, lse, cu_q, cu_k, nseq, max_sq, max_sk, total_q,
+                         total_k, ptq, ptk, H, D, scale, causal, opts, dq_mode, dq_static, dq, dk,
+                         dv, ws, ws_bytes, stream=None):
+    _check(lib().mxfa_varlen_bwd_opts(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                      ctypes.byref(do_mx), _p(o), _p(do), _p(lse), _p(cu_q),
+                                      _p(cu_k), nseq, max_sq, max_sk, total_q, total_k, ptq, ptk,
+                                      H, D, float(scale), int(causal), _opts_ref(opts), dq_mode,
+                                      float(dq_static), _p(dq), _p(dk), _p(dv), _p(ws), ws_bytes,
+                                      _stream(stream)), "mxfa_varlen_bwd_opts")
+
+
 def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,
-                  causal: bool = False, stream=None, out=None, o_mx: bool = False):
+                  causal: bool = False, stream=None, out=None, o_mx: bool = False,
+                  opts: Optional[AttnOpts] = None):
     """Forward on quantized operands -> (O bf16 [tokens, H, D], lse fp32), and with
-    o_mx=True also O as MXFP8 (Mx with ROW compact and packed scales) as a third item."""
+    o_mx=True also O as MXFP8 (Mx with ROW compact and packed scales) as a third item.
+    opts (AttnOpts) selects the rescale threshold and the P scale mode (no MXFP8 O then)."""
+    if opts is not None and o_mx:
+        raise ValueError("opts and o_mx cannot be combined")
     H, D = q.data.shape[-2], q.data.shape[-1]
     dev = q.data.device
     o = out[0] if out is not None else torch.empty(q.data.shape, dtype=torch.bfloat16, device=dev)
@@ -324,6 +384,8 @@ def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,
                 causal, o, lse)
         if o_mx:
             mxfa_fwd_mxo(*args, omx_s, stream)
+        elif opts is not None:
+            mxfa_fwd_opts(*args[:9], opts, o, lse, stream)
         else:
             mxfa_fwd(*args, stream)
     else:
@@ -334,6 +396,8 @@ def attention_fwd(q: Mx, k: Mx, v: Mx, seqs_q: Seqs, seqs_k: Seqs, scale: float,
                 seqs_k.ptiles, H, D, scale, causal, o, lse)
         if o_mx:
             mxfa_varlen_fwd_mxo(*args, omx_s, stream)
+        elif opts is not None:
+            mxfa_varlen_fwd_opts(*args[:16], opts, o, lse, stream)
         else:
             mxfa_varlen_fwd(*args, stream)
     return (o, lse, omx) if o_mx else (o, lse)
@@ -365,9 +429,12 @@ def mxfa_varlen_bwd_mxg(q, k, v, do_mx, o, do, lse, cu_q, cu_k, nseq, max_sq, ma
 def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Tensor,
                   lse: torch.Tensor, seqs_q: Seqs, seqs_k: Seqs, scale: float,
                   causal: bool = False, dq_mode: int = 0, dq_static: float = 1.0, stream=None,
-                  ws=None, out=None, grads_mx: bool = False):
+                  ws=None, out=None, grads_mx: bool = False, opts: Optional[AttnOpts] = None):
     """Backward on quantized operands -> (dQ, dK, dV) bf16; with grads_mx=True also the
-    three gradients as MXFP8 (Mx with ROW compact and packed scales), six items in all."""
+    three gradients as MXFP8 (Mx with ROW compact and packed scales), six items in all.
+    opts (AttnOpts) selects the P scale mode (no MXFP8 gradients then)."""
+    if opts is not None and grads_mx:
+        raise ValueError("opts and grads_mx cannot be combined")
     H, D = q.data.shape[-2], q.data.shape[-1]
     dev = q.data.device
     wsb = mxfa_bwd_workspace_size(seqs_q.total, seqs_q.nseq, H, D, dq_mode)
@@ -393,6 +460,8 @@ def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Ten
                 ws.numel())
         if grads_mx:
             mxfa_bwd_mxg(*args, *gs, stream)
+        elif opts is not None:
+            mxfa_bwd_opts(*args[:13], opts, *args[13:], stream)
         else:
             mxfa_bwd(*args, stream)
     else:
@@ -402,6 +471,8 @@ def attention_bwd(q: Mx, k: Mx, v: Mx, do_mx: Mx, o: torch.Tensor, do: torch.Ten
                 dq_static, dq, dk, dv, ws, ws.numel())
         if grads_mx:
             mxfa_varlen_bwd_mxg(*args, *gs, stream)
+        elif opts is not None:
+            mxfa_varlen_bwd_opts(*args[:20], opts, *args[20:], stream)
         else:
             mxfa_varlen_bwd(*args, stream)
     return (dq, dk, dv, *gmx) if grads_mx else (dq, dk, dv)
@@ -431,6 +502,41 @@ def rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float, seg_len: int
         structs[name] = MxOut(data.data_ptr(), sfc.data_ptr(), _p(sfp))
     mxfa_rmsnorm_quant(x, gamma, T, C, eps, seg_len, H, structs.get("row"), structs.get("col"),
                        structs.get("sq"), stream)
+    return res
+
+
+def mxfa_gemm_quant(a: MxIn, b: MxIn, M, N, K, y_bf16, y_row: Optional[MxOut],
+                    y_col: Optional[MxOut], stream=None):
+    ref = lambda m: ctypes.byref(m) if m is not None else None
+    _check(lib().mxfa_gemm_quant(ctypes.byref(a), ctypes.byref(b), M, N, K, _p(y_bf16), ref(y_row),
+                                 ref(y_col), _stream(stream)), "mxfa_gemm_quant")
+
+
+def mxfa_tensor_peak_probe(iters, ctas, cycles, stream=None):
+    _check(lib().mxfa_tensor_peak_probe(int(iters), int(ctas), _p(cycles), _stream(stream)),
+           "mxfa_tensor_peak_probe")
+
+
+def gemm_quant(a: Mx, b: Mx, bf16: bool = True, row: bool = True, col: bool = True,
+               stream=None):
+    """Y = A B^T on ROW-quantized A [M, K] and B [N, K] (Mx with packed scales, as
+    quantize(x.view(rows, K // 128, 128), ROW, Seqs.dense(1, rows)) makes them) ->
+    dict with 'bf16' (tensor [M, N]) and 'row' / 'col' (Mx over [M, N])."""
+    M, K = a.data.shape[0], a.data.numel() // a.data.shape[0]
+    N = b.data.shape[0]
+    dev = a.data.device
+    u8 = dict(dtype=torch.uint8, device=dev)
+    res, outs = {}, {}
+    if bf16:
+        res["bf16"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for name, blk, comp in (("row", ROW, (M, N // 32)), ("col", COL, (M // 32, N))):
+        if (name == "row" and row) or (name == "col" and col):
+            m = Mx(torch.empty((M, N), **u8), torch.empty(comp, **u8),
+                   torch.empty((M // 128) * (N // 128) * 512, **u8), blk)
+            res[name] = m
+            outs[name] = MxOut(m.data.data_ptr(), m.sf_compact.data_ptr(), m.sf_packed.data_ptr())
+    mxfa_gemm_quant(a.mx_in(), b.mx_in(), M, N, K, res.get("bf16"), outs.get("row"),
+                    outs.get("col"), stream)
     return res
 
 

@@ -64,13 +64,15 @@ def _load():
             lib.mxo_dequantize.argtypes = [P, P, I64, I64, I32, P, I32, P]
             lib.mxo_attn_fwd.restype = None
             lib.mxo_attn_fwd.argtypes = [P, P, P, P, P, I32, I32, I32, D, I32, I32,
-                                         I32, D, P, P, I64]
+                                         I32, D, P, P, I64, I32]
             lib.mxo_attn_bwd.restype = None
             lib.mxo_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I32, I32, I32, D,
-                                         I32, I32, I32, P, P, P, I64]
+                                         I32, I32, I32, P, P, P, I64, I32]
             lib.mxo_rmsnorm_quant.restype = None
             lib.mxo_rmsnorm_quant.argtypes = [P, P, I64, I64, ctypes.c_float, I32,
                                               ctypes.c_int32, P, P, P, P, P, P, P]
+            lib.mxo_gemm_nt.restype = None
+            lib.mxo_gemm_nt.argtypes = [P, P, I64, I64, I64, P]
             lib.mxo_num_threads.restype = I32
             lib.mxo_num_threads.argtypes = []
             lib.mxo_set_num_threads.restype = None
@@ -169,8 +171,10 @@ def qdq(x3d, mode: int, cu=None) -> np.ndarray:
 
 # ------------------------------------------------------------- attention
 def attn_fwd(q, k, v, cu_q, cu_k, scale, causal=False, quant_p=True, tile_n=128,
-             lazy_thr=0.0):
-    """Forward on dequantized operands [tokens, H, D] -> (O float64, lse [H, tokens])."""
+             lazy_thr=0.0, p_scale=0):
+    """Forward on dequantized operands [tokens, H, D] -> (O float64, lse [H, tokens]).
+
+    p_scale=1: every P block takes the constant exponent ceil(lazy_thr) - 8."""
     lib = _load()
     q, k, v = (_c(a, np.float64) for a in (q, k, v))
     tq, H, D = q.shape
@@ -180,13 +184,15 @@ def attn_fwd(q, k, v, cu_q, cu_k, scale, causal=False, quant_p=True, tile_n=128,
     lse = np.zeros((H, tq), np.float64)
     lib.mxo_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), n, H, D,
                      float(scale), int(causal), int(quant_p), int(tile_n),
-                     float(lazy_thr), _ptr(o), _ptr(lse), tq)
+                     float(lazy_thr), _ptr(o), _ptr(lse), tq, int(p_scale))
     return o, lse
 
 
 def attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal=False,
-             quant_p=True, quant_ds=True):
-    """Backward on dequantized operands -> (dQ, dK, dV) float64 [tokens, H, D]."""
+             quant_p=True, quant_ds=True, p_scale=0):
+    """Backward on dequantized operands -> (dQ, dK, dV) float64 [tokens, H, D].
+
+    p_scale=1: every P^T block takes the constant exponent -8."""
     lib = _load()
     q, k, v, do, o_bf, do_bf = (_c(a, np.float64) for a in (q, k, v, do, o_bf, do_bf))
     lse = _c(lse, np.float64)
@@ -198,13 +204,13 @@ def attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal=False,
     dv = np.zeros_like(v)
     lib.mxo_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(o_bf), _ptr(do_bf),
                      _ptr(lse), _ptr(cq), _ptr(ck), n, H, D, float(scale), int(causal),
-                     int(quant_p), int(quant_ds), _ptr(dq), _ptr(dk), _ptr(dv), tq)
+                     int(quant_p), int(quant_ds), _ptr(dq), _ptr(dk), _ptr(dv), tq, int(p_scale))
     return dq, dk, dv
 
 
 # --------------------------------------------------- the method, end to end
 def method_fwd(q_bf, k_bf, v_bf, cu_q, cu_k, scale, causal=False, quant=True,
-               tile_n=128, lazy_thr=0.0):
+               tile_n=128, lazy_thr=0.0, p_scale=0):
     """Quantize Q, K (1x32 along D) and V (32x1 along keys), then attention."""
     if quant:
         q = qdq(q_bf, ROW, cu_q)
@@ -212,11 +218,11 @@ def method_fwd(q_bf, k_bf, v_bf, cu_q, cu_k, scale, causal=False, quant=True,
         v = qdq(v_bf, COL, cu_k)
     else:
         q, k, v = q_bf, k_bf, v_bf
-    return attn_fwd(q, k, v, cu_q, cu_k, scale, causal, quant, tile_n, lazy_thr)
+    return attn_fwd(q, k, v, cu_q, cu_k, scale, causal, quant, tile_n, lazy_thr, p_scale)
 
 
 def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=False,
-               quant=True):
+               quant=True, p_scale=0):
     """Square-block Q, K, dO and row-block V, then the five-GEMM backward."""
     if quant:
         q = qdq(q_bf, SQ, cu_q)
@@ -226,7 +232,30 @@ def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=Fal
     else:
         q, k, do, v = q_bf, k_bf, do_bf, v_bf
     return attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal,
-                    quant, quant)
+                    quant, quant, p_scale)
+
+
+# ------------------------------------------------------- GEMM+Quantize
+def gemm_nt(a, b):
+    """y = a b^T in fp64 for a [M, K], b [N, K]."""
+    lib = _load()
+    a = _c(a, np.float64)
+    b = _c(b, np.float64)
+    M, K = a.shape
+    N = b.shape[0]
+    y = np.zeros((M, N), np.float64)
+    lib.mxo_gemm_nt(_ptr(a), _ptr(b), M, N, K, _ptr(y))
+    return y
+
+
+def method_gemm_quant(a_bf, b_bf):
+    """The GEMM+Quantize step: A, B quantized 1x32 along K, Y = A^ B^^T in fp64,
+    then Y quantized ROW (1x32 along N) and COL (32x1 along M).
+    Returns (Y, (row payload, row scales), (col payload, col scales))."""
+    a = dequantize(*quantize(a_bf, ROW), ROW)
+    b = dequantize(*quantize(b_bf, ROW), ROW)
+    y = gemm_nt(a, b)
+    return y, quantize(y, ROW), quantize(y, COL)
 
 
 # ------------------------------------------------------ RMSNorm+Quantize

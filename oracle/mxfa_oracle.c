@@ -240,6 +240,14 @@ static void qdq_block(double* v, int64_t n, int64_t vs) {
     v[i * vs] = mxo_e4m3_decode(mxo_e4m3_encode(ldexp(v[i * vs], -X))) * ldexp(1.0, X);
 }
 
+/* Quantize-dequantize a block with a given shared exponent X (the constant
+ * scale mode of P: "Meta's FlashAttention-4 Achieves 2.85 PF/s with MXFP8
+ * on Blackwell GPUs", item 4, constant scaling of softmax outputs). */
+static void qdq_block_fixed(double* v, int64_t n, int64_t vs, int X) {
+  for (int64_t i = 0; i < n; i++)
+    v[i * vs] = mxo_e4m3_decode(mxo_e4m3_encode(ldexp(v[i * vs], -X))) * ldexp(1.0, X);
+}
+
 static double flush_fp32_subnormal(double p) {
   return p < ldexp(1.0, -126) ? 0.0 : p;
 }
@@ -259,6 +267,9 @@ static double flush_fp32_subnormal(double p) {
  *   (lazy_thr = 0: exact rescale at every increase)
  *   O, l *= 2^(m_old - m);  P~ = 2^(s' - m);  l += sum P~ (unquantized)
  *   P~ quantized per 32-key block of the tile (when quant_p), then O += P^ V.
+ * p_scale = 1 replaces each block's own scale by one constant shared exponent
+ * X = ceil(lazy_thr) - 8, so the largest possible P~ = 2^ceil(lazy_thr) maps
+ * to 256 (constant scaling of softmax outputs, item 4 of the brifing.si page).
  * End: O /= l;  lse = (m + log2 l) * ln 2 (natural log); with no visible key
  * (an empty key sequence) O = 0 and lse = -inf.
  * causal masks key index > query index within a sequence (equal lengths).
@@ -266,7 +277,8 @@ static double flush_fp32_subnormal(double p) {
 void mxo_attn_fwd(const double* q, const double* k, const double* v,
                   const int32_t* cu_q, const int32_t* cu_k, int nseq, int H,
                   int D, double scale, int causal, int quant_p, int tile_n,
-                  double lazy_thr, double* o, double* lse, int64_t total_q) {
+                  double lazy_thr, double* o, double* lse, int64_t total_q, int p_scale) {
+  const int Xc = (int)ceil(lazy_thr) - 8;
   const double log2e = 1.4426950408889634074;
   const double ln2 = 0.69314718055994530942;
   /* rows (query token, head) are independent: one parallel loop over them */
@@ -315,7 +327,12 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
             l += sp[j];
           }
           if (quant_p)
-            for (int64_t b = 0; b < tile_n; b += 32) qdq_block(sp + b, 32, 1);
+            for (int64_t b = 0; b < tile_n; b += 32) {
+              if (p_scale)
+                qdq_block_fixed(sp + b, 32, 1, Xc);
+              else
+                qdq_block(sp + b, 32, 1);
+            }
           for (int64_t j = 0; j < nt; j++) {
             if (sp[j] == 0.0) continue;
             const double* vj = v + ((k0 + t0 + j) * H + h) * D;
@@ -353,13 +370,14 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
  *   (blocks anchored at the sequence start in both dimensions)
  *   dV_j = sum_i P^_ij dO_i;  dK_j = scale sum_i dS^_ij q_i;
  *   dQ_i = scale sum_j dS^_ij k_j.
- */
+ * p_scale = 1: P^ takes the constant shared exponent -8 (P <= 1 maps to
+ * <= 256) instead of each block's own. */
 void mxo_attn_bwd(const double* q, const double* k, const double* v,
                   const double* dO, const double* o_bf, const double* do_bf,
                   const double* lse, const int32_t* cu_q, const int32_t* cu_k,
                   int nseq, int H, int D, double scale, int causal, int quant_p,
                   int quant_ds, double* dq, double* dk, double* dv,
-                  int64_t total_q) {
+                  int64_t total_q, int p_scale) {
   /* heads in turn; inside a head, independent rows / columns / blocks run in
    * parallel (every element keeps its own summation order) */
   for (int g = 0; g < nseq; g++) {
@@ -394,7 +412,10 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
 #pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < lk; j++)
           for (int64_t ib = 0; ib < lq; ib += 32)
-            qdq_block(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk);
+            if (p_scale)
+              qdq_block_fixed(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk, -8);
+            else
+              qdq_block(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk);
       if (quant_ds) /* 32x32 square blocks */
 #pragma omp parallel for schedule(static)
         for (int64_t ib = 0; ib < lq; ib += 32)
@@ -513,6 +534,23 @@ void mxo_rmsnorm_quant(const float* x, const float* gamma, int64_t T, int64_t C,
   if (out_mask & 4) mxo_quantize(y, T, C, MXO_SQ, cu, nseg, q_sq, sf_sq);
   free(cu);
   free(y);
+}
+
+/* ------------------------------------------------------------------ */
+/* Projection GEMM ([RMS]: GEMM+Quantize; the quantization of Y is      */
+/* mxo_quantize, applied by the caller to the result)                   */
+/* ------------------------------------------------------------------ */
+
+/* y[m][n] = sum_k a[m][k] * b[n][k] in fp64 (a [M][K], b [N][K] row-major:
+ * a weight stored [out][in], as a projection layer holds it). */
+void mxo_gemm_nt(const double* a, const double* b, int64_t M, int64_t N, int64_t K, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; m++)
+    for (int64_t n = 0; n < N; n++) {
+      double s = 0.0;
+      for (int64_t k = 0; k < K; k++) s += a[m * K + k] * b[n * K + k];
+      y[m * N + n] = s;
+    }
 }
 
 int mxo_num_threads(void) {

@@ -102,6 +102,29 @@ def test_noalloc_argument_checks(lib):
     assert n(*args(m, 128, 0x4000, B=0)) == 1      # empty batch
 
 
+def test_attention_options_checks(lib):
+    # the *_opts calls validate their options before any launch
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    m = mxfa.MxIn(0x1000, 0x2000)
+    r = ctypes.byref
+    f = lib.mxfa_fwd_opts
+    fargs = lambda o: (r(m), r(m), r(m), 1, 256, 2, 128, 0.1, 0, o, 0x4000, 0x5000, None)
+    assert f(*fargs(r(mxfa.AttnOpts(-1.0, 0)))) == 1       # threshold below 0
+    assert f(*fargs(r(mxfa.AttnOpts(8.5, 0)))) == 1        # threshold above 8
+    assert f(*fargs(r(mxfa.AttnOpts(float("nan"), 0)))) == 1
+    assert f(*fargs(r(mxfa.AttnOpts(4.0, 2)))) == 1        # unknown P scale mode
+    assert f(*fargs(r(mxfa.AttnOpts(4.0, 1)))[:6] + (96,) + fargs(None)[7:]) == 2   # D
+    b = lib.mxfa_bwd_opts
+    ws = mxfa.mxfa_bwd_workspace_size(256, 1, 2, 128, 0)
+    bargs = lambda o, wsb=ws: (r(m), r(m), r(m), r(m), 0x4000, 0x5000, 0x6000, 1, 256, 2, 128, 0.1,
+                               0, o, 0, 1.0, 0x7000, 0x8000, 0x9000, 0xA000, wsb, None)
+    assert b(*bargs(r(mxfa.AttnOpts(8.0, 3)))) == 1
+    assert b(*bargs(r(mxfa.AttnOpts(8.0, 1)), ws - 1)) == 4  # workspace still checked
+    vf = lib.mxfa_varlen_fwd_opts
+    assert vf(r(m), r(m), r(m), None, None, 2, 10, 10, 20, 20, 2, 2, 2, 128, 0.1, 0, None, 0x4000,
+              0x5000, None) == 1                            # varlen needs cu_seqlens
+
+
 def test_attention_argument_checks(lib):
     from mxfp8_block_scaled_fa_gb300 import mxfa
     m = mxfa.MxIn(0x1000, 0x2000)

@@ -130,6 +130,43 @@ def test_bwd_varlen_empty_sequences(mx):
     check(got, ref)
 
 
+@pytest.mark.parametrize("varlen", [False, True])
+def test_bwd_constant_p_scale(mx, varlen):
+    # P^T quantized with the constant scale 2^-8 instead of each block's own,
+    # against the oracle in the same mode
+    import torch
+    H, D = 2, 128
+    scale = 1 / math.sqrt(D)
+    if varlen:
+        lq = [64, 300, 7, 129, 1, 255]
+        lk = [32, 200, 1, 260, 77, 128]
+        qb, kb, vb, dob, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=71)
+        sq, sk = mx.Seqs.varlen(lq, "cuda"), mx.Seqs.varlen(lk, "cuda")
+        causal = False
+    else:
+        B, S = 2, 300
+        qb, kb, vb, dob = (b.reshape(B * S, H, D) for b in inputs.dense_attn(B, H, S, D, seed=72))
+        cu_q = cu_k = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+        sq = sk = mx.Seqs.dense(B, S)
+        causal = True
+    o_bits, o_bf, lse = oracle_fwd_out(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, causal)
+    lse_dev = (torch.from_numpy(lse.astype(np.float32)).cuda() if varlen else
+               torch.from_numpy(lse.reshape(H, 2, 300).transpose(1, 0, 2).astype(np.float32)
+                                .copy()).cuda())
+    q = mx.quantize(to_dev(qb), mx.SQ, sq)
+    k = mx.quantize(to_dev(kb), mx.SQ, sk)
+    v = mx.quantize(to_dev(vb), mx.ROW, sk)
+    do_t = to_dev(dob)
+    dmx = mx.quantize(do_t, mx.SQ, sq)
+    got = mx.attention_bwd(q, k, v, dmx, to_dev(o_bits), do_t, lse_dev, sq, sk, scale, causal,
+                           opts=mx.AttnOpts(8.0, mx.P_SCALE_CONST))
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale,
+                            causal, True, 1)
+    check([host(t.float()).astype(np.float64) for t in got], ref, "constant P scale")
+
+
 def test_fwd_then_bwd_on_gpu(mx):
     # the path as a training step runs it: GPU forward output feeds the GPU backward
     import torch

@@ -180,6 +180,42 @@ def test_jagged_config_sampled_sequences(mx):
         grad_check([got[0][rq], got[1][rk], got[2][rk]], ref, f"jagged seq {i}")
 
 
+@pytest.mark.parametrize("kind", ["jagged", "uniform", "causal"])
+def test_long_kv_config_sampled_sequences(mx, kind):
+    # the long-key batches (16 sequences, H8, key lengths up to 16384): jagged
+    # and uniform keys behind 1024 queries per sequence, and causal jagged
+    # self-attention.  The whole batch runs on the GPU, forward and backward;
+    # the oracle recomputes every head of two sequences (the shortest key
+    # sequence and one drawn at random), the backward from the oracle's O and lse
+    import torch
+    qb, kb, vb, dob, cu_q, cu_k, causal = inputs.long_kv_attn(kind)
+    lq, lk = cu_q[1:] - cu_q[:-1], cu_k[1:] - cu_k[:-1]
+    sq, sk = mx.Seqs.varlen(lq, "cuda"), mx.Seqs.varlen(lk, "cuda")
+    o, lse = gpu_fwd(mx, qb, kb, vb, sq, sk, SCALE, causal)
+    picks = sorted({int(np.argmin(lk)), int(np.random.default_rng(7).integers(len(lk)))})
+    if kind == "causal":  # keep the oracle's backward (lq x lk doubles per head) small
+        picks = sorted({int(np.argmin(lk)), int(np.argsort(lk)[1])})
+    o_bits = inputs.f32_to_bf16_bits(o.astype(np.float32))
+    lse_all = lse.copy()
+    fwd_ref = {}
+    for i in picks:
+        rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
+        oo, lo, ob, obf, lo32 = oracle_fwd_full(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), None, None,
+                                                causal)
+        fwd_check(o[rq], lse[:, rq], oo, lo)
+        fwd_ref[i] = (obf, lo32)
+        o_bits[rq] = ob
+        lse_all[:, rq] = lo32
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, torch.from_numpy(lse_all.astype(np.float32)).cuda(),
+                  sq, sk, SCALE, causal)
+    for i in picks:
+        rq, rk = slice(cu_q[i], cu_q[i + 1]), slice(cu_k[i], cu_k[i + 1])
+        obf, lo32 = fwd_ref[i]
+        ref = oracle.method_bwd(f64(qb[rq]), f64(kb[rk]), f64(vb[rk]), f64(dob[rq]), obf, lo32, None,
+                                None, SCALE, causal, True)
+        grad_check([got[0][rq], got[1][rk], got[2][rk]], ref, f"long-kv {kind} seq {i}")
+
+
 def _fused_chain(mx, x, g, dob, B, S, H):
     """RMSNorm+Quantize on the GPU, then causal self-attention forward and
     backward on its outputs: the 1x32 row layout is Q and K of the forward

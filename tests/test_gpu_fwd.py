@@ -115,6 +115,44 @@ def test_fwd_varlen_empty_sequences(mx, causal):
     check(o[~empty], lse[:, ~empty], oo[~empty], lo[:, ~empty])
 
 
+@pytest.mark.parametrize("thr,p_scale,varlen", [
+    (0.0, 0, False),   # exact rescale at every increase of the running max
+    (4.0, 0, True),
+    (8.0, 1, False),   # constant P scale with the default threshold
+    (0.0, 1, True),
+    (2.5, 1, False),   # a non-integer threshold: constant exponent ceil(2.5) - 8
+])
+def test_fwd_options(mx, thr, p_scale, varlen):
+    # the rescale threshold and the P scale mode against the oracle run with
+    # the same options
+    H, D = 2, 128
+    scale = 1 / math.sqrt(D)
+    if varlen:
+        lens = [64, 300, 7, 129, 1, 255]
+        qb, kb, vb, _, cu, _ = inputs.varlen_attn(lens, lens, H, D, seed=61)
+        seqs = mx.Seqs.varlen(lens, "cuda")
+    else:
+        B, S = 2, 384
+        qb, kb, vb, _ = (b.reshape(B * S, H, D) for b in inputs.dense_attn(B, H, S, D, seed=62))
+        cu = np.arange(0, (B + 1) * S, S, dtype=np.int32)
+        seqs = mx.Seqs.dense(B, S)
+    import torch
+    opts = mx.AttnOpts(thr, p_scale)
+    q = mx.quantize(to_dev(qb), mx.ROW, seqs)
+    k = mx.quantize(to_dev(kb), mx.ROW, seqs)
+    v = mx.quantize(to_dev(vb), mx.COL, seqs)
+    o, lse = mx.attention_fwd(q, k, v, seqs, seqs, scale, True, opts=opts)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    oo, lo = oracle.method_fwd(f64(qb), f64(kb), f64(vb), cu, cu, scale, True, True, 128, thr,
+                               p_scale)
+    og = host(o.float()).astype(np.float64)
+    lg = host(lse)
+    if not varlen:
+        lg = lg.reshape(2, H, 384).transpose(1, 0, 2).reshape(H, -1)
+    check(og, lg, oo, lo)
+
+
 @pytest.mark.parametrize("outliers_v", [False, True])
 def test_fwd_outliers_small(mx, outliers_v):
     # the outlier recipe (1% of Q/K channels x20, 0.1% of elements x200);

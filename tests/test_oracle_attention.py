@@ -261,6 +261,65 @@ def test_bwd_quantized_close_to_exact():
         assert 1e-3 < rel < 0.15
 
 
+# ----------------------------------------------------- constant P scale mode
+def _one_hot_fwd(p_scale, lazy_thr):
+    # one query (q = 1), 64 keys with scores s'_j = k_j (scale ln 2 makes
+    # scale * log2 e = 1 exactly), V_j = e_j so that O_j = P^_j / l
+    keys = np.full(64, -40.0)
+    keys[0] = 0.0                        # block 0: P~ = 1 (the row maximum)
+    keys[1:32] = -30.0
+    keys[32], keys[33], keys[34] = -10.0, -18.0, -11.0   # block 1: max 2^-10
+    v = np.eye(64).reshape(64, 1, 64)
+    qq = np.zeros((1, 1, 64)); qq[0, 0, 0] = 1.0
+    kk = np.zeros((64, 1, 64)); kk[:, 0, 0] = keys
+    o, lse = oracle.attn_fwd(qq, kk, v, np.array([0, 1], np.int32), np.array([0, 64], np.int32),
+                             math.log(2.0), False, True, 128, lazy_thr, p_scale)
+    l = 1 + 31 * 2.0 ** -30 + 2.0 ** -10 + 2.0 ** -18 + 2.0 ** -11 + 29 * 2.0 ** -40
+    return o[0, 0] * l
+
+
+def test_constant_p_scale_forward_worked_example():
+    # dynamic block scales: block 1 (max 2^-10) takes 2^-18, so 2^-18 is kept
+    # exactly; the constant scale (exact rescale, threshold 0 -> 2^-8) puts
+    # 2^-18 at 2^-10 on the E4M3 grid, half the smallest subnormal 2^-9: a tie
+    # that rounds to the even code 0.  2^-10 -> 0.25 and 2^-11 -> 0.125 stay exact.
+    pd = _one_hot_fwd(0, 0.0)
+    pc = _one_hot_fwd(1, 0.0)
+    for p in (pd, pc):
+        assert abs(p[0] - 1.0) < 1e-15
+        assert abs(p[32] - 2.0 ** -10) < 1e-18 and abs(p[34] - 2.0 ** -11) < 1e-18
+        assert np.all(np.abs(p[1:32]) < 1e-20)   # 2^-30 flushes in both modes
+    assert abs(pd[33] - 2.0 ** -18) < 1e-20
+    assert pc[33] == 0.0
+    # the lazy threshold 8 makes the constant exponent 0 (the largest possible
+    # P~ = 2^8 -> 256): 2^-10 is then half the smallest E4M3 step 2^-9, a tie
+    # to the even code 0, and 2^-11, 2^-18 lie below it -- block 1 vanishes
+    p8 = _one_hot_fwd(1, 8.0)
+    assert abs(p8[0] - 1.0) < 1e-15
+    assert p8[32] == 0.0 and p8[33] == 0.0 and p8[34] == 0.0
+
+
+def test_constant_p_scale_backward_worked_example():
+    # one key (S = 0), 32 queries with lse_i chosen so that P_i = exp(-lse_i):
+    # P = (2^-10, 2^-19, rest 2^-10); dO_i = e_i so that dV[i] = P^_i.  The
+    # dynamic block scale 2^-18 keeps 2^-19 (0.5 on the E4M3 grid); the
+    # constant scale 2^-8 puts it at 2^-11, below half of 2^-9: zero
+    L = 32
+    q = np.zeros((L, 1, 1)); k = np.zeros((1, 1, 1))
+    v = np.zeros((1, 1, L)); do = np.eye(L).reshape(L, 1, L)
+    o = np.zeros((L, 1, L))
+    p = np.full(L, 2.0 ** -10); p[1] = 2.0 ** -19
+    lse = (-np.log(p)).reshape(1, L)
+    cq, ck = np.array([0, L], np.int32), np.array([0, 1], np.int32)
+    qd = np.zeros((L, 1, L)); kd = np.zeros((1, 1, L))
+    _, _, dv_d = oracle.attn_bwd(qd, kd, v, do, o, do, lse, cq, ck, 1.0, False, True, False, 0)
+    _, _, dv_c = oracle.attn_bwd(qd, kd, v, do, o, do, lse, cq, ck, 1.0, False, True, False, 1)
+    np.testing.assert_allclose(dv_d[0, 0, 1], 2.0 ** -19, rtol=1e-12)
+    assert dv_c[0, 0, 1] == 0.0
+    np.testing.assert_allclose(dv_c[0, 0, [0, 2, 31]], 2.0 ** -10, rtol=1e-12)
+    np.testing.assert_allclose(dv_d[0, 0, [0, 2, 31]], 2.0 ** -10, rtol=1e-12)
+
+
 def test_backward_p_clamped_at_one():
     # One query, three keys, D = 1, scale 1: S = (2, 0.5, -1) with lse = 1
     # given (smaller than the first score, as a recompute from other operands
