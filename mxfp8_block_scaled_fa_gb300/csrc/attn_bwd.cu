@@ -100,12 +100,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   int L;
   seq_info(a.sq, g, s0, L);
   if (t * QT >= L) return;
-  const int64_t t128 = seq_units_before(a.sq, g, 128) + t / 2;
+  const int64_t t128 = seq_units_before_warp(a.sq, g, 128, threadIdx.x & 31) + t / 2;
   if (t128 >= a.ptiles_q) {
     atomicOr(&g_status_bwd, DEV_BAD_INDEX);
     return;
   }
-  uint8_t* rec = a.rec + ((seq_units_before(a.sq, g, QT) + t) * a.H + h) * REC_BYTES;
+  uint8_t* rec = a.rec + ((seq_units_before_warp(a.sq, g, QT, threadIdx.x & 31) + t) * a.H + h) * REC_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* ndelta = reinterpret_cast<float*>(rec + REC_NDELTA);
   for (int r = warp * 8; r < warp * 8 + 8; r++) {
@@ -291,9 +291,9 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
   const int nq = (lq + QT - 1) / QT;
   const int first = a.causal ? min(nq, (kt * KT) / QT) : 0;
   const int ntile = nq - first;
-  const int64_t tq_base = seq_units_before(a.sq, g, 128);
-  const int64_t tq64 = seq_units_before(a.sq, g, QT);  // first tile record of this sequence
-  const int64_t tk = seq_units_before(a.sk, g, 128) + kt;
+  const int64_t tq_base = seq_units_before_warp(a.sq, g, 128, lane);
+  const int64_t tq64 = seq_units_before_warp(a.sq, g, QT, lane);  // first tile record of this sequence
+  const int64_t tk = seq_units_before_warp(a.sk, g, 128, lane) + kt;
 
   const uint32_t bar0 = base + OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         if (kvalid && sfc != nullptr) *reinterpret_cast<uint32_t*>(sfc + (tok * a.H + h) * 4) = sfw;
         // packed ROW atom of this key tile; rows past the sequence hold 0x7F
         if (sfp != nullptr) {
-          const int64_t tile = seq_units_before(a.sk, g, 128) + kt;
+          const int64_t tile = seq_units_before_warp(a.sk, g, 128, lane) + kt;
           *reinterpret_cast<uint32_t*>(sfp + (tile * a.H + h) * 512 + (r & 31) * 16 + (r >> 5) * 4) =
               kvalid ? sfw : 0x7F7F7F7Fu;
         }

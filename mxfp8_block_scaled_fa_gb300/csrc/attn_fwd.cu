@@ -126,8 +126,10 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
   const int nkv_a = a.causal ? min(nkv_all, 2 * qp + 1) : nkv_all;
   const int nkv_b = !has_b ? 0 : a.causal ? min(nkv_all, 2 * qp + 2) : nkv_all;
   const int nkv_max = max(nkv_a, nkv_b);
-  const int64_t tq_g = seq_units_before(a.sq, g, TILE) + 2 * qp;  // packed tile of Q_A
-  const int64_t tk_g0 = seq_units_before(a.sk, g, TILE);
+  // packed tiles of Q_A and of key tile 0 (every thread of the CTA is here:
+  // each warp sums the sequences' tile counts across its lanes)
+  const int64_t tq_g = seq_units_before_warp(a.sq, g, TILE, lane) + 2 * qp;
+  const int64_t tk_g0 = seq_units_before_warp(a.sk, g, TILE, lane);
 
   const uint32_t bar0 = base + OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
           *reinterpret_cast<uint32_t*>(a.omx_sfc + (tok * a.H + h) * 4) = sfw;
         // packed ROW atom of this query tile; rows past the sequence hold 0x7F
         if (a.omx_sfp != nullptr) {
-          const int64_t tile = seq_units_before(a.sq, g, TILE) + 2 * qp + x;
+          const int64_t tile = tq_g + x;
           *reinterpret_cast<uint32_t*>(a.omx_sfp + (tile * a.H + h) * 512 + (row & 31) * 16 + (row >> 5) * 4) =
               valid ? sfw : 0x7F7F7F7Fu;
         }

@@ -22,11 +22,24 @@ __device__ __forceinline__ int64_t seq_units_before(const Seqs& s, int g, int gr
   if (!s.cu) return int64_t(g) * ((s.seqlen + gran - 1) / gran);
   int64_t acc = 0;
   int prev = __ldg(s.cu);
+#pragma unroll 8
   for (int i = 0; i < g; i++) {
     int nx = __ldg(s.cu + i + 1);
     acc += (nx - prev + gran - 1) / gran;
     prev = nx;
   }
+  return acc;
+}
+
+// seq_units_before computed by a whole (converged) warp: lane l sums the
+// sequences l, l + 32, ... and a butterfly adds the lanes' sums.  Every lane
+// returns the total.
+__device__ __forceinline__ int64_t seq_units_before_warp(const Seqs& s, int g, int gran, int lane) {
+  if (!s.cu) return int64_t(g) * ((s.seqlen + gran - 1) / gran);
+  long long acc = 0;
+  for (int i = lane; i < g; i += 32) acc += (__ldg(s.cu + i + 1) - __ldg(s.cu + i) + gran - 1) / gran;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
   return acc;
 }
 

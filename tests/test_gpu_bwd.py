@@ -69,6 +69,7 @@ def check(got, ref, tag=""):
     (2, 2, 300, True, 0, 1.0),      # ragged tail in both key and query tiles
     (2, 3, 300, False, 1, 4.0),
     (1, 1, 33, False, 0, 1.0),
+    (4, 20, 1000, True, 0, 1.0),    # more work items than SMs
 ])
 def test_bwd_dense(mx, B, H, S, causal, dq_mode, dq_static):
     import torch

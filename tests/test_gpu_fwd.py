@@ -68,6 +68,8 @@ def check(o, lse, oo, lo):
     (1, 1, 1, False),       # single key
     (1, 2, 33, True),
     (3, 2, 640, True),      # several tiles per head, more than the K/V ring
+    (4, 20, 1000, True),    # more work items than SMs: a CTA walks several items
+    (2, 40, 768, False),
 ])
 def test_fwd_dense(mx, B, H, S, causal):
     D = 128
