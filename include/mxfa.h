@@ -143,6 +143,18 @@ mxfa_status mxfa_quantize(const void* x, int64_t tokens, int H, int D, mxfa_bloc
                           const int32_t* cu_seqlens, int nseq, int max_seqlen,
                           int64_t packed_tiles, const mxfa_mx_out* out, mxfa_stream_t stream);
 
+/* mxfa_quantize_dual -- one read of x, two layouts: blk (MXFA_BLK_COL or
+ * MXFA_BLK_SQ) into out, and MXFA_BLK_ROW into out_row, each byte for byte as
+ * mxfa_quantize would write it ([ITEMS] item 7: quantization fused so that no
+ * separate pass reads the tensor again).  COL + ROW serves V (forward, then
+ * backward); SQ + ROW serves Q and K (backward, then forward).  Arguments as
+ * mxfa_quantize; out_row and its payload are required, its scale pointers
+ * nullable; another blk is MXFA_ERR_INVALID_ARG. */
+mxfa_status mxfa_quantize_dual(const void* x, int64_t tokens, int H, int D, mxfa_block blk,
+                               const int32_t* cu_seqlens, int nseq, int max_seqlen,
+                               int64_t packed_tiles, const mxfa_mx_out* out,
+                               const mxfa_mx_out* out_row, mxfa_stream_t stream);
+
 /* mxfa_sf_pack -- compact scales -> packed scales for the same block kind,
  * values unchanged, padding rows 0x7F ([KDIM] paragraph 3, [ITEMS] item 5:
  * only the scale factors are scattered and padded; payload stays compact).

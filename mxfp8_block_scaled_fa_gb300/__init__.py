@@ -14,7 +14,7 @@ def __getattr__(name):
                                             "Mx", "MxIn", "MxOut", "Seqs", "ROW", "COL", "SQ",
                                             "AttnOpts", "P_SCALE_BLOCK", "P_SCALE_CONST",
                                             "RESCALE_THRESHOLD",
-                                            "quantize", "sf_pack", "sf_unpack", "attention_fwd",
+                                            "quantize", "quantize_dual", "sf_pack", "sf_unpack", "attention_fwd",
                                             "attention_bwd", "rmsnorm_quant", "gemm_quant",
                                             "device_status"):
         from . import mxfa as _m

@@ -312,6 +312,7 @@ mxfa_status mxfa_quantize(const void* x, int64_t tokens, int H, int D, mxfa_bloc
   if (!aligned16(x) || !aligned16(out->data)) return MXFA_ERR_MISALIGNED;
   if (out->sf_packed && packed_tiles <= 0) return MXFA_ERR_INVALID_ARG;
   QuantArgs a;
+  memset(&a, 0, sizeof(a));
   a.x = static_cast<const uint16_t*>(x);
   a.tokens = tokens;
   a.H = H;
@@ -322,6 +323,35 @@ mxfa_status mxfa_quantize(const void* x, int64_t tokens, int H, int D, mxfa_bloc
   a.data = out->data;
   a.sf_compact = out->sf_compact;
   a.sf_packed = out->sf_packed;
+  if (tokens == 0) return MXFA_OK;
+  return from_cuda(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mxfa_status mxfa_quantize_dual(const void* x, int64_t tokens, int H, int D, mxfa_block blk,
+                               const int32_t* cu, int nseq, int max_seqlen, int64_t packed_tiles,
+                               const mxfa_mx_out* out, const mxfa_mx_out* out_row, mxfa_stream_t stream) {
+  if (!x || !out || !out->data || !out_row || !out_row->data || H <= 0) return MXFA_ERR_INVALID_ARG;
+  if (blk != MXFA_BLK_COL && blk != MXFA_BLK_SQ) return MXFA_ERR_INVALID_ARG;
+  if (D != 128) return MXFA_ERR_UNSUPPORTED;
+  mxfa_status s = check_seqs(cu, nseq, max_seqlen, tokens);
+  if (s) return s;
+  if (!aligned16(x) || !aligned16(out->data) || !aligned16(out_row->data)) return MXFA_ERR_MISALIGNED;
+  if ((out->sf_packed || out_row->sf_packed) && packed_tiles <= 0) return MXFA_ERR_INVALID_ARG;
+  QuantArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const uint16_t*>(x);
+  a.tokens = tokens;
+  a.H = H;
+  a.D = D;
+  a.mode = int(blk);
+  a.seq = Seqs{cu, nseq, max_seqlen};
+  a.packed_tiles = packed_tiles;
+  a.data = out->data;
+  a.sf_compact = out->sf_compact;
+  a.sf_packed = out->sf_packed;
+  a.row_data = out_row->data;
+  a.row_sfc = out_row->sf_compact;
+  a.row_sfp = out_row->sf_packed;
   if (tokens == 0) return MXFA_OK;
   return from_cuda(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }

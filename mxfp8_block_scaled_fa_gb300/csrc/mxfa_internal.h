@@ -53,6 +53,11 @@ struct QuantArgs {
   uint8_t* data;
   uint8_t* sf_compact;  // nullable
   uint8_t* sf_packed;   // nullable
+  // modes 1 and 2 only, nullable: the same input also quantized ROW (1x32
+  // along D) from the same read -- payload, compact and packed scales
+  uint8_t* row_data;
+  uint8_t* row_sfc;
+  uint8_t* row_sfp;
 };
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 

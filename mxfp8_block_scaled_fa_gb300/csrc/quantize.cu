@@ -126,6 +126,10 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
     } else {
       if (lead) a.sf_packed[(tile_g * a.H + h) * 16 + kb4 * 4 + dcol / 32] = 0x7F;
     }
+    if (a.row_sfp && lead) {
+      uint8_t* base = a.row_sfp + (tile_g * a.H + h) * 512;
+      for (int r = 0; r < 32; r++) base[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
+    }
     return;
   }
 
@@ -158,8 +162,9 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
       }
     } else {
       uint32_t m = max(max(hmax2(cm[0]), hmax2(cm[1])), max(hmax2(cm[2]), hmax2(cm[3])));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const unsigned quad = __activemask();  // whole lane quads are active together
+      m = max(m, __shfl_xor_sync(quad, m, 1));
+      m = max(m, __shfl_xor_sync(quad, m, 2));
       uint32_t sb = e8m0_from_bf16abs(m);
 #pragma unroll
       for (int i = 0; i < 8; i++) s[i] = sb;
@@ -197,6 +202,39 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
       if (a.sf_compact) a.sf_compact[b32 * (cols / 32) + col0 / 32] = uint8_t(s[0]);
       if (a.sf_packed) a.sf_packed[(tile_g * a.H + h) * 16 + kb4 * 4 + dcol / 32] = uint8_t(s[0]);
     }
+  }
+  if (MODE != 0 && a.row_data) {
+    // the same rows in 1x32 blocks along D: a row's 32-column block spans the
+    // four threads of this lane quad (8 columns each), so its maximum takes
+    // two butterfly steps
+    uint8_t* rpk = a.row_sfp ? a.row_sfp + (tile_g * a.H + h) * 512 : nullptr;
+    const unsigned quad = __activemask();  // whole lane quads are active together
+#pragma unroll
+    for (int r = 0; r < 32; r++) {
+      uint32_t m = max(max(hmax2(abs2(v[r].x)), hmax2(abs2(v[r].y))), max(hmax2(abs2(v[r].z)), hmax2(abs2(v[r].w))));
+      m = max(m, __shfl_xor_sync(quad, m, 1));
+      m = max(m, __shfl_xor_sync(quad, m, 2));
+      if (r >= nr) continue;
+      const uint32_t sc = e8m0_from_bf16abs(m);
+      uint2 out;
+      if (sc == 0xFFu) {
+        out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      } else {
+        float inv[8];
+        const float f = e8m0_inv_scale(sc);
+#pragma unroll
+        for (int i = 0; i < 8; i++) inv[i] = f;
+        out = cvt8(v[r], inv);
+      }
+      *reinterpret_cast<uint2*>(a.row_data + (r0 + r) * cols + col0) = out;
+      if (lead) {
+        if (a.row_sfc) a.row_sfc[(r0 + r) * (cols / 32) + col0 / 32] = uint8_t(sc);
+        if (rpk) rpk[atom_off(kb4 * 32 + r, dcol / 32)] = uint8_t(sc);
+      }
+    }
+    // rows past the sequence in this block: padding scales of the packed atom
+    if (rpk && lead)
+      for (int r = nr; r < 32; r++) rpk[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
   }
 }
 

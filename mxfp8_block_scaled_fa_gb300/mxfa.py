@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "mxfa_sf_packed_bytes": (S, [I, I64, I]),
             "mxfa_quantize": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
             "mxfa_sf_pack": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
+            "mxfa_quantize_dual": (I, [P, I64, I, I, I, P, I, I, I64, P, P, P]),
             "mxfa_sf_unpack": (I, [P, I64, I, I, I, P, I, I, I64, P, P]),
             "mxfa_fwd": (I, [P, P, P, I, I, I, I, F, I, P, P, P]),
             "mxfa_varlen_fwd": (I, [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, I, F, I, P, P,
@@ -301,6 +302,31 @@ def quantize(x: torch.Tensor, blk: int, seqs: Seqs, compact=True, packed=True,
     mxfa_quantize(x3, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len, seqs.ptiles,
                   out, stream)
     return Mx(data, sfc, sfp, blk)
+
+
+def mxfa_quantize_dual(x, tokens, H, D, blk, cu_seqlens, nseq, max_seqlen, packed_tiles,
+                       out: MxOut, out_row: MxOut, stream=None):
+    _check(lib().mxfa_quantize_dual(_p(x), tokens, H, D, blk, _p(cu_seqlens), nseq, max_seqlen,
+                                    packed_tiles, ctypes.byref(out), ctypes.byref(out_row),
+                                    _stream(stream)), "mxfa_quantize_dual")
+
+
+def quantize_dual(x: torch.Tensor, blk: int, seqs: Seqs, stream=None):
+    """bf16 [tokens, H, D] -> (Mx in layout blk (COL or SQ), Mx in ROW) from one read."""
+    H, D = x.shape[-2], x.shape[-1]
+    x3 = x.reshape(-1, H, D)
+    dev = x.device
+    outs, structs = [], []
+    for b in (blk, ROW):
+        data = torch.empty(x3.shape, dtype=torch.uint8, device=dev)
+        comp_shape, pbytes = _sf_shapes(b, seqs, H, D)
+        sfc = torch.empty(comp_shape, dtype=torch.uint8, device=dev)
+        sfp = torch.empty(max(pbytes, 16), dtype=torch.uint8, device=dev)
+        outs.append(Mx(data, sfc, sfp, b))
+        structs.append(MxOut(data.data_ptr(), sfc.data_ptr(), sfp.data_ptr()))
+    mxfa_quantize_dual(x3, seqs.total, H, D, blk, seqs.cu_dev, seqs.nseq, seqs.max_len, seqs.ptiles,
+                       structs[0], structs[1], stream)
+    return outs[0], outs[1]
 
 
 def sf_pack(sf_compact: torch.Tensor, blk: int, seqs: Seqs, H: int, D: int = 128,

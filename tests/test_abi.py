@@ -85,6 +85,16 @@ def test_sf_unpack_argument_checks(lib):
     assert u(0x3000, 255, 2, 128, 0, None, 1, 256, 2, 0x2000, None) == 1    # tokens != nseq*len
 
 
+def test_quantize_dual_argument_checks(lib):
+    q = lib.mxfa_quantize_dual
+    o, o2 = _out(), _out(data=0x4000)
+    ref = ctypes.byref
+    assert q(0x1000, 256, 2, 128, 0, None, 1, 256, 2, ref(o), ref(o2), None) == 1    # ROW first
+    assert q(0x1000, 256, 2, 128, 1, None, 1, 256, 2, ref(o), None, None) == 1       # no ROW output
+    assert q(0x1000, 256, 2, 64, 2, None, 1, 256, 2, ref(o), ref(o2), None) == 2     # D != 128
+    assert q(0x1000, 256, 2, 128, 2, None, 1, 256, 2, ref(o), ref(_out(data=0x4004)), None) == 3
+
+
 def test_noalloc_argument_checks(lib):
     # the no-allocation backward validates like mxfa_bwd before it looks at
     # the size of its scratch array or touches a device

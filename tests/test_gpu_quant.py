@@ -50,6 +50,45 @@ def _check_quant(mx, bits3, lens, H, blk):
     np.testing.assert_array_equal(host(comp2), s_ref)
 
 
+def _check_dual(mx, bits3, lens, H, blk):
+    # one read, two layouts: blk (COL or SQ) and ROW, each equal to the
+    # oracle's quantization of the same bf16 tensor, compact and packed
+    import torch
+    tokens = bits3.shape[0]
+    seqs = mx.Seqs.varlen(lens, "cuda") if lens is not None else mx.Seqs.dense(1, tokens)
+    lens_ = lens if lens is not None else [tokens]
+    cu = seqs.cu_host
+    first, row = mx.quantize_dual(to_dev(bits3), blk, seqs)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for m, b in ((first, blk), (row, mx.ROW)):
+        q_ref, s_ref = oracle.quantize(f64(bits3).reshape(tokens, -1), b, cu)
+        np.testing.assert_array_equal(host(m.data).reshape(tokens, -1), q_ref, err_msg=str(b))
+        np.testing.assert_array_equal(host(m.sf_compact), s_ref, err_msg=str(b))
+        comp, pad = unpack_packed(host(m.sf_packed), b, lens_, H)
+        np.testing.assert_array_equal(comp, s_ref, err_msg=str(b))
+        assert np.all(pad == 0x7F), b
+
+
+@pytest.mark.parametrize("blk", [1, 2])
+@pytest.mark.parametrize("case", ["dense", "ragged", "empty", "odd_heads"])
+def test_quantize_dual(mx, blk, case):
+    if case == "dense":
+        q, _, _, _ = inputs.dense_attn(2, 2, 384, 128, seed=7)
+        _check_dual(mx, q.reshape(768, 2, 128), None, 2, blk)
+    elif case == "ragged":
+        lens = [5, 130, 64, 33, 1, 257]
+        q, _, _, _, _, _ = inputs.varlen_attn(lens, lens, 3, 128, seed=8)
+        _check_dual(mx, q, lens, 3, blk)
+    elif case == "empty":
+        lens = [0, 40, 0, 129, 0]
+        q, _, _, _, _, _ = inputs.varlen_attn(lens, lens, 2, 128, seed=9)
+        _check_dual(mx, q, lens, 2, blk)
+    else:  # 5 heads: the last warp of a column block is partly idle
+        q, _, _, _ = inputs.dense_attn(1, 5, 160, 128, seed=10, outliers=True)
+        _check_dual(mx, q.reshape(160, 5, 128), None, 5, blk)
+
+
 @pytest.mark.parametrize("blk,name", MODES)
 def test_quantize_tiny_dense(mx, blk, name):
     q, _, _, _ = inputs.dense_attn(1, 2, 256, 128, seed=0)
