@@ -234,7 +234,7 @@ mxfa_status mxfa_varlen_fwd_opts(const mxfa_mx* q, const mxfa_mx* k, const mxfa_
 
 /* Workspace of the backward pass for total_q query tokens in nseq sequences:
  * one 2560-byte record per (64-query tile, head) -- the tile's scale atoms,
- * lse * log2(e) and Delta = rowsum(dO * O) -- for at most
+ * lse * log2(e) and Delta = rowsum(dO^ * O) -- for at most
  * ceil(total_q / 64) + nseq tiles, followed by the dQ accumulator
  * ([total_q][H][128], fp32 when dq_mode = 0, fp16 when 1). */
 size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_mode);
@@ -243,7 +243,10 @@ size_t mxfa_bwd_workspace_size(int64_t total_q, int nseq, int H, int D, int dq_m
  *  q, k, dO   SQ-quantized payload + packed SQ scales (32x32 blocks serve
  *             both GEMM orientations)
  *  v          ROW-quantized payload + packed ROW scales
- *  o, dout    bf16 O and dO [B][S][H][128];  lse fp32 [B][H][S] from mxfa_fwd
+ *  o, dout    bf16 O and dO [B][S][H][128];  lse fp32 [B][H][S] from mxfa_fwd.
+ *             Delta = rowsum(dO^ * O) takes the dequantized square-block dO^
+ *             of dout_mx (the operand that also enters dP), so dout itself
+ *             is checked but not read
  *  dq_mode    0: dQ reduced in fp32;  1: fp16 with static scale
  *             dq_static_scale (a power of two; partials are multiplied by it
  *             before the fp16 reduction and divided after)

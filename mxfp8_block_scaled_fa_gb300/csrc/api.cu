@@ -222,6 +222,7 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   a.sfk = k->sf;
   a.sfv = v->sf;
   a.sfdo = dmx->sf;
+  a.do_q = dmx->data;
   a.o = static_cast<const uint16_t*>(o);
   a.dout = static_cast<const uint16_t*>(dout);
   a.lse = lse;

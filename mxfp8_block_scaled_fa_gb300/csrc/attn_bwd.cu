@@ -87,7 +87,9 @@ constexpr int NTHREADS = 512;
 
 // ------------------------------------------------------------ pre / post
 // Tile records.  One CTA (256 threads) per (64-query tile of a sequence, head):
-//   -Delta[r] with Delta[r] = sum_d dO[r,d] * O[r,d] (fp32 from bf16, warp per row),
+//   -Delta[r] with Delta[r] = sum_d dO^[r,d] * O[r,d] (fp32, warp per row), dO^
+//   the dequantized 32x32-block dO that also enters dP = dO^ V^, so that
+//   dS = P (dP - Delta) cancels consistently on peaked softmax rows,
 //   -lse[r] * log2(e)  (-inf past the sequence end: P = 2^-inf = 0),
 //   the four scale atoms of the tile built from the packed square scales of
 //   Q and dO: rows = queries (for S^T and dP^T) and rows = d (for dK and dV).
@@ -107,6 +109,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   }
   uint8_t* rec = a.rec + ((seq_units_before_warp(a.sq, g, QT, threadIdx.x & 31) + t) * a.H + h) * REC_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + (t128 * a.H + h) * 16));
+  const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + (t128 * a.H + h) * 16));
+  auto pick = [](uint4 e, int tb) { return tb == 0 ? e.x : tb == 1 ? e.y : tb == 2 ? e.z : e.w; };
+  const int tb0 = (t & 1) * 2;
   float* ndelta = reinterpret_cast<float*>(rec + REC_NDELTA);
   for (int r = warp * 8; r < warp * 8 + 8; r++) {
     const int q = t * QT + r;
@@ -114,10 +120,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
     if (q < L) {
       const int64_t off = ((s0 + q) * a.H + h) * 128 + lane * 4;
       const uint2 ov = *reinterpret_cast<const uint2*>(a.o + off);
-      const uint2 dv = *reinterpret_cast<const uint2*>(a.dout + off);
+      // dO^ of these four columns: E4M3 codes times the 32x32 block scale of
+      // (query block tb0 + r / 32, d block lane / 8)
+      const uint32_t dq4 = *reinterpret_cast<const uint32_t*>(a.do_q + off);
+      const uint32_t sb = (pick(d4, tb0 + (r >> 5)) >> (8 * (lane >> 3))) & 0xFFu;
+      const float f = e8m0_value(sb);
+      const float2 d01 = e4m3x2_to_float2(dq4 & 0xFFFFu), d23 = e4m3x2_to_float2(dq4 >> 16);
       auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
       auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-      d = lo(ov.x) * lo(dv.x) + hi(ov.x) * hi(dv.x) + lo(ov.y) * lo(dv.y) + hi(ov.y) * hi(dv.y);
+      d = lo(ov.x) * (d01.x * f) + hi(ov.x) * (d01.y * f) + lo(ov.y) * (d23.x * f) + hi(ov.y) * (d23.y * f);
 #pragma unroll
       for (int off2 = 16; off2 >= 1; off2 >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off2);
     }
@@ -133,10 +144,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
     }
     reinterpret_cast<float*>(rec + REC_NL2)[tid] = nl2;
   }
-  const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(a.sfq + (t128 * a.H + h) * 16));
-  const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(a.sfdo + (t128 * a.H + h) * 16));
-  auto pick = [](uint4 e, int tb) { return tb == 0 ? e.x : tb == 1 ? e.y : tb == 2 ? e.z : e.w; };
-  const int tb0 = (t & 1) * 2;
   if (tid < 128) {
     const int w = tid, rg = w & 3;
     uint32_t* aq = reinterpret_cast<uint32_t*>(rec + REC_SFQ);

@@ -6,6 +6,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace mxfa {
@@ -414,6 +415,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
   return r;
+}
+// Two E4M3 codes (lo byte = first) -> their values as fp32 (exact).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(two_codes)));
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(hv);
 }
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);

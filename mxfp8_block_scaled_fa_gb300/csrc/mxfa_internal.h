@@ -120,6 +120,7 @@ struct BwdArgs {
   const uint8_t* sfdo;  // packed SQ
   const uint16_t* o;    // bf16
   const uint16_t* dout; // bf16
+  const uint8_t* do_q;  // dO's E4M3 payload (32x32 blocks; scales sfdo)
   const float* lse;
   Seqs sq, sk;
   int64_t total_q, total_k;

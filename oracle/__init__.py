@@ -192,6 +192,8 @@ def attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal=False,
              quant_p=True, quant_ds=True, p_scale=0):
     """Backward on dequantized operands -> (dQ, dK, dV) float64 [tokens, H, D].
 
+    do enters dP; do_bf enters Delta = rowsum(do_bf * o_bf) (the method passes
+    the same dequantized dO for both, see method_bwd).
     p_scale=1: every P^T block takes the constant exponent -8."""
     lib = _load()
     q, k, v, do, o_bf, do_bf = (_c(a, np.float64) for a in (q, k, v, do, o_bf, do_bf))
@@ -223,7 +225,12 @@ def method_fwd(q_bf, k_bf, v_bf, cu_q, cu_k, scale, causal=False, quant=True,
 
 def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=False,
                quant=True, p_scale=0):
-    """Square-block Q, K, dO and row-block V, then the five-GEMM backward."""
+    """Square-block Q, K, dO and row-block V, then the five-GEMM backward.
+
+    Delta = rowsum(dO^ * O) takes the same dequantized dO^ that enters
+    dP = dO^ V^ (reading: the backward runs on the quantized operands, and
+    the identity sum_j P_ij dP_ij = dO_i . O_i that dS = P (dP - Delta)
+    relies on holds for one and the same dO)."""
     if quant:
         q = qdq(q_bf, SQ, cu_q)
         k = qdq(k_bf, SQ, cu_k)
@@ -231,7 +238,7 @@ def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=Fal
         v = qdq(v_bf, ROW, cu_k)
     else:
         q, k, do, v = q_bf, k_bf, do_bf, v_bf
-    return attn_bwd(q, k, v, do, o_bf, do_bf, lse, cu_q, cu_k, scale, causal,
+    return attn_bwd(q, k, v, do, o_bf, do, lse, cu_q, cu_k, scale, causal,
                     quant, quant, p_scale)
 
 

@@ -357,7 +357,9 @@ void mxo_attn_fwd(const double* q, const double* k, const double* v,
 /* ------------------------------------------------------------------ */
 
 /* q, k, dO are the dequantized square-block operands, v the dequantized
- * row-block operand; o_bf and do_bf are the bf16 O and dO (as fp64 values);
+ * row-block operand; o_bf is the bf16 O and do_bf the dO that enters Delta
+ * (the method passes the dequantized square-block dO, the one that also
+ * enters dP; as fp64 values);
  * lse[head][query token] from the forward pass.  Per sequence and head:
  *   Delta_i = sum_d dO_bf[i,d] * O_bf[i,d]
  *   P_ij = exp(min(q_i.k_j * scale - lse_i, 0))   (0 where masked; < 2^-126 -> 0)

@@ -267,9 +267,9 @@ def test_fused_chain_small(mx):
     fwd_check(o_gpu, lse_gpu, oo, lo)
     # the backward against the oracle's backward on the O (bf16) and lse
     # (fp32) that the GPU backward received
-    dof = f64(dob).reshape(T, H, D)
-    ref_g = oracle.attn_bwd(deq["sq"], deq["sq"], deq["row"], oracle.qdq(dof, 2, cu), o_gpu, dof,
-                            lse_gpu, cu, cu, SCALE, True, True, True)
+    dos = oracle.qdq(f64(dob).reshape(T, H, D), 2, cu)  # dO^ enters dP and Delta
+    ref_g = oracle.attn_bwd(deq["sq"], deq["sq"], deq["row"], dos, o_gpu, dos, lse_gpu, cu, cu, SCALE,
+                            True, True, True)
     grad_check([host(t.float()).astype(np.float64) for t in grads], ref_g, "fused chain")
 
 
@@ -290,9 +290,8 @@ def test_fused_config_sampled_head(mx):
     o_gpu = host(o.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs]
     lse_gpu = host(lse).reshape(B, H, S)[b, hs].astype(np.float64)
     fwd_check(o_gpu, lse_gpu, oo, lo)
-    dof = f64(dob[b, :, hs, :])
-    ref_g = oracle.attn_bwd(qs, qs, q, oracle.qdq(dof, 2), o_gpu, dof, lse_gpu, None, None, SCALE,
-                            True, True, True)
+    dos = oracle.qdq(f64(dob[b, :, hs, :]), 2)  # dO^ enters dP and Delta
+    ref_g = oracle.attn_bwd(qs, qs, q, dos, o_gpu, dos, lse_gpu, None, None, SCALE, True, True, True)
     got = [host(t.float()).astype(np.float64).reshape(B, S, H, D)[b, :, hs] for t in grads]
     grad_check(got, ref_g, "fused config")
 

@@ -320,6 +320,29 @@ def test_constant_p_scale_backward_worked_example():
     np.testing.assert_allclose(dv_d[0, 0, [0, 2, 31]], 2.0 ** -10, rtol=1e-12)
 
 
+def test_delta_from_the_quantized_do():
+    # With a single key the softmax is the constant 1, so the exact gradients
+    # with respect to Q and K vanish.  The method keeps that exactly when
+    # Delta takes the same dequantized dO^ as dP: with V and O exact (small
+    # integers survive every block scale), dP = dO^ . V = dO^ . O = Delta and
+    # dS = 0.  Taking Delta from the bf16 dO instead (1 + 2^-6 rounds to 1 in
+    # E4M3) leaves dS = P (dO^ - dO) . V != 0.
+    D = 32
+    q = np.zeros((1, 1, D)); q[0, 0, :4] = [1.0, -2.0, 3.0, 1.0]
+    k = np.zeros((1, 1, D)); k[0, 0, :4] = [2.0, 1.0, -1.0, 4.0]
+    v = np.zeros((1, 1, D)); v[0, 0, :4] = [3.0, -1.0, 2.0, 1.0]
+    do = np.zeros((1, 1, D)); do[0, 0, :4] = 1.0 + 2.0 ** -6
+    o, lse = oracle.method_fwd(q, k, v, None, None, 0.25, False, True)
+    np.testing.assert_array_equal(o, v)   # one key: O = V exactly
+    dq, dk, dv = oracle.method_bwd(q, k, v, do, o, lse, None, None, 0.25, False, True)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    dos = oracle.qdq(do, 2)
+    assert dos[0, 0, 0] == 1.0
+    dq0, dk0, _ = oracle.attn_bwd(oracle.qdq(q, 2), oracle.qdq(k, 2), oracle.qdq(v, 0), dos, o, do, lse,
+                                  None, None, 0.25, False, True, True)
+    assert np.abs(dq0).max() > 0 and np.abs(dk0).max() > 0
+
+
 def test_backward_p_clamped_at_one():
     # One query, three keys, D = 1, scale 1: S = (2, 0.5, -1) with lse = 1
     # given (smaller than the first score, as a recompute from other operands
