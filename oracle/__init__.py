@@ -71,6 +71,16 @@ def _load():
             lib.mxo_rmsnorm_quant.restype = None
             lib.mxo_rmsnorm_quant.argtypes = [P, P, I64, I64, ctypes.c_float, I32,
                                               ctypes.c_int32, P, P, P, P, P, P, P]
+            lib.mxo_fp_decode.restype = D
+            lib.mxo_fp_decode.argtypes = [I32, ctypes.c_uint8]
+            lib.mxo_fp_encode.restype = ctypes.c_uint8
+            lib.mxo_fp_encode.argtypes = [I32, D]
+            lib.mxo_fp_max.restype = D
+            lib.mxo_fp_max.argtypes = [I32]
+            lib.mxo_quantize_mx.restype = None
+            lib.mxo_quantize_mx.argtypes = [P, I64, I64, I32, P, P]
+            lib.mxo_quantize_nvfp4.restype = D
+            lib.mxo_quantize_nvfp4.argtypes = [P, I64, I64, P, P]
             lib.mxo_gemm_nt.restype = None
             lib.mxo_gemm_nt.argtypes = [P, P, I64, I64, I64, P]
             lib.mxo_num_threads.restype = I32
@@ -240,6 +250,56 @@ def method_bwd(q_bf, k_bf, v_bf, do_bf, o_bf, lse, cu_q, cu_k, scale, causal=Fal
         q, k, do, v = q_bf, k_bf, do_bf, v_bf
     return attn_bwd(q, k, v, do, o_bf, do, lse, cu_q, cu_k, scale, causal,
                     quant, quant, p_scale)
+
+
+# ------------------------------------------ lower-precision element formats
+E2M1, E2M3, E3M2 = 0, 1, 2
+
+
+def fp_decode(fmt: int, codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.mxo_fp_decode(fmt, int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def fp_encode(fmt: int, vals) -> np.ndarray:
+    lib = _load()
+    v = np.asarray(vals, dtype=np.float64)
+    return np.array([lib.mxo_fp_encode(fmt, float(x)) for x in v.ravel()],
+                    dtype=np.uint8).reshape(v.shape)
+
+
+def fp_max(fmt: int) -> float:
+    return float(_load().mxo_fp_max(fmt))
+
+
+def quantize_mx(x2d, fmt: int):
+    """MXFP4 / MXFP6: x[rows, cols] -> (codes u8 [rows, cols] unpacked, E8M0 [rows, cols/32])."""
+    lib = _load()
+    x = _c(x2d, np.float64)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    sf = np.zeros((rows, cols // 32), np.uint8)
+    lib.mxo_quantize_mx(_ptr(x), rows, cols, fmt, _ptr(q), _ptr(sf))
+    return q, sf
+
+
+def dequantize_mx(q, sf, fmt: int) -> np.ndarray:
+    vals = fp_decode(fmt, np.arange(256, dtype=np.uint8) & (0x0F if fmt == E2M1 else 0x3F))
+    x = vals[np.asarray(q)]
+    return x * np.ldexp(1.0, np.repeat(np.asarray(sf, np.int64), 32, axis=1) - 127)
+
+
+def quantize_nvfp4(x2d):
+    """NVFP4: x[rows, cols] -> (E2M1 codes u8 [rows, cols], E4M3 scales [rows, cols/16],
+    fp32 tensor scale)."""
+    lib = _load()
+    x = _c(x2d, np.float64)
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    sf = np.zeros((rows, cols // 16), np.uint8)
+    st = lib.mxo_quantize_nvfp4(_ptr(x), rows, cols, _ptr(q), _ptr(sf))
+    return q, sf, st
 
 
 # ------------------------------------------------------- GEMM+Quantize

@@ -410,14 +410,16 @@ void mxo_attn_bwd(const double* q, const double* k, const double* v,
           dS[i * lk + j] = p * (dp - delta);
         }
       }
-      if (quant_p) /* 1x32 along queries, for every key column */
+      if (quant_p) { /* 1x32 along queries, for every key column */
 #pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < lk; j++)
-          for (int64_t ib = 0; ib < lq; ib += 32)
+          for (int64_t ib = 0; ib < lq; ib += 32) {
             if (p_scale)
               qdq_block_fixed(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk, -8);
             else
               qdq_block(P + ib * lk + j, lq - ib < 32 ? lq - ib : 32, lk);
+          }
+      }
       if (quant_ds) /* 32x32 square blocks */
 #pragma omp parallel for schedule(static)
         for (int64_t ib = 0; ib < lq; ib += 32)
@@ -536,6 +538,144 @@ void mxo_rmsnorm_quant(const float* x, const float* gamma, int64_t T, int64_t C,
   if (out_mask & 4) mxo_quantize(y, T, C, MXO_SQ, cu, nseg, q_sq, sf_sq);
   free(cu);
   free(y);
+}
+
+/* ------------------------------------------------------------------ */
+/* Lower-precision element formats (MXFP6, MXFP4, NVFP4): the formats the */
+/* pages name as the next step ("Meta's FlashAttention-4 Achieves 2.85   */
+/* PF/s with MXFP8 on Blackwell GPUs", item 12; "Meta's MXFP8             */
+/* FlashAttention-4 kernel ...", paragraph 1: Blackwell's block-scaled   */
+/* MMA runs MXFP8, MXFP6, MXFP4 and NVFP4).  The element formats follow  */
+/* the OCP MX definitions: E2M1 (bias 1, max 6), E2M3 (bias 1, max 7.5), */
+/* E3M2 (bias 3, max 28); no Inf or NaN codes, subnormals at exponent 0. */
+/* ------------------------------------------------------------------ */
+
+#define MXO_E2M1 0
+#define MXO_E2M3 1
+#define MXO_E3M2 2
+
+static void fmt_params(int fmt, int* ebits, int* mbits, int* bias) {
+  if (fmt == MXO_E2M1) { *ebits = 2; *mbits = 1; *bias = 1; }
+  else if (fmt == MXO_E2M3) { *ebits = 2; *mbits = 3; *bias = 1; }
+  else { *ebits = 3; *mbits = 2; *bias = 3; }
+}
+
+/* Value of a code of `fmt` (sign bit above the exponent and mantissa). */
+double mxo_fp_decode(int fmt, uint8_t c) {
+  int eb, mb, bias;
+  fmt_params(fmt, &eb, &mb, &bias);
+  int sign = (c >> (eb + mb)) & 1;
+  int e = (c >> mb) & ((1 << eb) - 1);
+  int m = c & ((1 << mb) - 1);
+  double v = e == 0 ? ldexp((double)m, 1 - bias - mb) : ldexp(1.0 + (double)m / (1 << mb), e - bias);
+  return sign ? -v : v;
+}
+
+/* Largest finite value of `fmt`. */
+double mxo_fp_max(int fmt) {
+  int eb, mb, bias;
+  fmt_params(fmt, &eb, &mb, &bias);
+  return ldexp(2.0 - ldexp(1.0, -mb), (1 << eb) - 1 - bias);
+}
+
+/* Round to `fmt`: nearest, ties to even code, saturating at the maximum
+ * (OCP MX conversion with saturation); NaN -> the maximum (these formats
+ * have no NaN; NaN blocks are marked by the scale instead). */
+uint8_t mxo_fp_encode(int fmt, double y) {
+  int eb, mb, bias;
+  fmt_params(fmt, &eb, &mb, &bias);
+  uint8_t sign = (!isnan(y) && signbit(y)) ? (uint8_t)(1 << (eb + mb)) : 0;
+  double a = isnan(y) ? mxo_fp_max(fmt) : fabs(y);
+  if (a >= mxo_fp_max(fmt)) a = mxo_fp_max(fmt);
+  /* exhaustive search over the non-negative codes: the nearest value, ties
+   * to the even code (codes are ordered by value) */
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < (1 << (eb + mb)); c++) {
+    double d = fabs(mxo_fp_decode(fmt, (uint8_t)c) - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* Largest exponent of `fmt` (emax): floor(log2 of its maximum). */
+static int fp_emax(int fmt) {
+  int eb, mb, bias;
+  fmt_params(fmt, &eb, &mb, &bias);
+  return (1 << eb) - 1 - bias;
+}
+
+/* MX quantization of x[rows][cols] in 1x32 blocks along the columns with
+ * element format fmt: E8M0 scale from floor(log2 amax) - emax(fmt) clamped
+ * to [0, 254] (the OCP rule, as for E4M3), elements rounded to fmt.  Codes
+ * one per byte (unpacked); a block holding NaN or Inf gets scale 0xFF and
+ * code 0. */
+void mxo_quantize_mx(const double* x, int64_t rows, int64_t cols, int fmt, uint8_t* q, uint8_t* sf) {
+  int64_t nb = cols / 32;
+  for (int64_t r = 0; r < rows; r++)
+    for (int64_t b = 0; b < nb; b++) {
+      const double* v = x + r * cols + b * 32;
+      double amax = 0.0;
+      int bad = 0;
+      for (int i = 0; i < 32; i++) {
+        double a = fabs(v[i]);
+        if (isnan(a) || isinf(a)) bad = 1;
+        else if (a > amax) amax = a;
+      }
+      uint8_t* qq = q + r * cols + b * 32;
+      if (bad) {
+        sf[r * nb + b] = 0xFF;
+        for (int i = 0; i < 32; i++) qq[i] = 0;
+        continue;
+      }
+      int s = 0;
+      if (amax > 0.0) {
+        int ex;
+        frexp(amax, &ex);
+        s = (ex - 1) - fp_emax(fmt) + 127;
+        if (s < 0) s = 0;
+        if (s > 254) s = 254;
+      }
+      sf[r * nb + b] = (uint8_t)s;
+      for (int i = 0; i < 32; i++) qq[i] = mxo_fp_encode(fmt, ldexp(v[i], 127 - s));
+    }
+}
+
+/* NVFP4 quantization of x[rows][cols] (reading: the recipe the format is
+ * published with): one fp32 tensor scale st = amax(|x|) / (448 * 6) (1 if
+ * the tensor is all zero), per 16 columns an E4M3 block scale
+ * sb = E4M3(amax_block / (6 st)) (nearest-even, saturating), and E2M1
+ * elements x / (sb st) (0 where sb = 0).  Returns st. */
+double mxo_quantize_nvfp4(const double* x, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sf) {
+  /* the scales are decided in fp32, each step one correctly rounded fp32
+   * operation (x holds bf16 values, exact in fp32) */
+  float amax = 0.0f;
+  for (int64_t i = 0; i < rows * cols; i++)
+    if ((float)fabs(x[i]) > amax) amax = (float)fabs(x[i]);
+  volatile float st = 1.0f;
+  if (amax > 0.0f) st = amax / 2688.0f; /* 448 * 6 */
+  volatile float d6 = 6.0f * st;
+  int64_t nb = cols / 16;
+  for (int64_t r = 0; r < rows; r++)
+    for (int64_t b = 0; b < nb; b++) {
+      const double* v = x + r * cols + b * 16;
+      float bm = 0.0f;
+      for (int i = 0; i < 16; i++)
+        if ((float)fabs(v[i]) > bm) bm = (float)fabs(v[i]);
+      volatile float ratio = bm / d6;
+      uint8_t code = mxo_e4m3_encode((double)ratio);
+      sf[r * nb + b] = code;
+      volatile float sbv = (float)mxo_e4m3_decode(code) * st;
+      uint8_t* qq = q + r * cols + b * 16;
+      for (int i = 0; i < 16; i++) {
+        volatile float e = (float)v[i] / sbv;
+        qq[i] = sbv > 0.0f ? mxo_fp_encode(MXO_E2M1, (double)e) : 0;
+      }
+    }
+  return (double)st;
 }
 
 /* ------------------------------------------------------------------ */
