@@ -383,6 +383,51 @@ mxfa_status mxfa_gemm_quant(const mxfa_mx* a, const mxfa_mx* b, int64_t M, int64
                             void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
                             mxfa_stream_t stream);
 
+/* Lower-precision formats -- the next formats the pages name ([ITEMS] item
+ * 12: MXFP6 and MXFP4; [KDIM] paragraph 1: Blackwell's block-scaled MMA runs
+ * MXFP8, MXFP6, MXFP4 and NVFP4).
+ * mxfa_quantize_lowp -- bf16 x[rows][cols] -> codes in 1x32 blocks along the
+ * columns with E8M0 scales
+ * (MXFP4 = E2M1, max 6, emax 2; MXFP6 = E2M3, max 7.5, emax 2, or E3M2, max
+ * 28, emax 4: scale = floor(log2 amax) - emax, clamped to [0, 254]; codes
+ * nearest-even, saturating; a block holding Inf / NaN gets scale 0xFF and
+ * codes 0), or NVFP4 in 1x16 blocks: fp32 tensor scale st = amax / 2688
+ * (448 * 6; 1 for an all-zero tensor), written to *tensor_scale (DEVICE),
+ * E4M3 block scales E4M3(amax_block / (6 st)) and E2M1 codes of
+ * x / (scale * st), every step one correctly rounded fp32 operation (NVFP4
+ * inputs must be finite).
+ *  q          [rows][cols] bytes: with MXFA_LOWP_CODES one code per byte in
+ *             the low bits; with MXFA_LOWP_MMA (MX formats) the form the
+ *             block-scaled MMA reads sub-byte operands in from shared memory:
+ *             each run of 16 codes packed little-endian (code j at bit 4j for
+ *             FP4, 6j for FP6) in the first 8 / 12 bytes of a 16-byte group,
+ *             the rest zero -- still one byte of storage per element
+ *  sf         scales [rows][cols / 32] (MX) or [rows][cols / 16] (NVFP4)
+ *  sf_packed  MX only, nullable: packed atoms per (128-row tile, 128-column
+ *             group) as the GEMM reads them (rows, cols multiples of 128)
+ * cols must be a multiple of 32 (MX) or 16 (NVFP4). */
+#define MXFA_LOWP_MXFP4 0
+#define MXFA_LOWP_MXFP6_E2M3 1
+#define MXFA_LOWP_MXFP6_E3M2 2
+#define MXFA_LOWP_NVFP4 3
+#define MXFA_LOWP_CODES 0
+#define MXFA_LOWP_MMA 1
+mxfa_status mxfa_quantize_lowp(const void* x, int64_t rows, int cols, int fmt, int q_layout, uint8_t* q,
+                               uint8_t* sf, uint8_t* sf_packed, float* tensor_scale, mxfa_stream_t stream);
+
+/* mxfa_gemm_quant_fmt -- mxfa_gemm_quant with the element format of each
+ * operand: MXFA_ELEM_E4M3 (MXFP8), or MXFP6 / MXFP4 operands from
+ * mxfa_quantize_lowp (MXFA_LOWP_MMA layout, packed scale atoms), which the tensor
+ * core's mixed-format block-scaled MMA reads at the MXFP8 rate.  The output
+ * options are those of mxfa_gemm_quant. */
+#define MXFA_ELEM_E4M3 0
+#define MXFA_ELEM_E2M3 1
+#define MXFA_ELEM_E3M2 2
+#define MXFA_ELEM_E2M1 3
+mxfa_status mxfa_gemm_quant_fmt(const mxfa_mx* a, int a_fmt, const mxfa_mx* b, int b_fmt, int64_t M,
+                                int64_t N, int64_t K, void* y_bf16, const mxfa_mx_out* y_row,
+                                const mxfa_mx_out* y_col, mxfa_stream_t stream);
+
 /* mxfa_tensor_peak_probe -- `ctas` CTAs (one per SM at most) each issue
  * `iters` x 4 back-to-back block-scaled MMAs (M = 128, N = 256, K = 32, E4M3,
  * operands resident in shared memory) and write the SM clock cycles they took

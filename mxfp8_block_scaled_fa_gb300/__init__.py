@@ -15,7 +15,10 @@ def __getattr__(name):
                                             "AttnOpts", "P_SCALE_BLOCK", "P_SCALE_CONST",
                                             "RESCALE_THRESHOLD",
                                             "quantize", "quantize_dual", "sf_pack", "sf_unpack", "attention_fwd",
-                                            "attention_bwd", "rmsnorm_quant", "gemm_quant",
+                                            "attention_bwd", "rmsnorm_quant", "gemm_quant", "quantize_lowp",
+                                            "LOWP_MXFP4", "LOWP_MXFP6_E2M3", "LOWP_MXFP6_E3M2",
+                                            "LOWP_NVFP4", "LOWP_CODES", "LOWP_MMA", "ELEM_E4M3", "ELEM_E2M3", "ELEM_E3M2",
+                                            "ELEM_E2M1",
                                             "device_status"):
         from . import mxfa as _m
         return getattr(_m, name)

@@ -126,6 +126,10 @@ mxfa_status read_opts(const mxfa_attn_opts* opts, float& thr, int& p_scale) {
   return MXFA_OK;
 }
 
+mxfa_status gemm_common(const mxfa_mx* a, int a_code, const mxfa_mx* b, int b_code, int64_t M, int64_t N,
+                        int64_t K, void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
+                        mxfa_stream_t stream);
+
 mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seqs sq, Seqs sk,
                        int64_t total_q, int64_t total_k, int64_t ptq, int64_t ptk, int H, int D,
                        float scale, int causal, void* o, float* lse, const mxfa_mx_out* omx, bool dense,
@@ -611,9 +615,53 @@ mxfa_status mxfa_rmsnorm_quant(const void* x, const float* gamma, int64_t T, int
   return from_cuda(launch_rmsnorm_quant(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mxfa_status mxfa_gemm_quant_fmt(const mxfa_mx* a, int a_fmt, const mxfa_mx* b, int b_fmt, int64_t M,
+                                int64_t N, int64_t K, void* y_bf16, const mxfa_mx_out* y_row,
+                                const mxfa_mx_out* y_col, mxfa_stream_t stream) {
+  // element formats -> the MMA kind's format codes
+  auto code = [](int f) { return f == MXFA_ELEM_E4M3 ? 0 : f == MXFA_ELEM_E2M3 ? 3 : f == MXFA_ELEM_E3M2 ? 4 : 5; };
+  for (int f : {a_fmt, b_fmt})
+    if (f != MXFA_ELEM_E4M3 && f != MXFA_ELEM_E2M3 && f != MXFA_ELEM_E3M2 && f != MXFA_ELEM_E2M1)
+      return MXFA_ERR_INVALID_ARG;
+  return gemm_common(a, code(a_fmt), b, code(b_fmt), M, N, K, y_bf16, y_row, y_col, stream);
+}
+
 mxfa_status mxfa_gemm_quant(const mxfa_mx* a, const mxfa_mx* b, int64_t M, int64_t N, int64_t K,
                             void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
                             mxfa_stream_t stream) {
+  return gemm_common(a, 0, b, 0, M, N, K, y_bf16, y_row, y_col, stream);
+}
+
+mxfa_status mxfa_quantize_lowp(const void* x, int64_t rows, int cols, int fmt, int q_layout, uint8_t* q,
+                               uint8_t* sf, uint8_t* sf_packed, float* tensor_scale, mxfa_stream_t stream) {
+  if (!x || !q || !sf || rows < 0 || cols <= 0) return MXFA_ERR_INVALID_ARG;
+  if (fmt < MXFA_LOWP_MXFP4 || fmt > MXFA_LOWP_NVFP4) return MXFA_ERR_INVALID_ARG;
+  if (q_layout != MXFA_LOWP_CODES && q_layout != MXFA_LOWP_MMA) return MXFA_ERR_INVALID_ARG;
+  if (q_layout == MXFA_LOWP_MMA && fmt == MXFA_LOWP_NVFP4) return MXFA_ERR_UNSUPPORTED;
+  if (cols % (fmt == MXFA_LOWP_NVFP4 ? 16 : 32) != 0) return MXFA_ERR_UNSUPPORTED;
+  if (fmt == MXFA_LOWP_NVFP4 && (!tensor_scale || !aligned4(tensor_scale))) return MXFA_ERR_INVALID_ARG;
+  if (sf_packed && (fmt == MXFA_LOWP_NVFP4 || rows % 128 != 0 || cols % 128 != 0)) return MXFA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || (sf_packed && !aligned16(sf_packed))) return MXFA_ERR_MISALIGNED;
+  if (rows * int64_t(cols) >= (int64_t(1) << 40)) return MXFA_ERR_UNSUPPORTED;
+  LowpArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.fmt = fmt;
+  a.q = q;
+  a.q_mma = q_layout == MXFA_LOWP_MMA;
+  a.sf = sf;
+  a.sf_packed = sf_packed;
+  a.tensor_scale = tensor_scale;
+  return from_cuda(launch_lowp_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+mxfa_status gemm_common(const mxfa_mx* a, int a_code, const mxfa_mx* b, int b_code, int64_t M, int64_t N,
+                        int64_t K, void* y_bf16, const mxfa_mx_out* y_row, const mxfa_mx_out* y_col,
+                        mxfa_stream_t stream) {
   mxfa_status s;
   if ((s = check_mx(a)) || (s = check_mx(b))) return s;
   if (M < 0 || N < 0 || K < 0) return MXFA_ERR_INVALID_ARG;
@@ -639,11 +687,16 @@ mxfa_status mxfa_gemm_quant(const mxfa_mx* a, const mxfa_mx* b, int64_t M, int64
   g.M = M;
   g.N = N;
   g.K = K;
+  g.a_fmt = a_code;
+  g.b_fmt = b_code;
   g.y_bf16 = static_cast<uint16_t*>(y_bf16);
   if (y_row) { g.row_data = y_row->data; g.row_sfc = y_row->sf_compact; g.row_sfp = y_row->sf_packed; }
   if (y_col) { g.col_data = y_col->data; g.col_sfc = y_col->sf_compact; g.col_sfp = y_col->sf_packed; }
   return from_cuda(launch_gemm_quant(g, reinterpret_cast<cudaStream_t>(stream)));
 }
+}  // namespace
+
+extern "C" {
 
 mxfa_status mxfa_tensor_peak_probe(int iters, int ctas, unsigned long long* cycles, mxfa_stream_t stream) {
   if (iters <= 0 || ctas <= 0 || !cycles) return MXFA_ERR_INVALID_ARG;

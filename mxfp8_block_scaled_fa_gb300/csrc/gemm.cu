@@ -6,7 +6,9 @@
 // "Meta's FlashAttention-4 Achieves 2.85 PF/s with MXFP8 on Blackwell GPUs",
 // item 7: GEMM+Quantize emitting FP8 with dual scale-factor layouts):
 //   Y = A B^T with A [M][K] and B [N][K] MXFP8 (E4M3, E8M0 scale per 32
-//   along K), fp32 accumulation in tensor memory, and an epilogue that writes
+//   along K) -- or MXFP6 / MXFP4 operands, one code per byte, which the same
+//   MMA kind reads (the pages' next formats) -- fp32 accumulation in tensor
+//   memory, and an epilogue that writes
 //   Y as bf16 and/or as MXFP8 in two block layouts -- 1x32 along N (ROW: the
 //   next GEMM's K dimension, e.g. Q and K of attention) and 32x1 along M
 //   (COL: e.g. V of attention, whose MMA K dimension is the token axis) --
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
 #pragma unroll
         for (int k = 0; k < 4; k++)
           mma_mxf8_ss_w(tm + COL_ACC + 128u * b, dA + uint64_t(2 * k), dB + uint64_t(2 * k),
-                        idesc_mxf8(128, 128, 0, 0, k, k), tm + sfa, tm + sfb, (kk > 0 || k > 0) ? 1u : 0u);
+                        idesc_mxf8(128, 128, 0, 0, k, k, a.a_fmt, a.b_fmt), tm + sfa, tm + sfb,
+                        (kk > 0 || k > 0) ? 1u : 0u);
         tc_commit_w(BAR(B_EMPTY + s));  // the stage (and its scale slots) may be refilled
       }
       if (ok) tc_commit_w(BAR(B_ACCFULL + b));

@@ -249,10 +249,12 @@ __device__ __forceinline__ void tc_cp_sf_w(uint32_t tmem_col, uint64_t sdesc) {
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, E8M0 scales,
 // fp32 accumulation.  a_mn / b_mn: 1 = operand is MN-major in smem.
 // sfa_id / sfb_id select the byte of each 32-bit scale column.
+// a_fmt / b_fmt: element format codes of the kind (0 E4M3, 3 E2M3, 4 E3M2,
+// 5 E2M1; the sub-byte formats one element per byte in shared memory).
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_mn, int b_mn, int sfa_id,
-                                                  int sfb_id) {
+                                                  int sfb_id, int a_fmt = 0, int b_fmt = 0) {
   return (uint32_t(sfb_id & 3) << 4)       // B scale-factor id
-         | (0u << 7) | (0u << 10)          // A, B format: E4M3
+         | (uint32_t(a_fmt & 7) << 7) | (uint32_t(b_fmt & 7) << 10)  // A, B element formats
          | (uint32_t(a_mn & 1) << 15)      // A major
          | (uint32_t(b_mn & 1) << 16)      // B major
          | (uint32_t(N >> 3) << 17)        // N / 8

@@ -61,6 +61,22 @@ struct QuantArgs {
 };
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 
+// Lower-precision quantization (MXFP4, MXFP6, NVFP4) of bf16 x[rows][cols]
+// in 1x32 (MX) or 1x16 (NVFP4) blocks along the columns; codes unpacked, one
+// per byte.
+struct LowpArgs {
+  const uint16_t* x;
+  int64_t rows;
+  int cols;
+  int fmt;              // 0 E2M1 (MXFP4), 1 E2M3, 2 E3M2 (MXFP6), 3 NVFP4
+  uint8_t* q;           // codes [rows][cols]
+  int q_mma;            // MX only: q in the MMA form (16 codes packed, padded to 16 bytes)
+  uint8_t* sf;          // scales [rows][cols / 32] (E8M0) or [rows][cols / 16] (E4M3)
+  uint8_t* sf_packed;   // nullable, MX only: packed atoms per (128-row tile, 128-column group)
+  float* tensor_scale;  // NVFP4: device fp32, receives the tensor scale
+};
+cudaError_t launch_lowp_quantize(const LowpArgs& a, cudaStream_t s);
+
 struct PackArgs {
   const uint8_t* sf_compact;
   int64_t tokens;
@@ -151,6 +167,7 @@ struct GemmArgs {
   const uint8_t* sfa;      // packed ROW atoms of A: entry (m / 128) * (K / 128) + k / 128
   const uint8_t* sfb;      // packed ROW atoms of B: entry (n / 128) * (K / 128) + k / 128
   int64_t M, N, K;         // multiples of 128
+  int a_fmt, b_fmt;        // element format codes of the MMA kind (0 E4M3, 3 E2M3, 4 E3M2, 5 E2M1)
   uint16_t* y_bf16;        // nullable: Y bf16 [M][N]
   uint8_t *row_data, *row_sfc, *row_sfp;  // nullable: Y MXFP8, 1x32 along N
   uint8_t *col_data, *col_sfc, *col_sfp;  // nullable: Y MXFP8, 32x1 along M

@@ -251,6 +251,189 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------- MXFP4 / MXFP6 / NVFP4
+// The lower-precision formats the pages name as the next step ("Meta's
+// FlashAttention-4 Achieves 2.85 PF/s with MXFP8 on Blackwell GPUs", item 12).
+// Element formats per the OCP MX definitions (E2M1 max 6, E2M3 max 7.5,
+// E3M2 max 28); MX scales by the same rule as MXFP8 with the format's emax
+// (2, 2, 4); NVFP4 with an fp32 tensor scale st = amax / (448 * 6), E4M3
+// block scales E4M3(amax_block / (6 st)) per 16 and E2M1 codes of
+// x / (scale * st), every step one correctly rounded fp32 operation.
+// Codes are written one per byte (in the low bits), or for MX formats in
+// the MMA's shared-memory form (16 codes packed, padded to 16 bytes).
+
+// two fp32 -> E2M1 codes (round to nearest even, saturating at 6): lo in bits 0-3
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two fp32 -> FP6 codes (E2M3 when E3 is false, else E3M2): lo in byte 0
+template <bool E3>
+__device__ __forceinline__ uint32_t cvt_fp6x2(float lo, float hi) {
+  uint16_t r;
+  if (E3)
+    asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// two fp32 -> two unpacked code bytes of format FMT (0 E2M1, 1 E2M3, 2 E3M2)
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_lowp2(float lo, float hi) {
+  if (FMT == 0) {
+    const uint32_t b = cvt_e2m1x2(lo, hi);
+    return (b & 0xFu) | ((b & 0xF0u) << 4);
+  }
+  return cvt_fp6x2<FMT == 2>(lo, hi) & 0x3F3Fu;
+}
+
+// MX: one thread per 1x32 block (64 bytes in, 32 bytes of codes out).
+template <int FMT>
+__global__ void __launch_bounds__(256) lowp_mx_kernel(LowpArgs a) {
+  constexpr uint32_t kEmax = FMT == 2 ? 4u : 2u;
+  const int nb = a.cols / 32;
+  const int64_t blk = int64_t(blockIdx.x) * 256 + threadIdx.x;
+  if (blk >= a.rows * nb) return;
+  const int64_t r = blk / nb;
+  const int cb = int(blk % nb);
+  const uint16_t* src = a.x + r * a.cols + cb * 32;
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint4 v = ldg16(src + 8 * i);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+  uint32_t mx = 0;
+#pragma unroll
+  for (int e = 0; e < 16; e++) mx = max(mx, hmax2(abs2(w[e])));
+  // scale: exponent of the block maximum minus the format's emax, clamped
+  // at 0; a block holding Inf or NaN gets 0xFF and codes 0
+  const uint32_t ex = mx >> 7;
+  const uint32_t sc = mx >= 0x7F80u ? 0xFFu : (ex > kEmax ? ex - kEmax : 0u);
+  uint32_t out[8];
+  if (sc == 0xFFu) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) out[i] = 0u;
+  } else {
+    const float f = __uint_as_float((254u - sc) << 23);  // 2^(127 - sc), exact scaling
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const uint32_t lo = cvt_lowp2<FMT>(bf_lo(w[2 * i]) * f, bf_hi(w[2 * i]) * f);
+      const uint32_t hi = cvt_lowp2<FMT>(bf_lo(w[2 * i + 1]) * f, bf_hi(w[2 * i + 1]) * f);
+      out[i] = lo | (hi << 16);
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.q + r * a.cols + cb * 32);
+  if (a.q_mma) {
+    // the MMA's shared-memory form: 16 codes packed little-endian (4 or 6
+    // bits each), then zero padding up to 16 bytes
+#pragma unroll
+    for (int g = 0; g < 2; g++) {
+      const uint32_t* o = out + 4 * g;
+      if (FMT == 0) {
+        uint32_t n[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+          n[i] = (o[i] & 0xFu) | ((o[i] >> 4) & 0xF0u) | ((o[i] >> 8) & 0xF00u) | ((o[i] >> 12) & 0xF000u);
+        dst[g] = make_uint4(n[0] | (n[1] << 16), n[2] | (n[3] << 16), 0u, 0u);
+      } else {
+        uint32_t t[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+          t[i] = (o[i] & 0x3Fu) | ((o[i] >> 2) & 0xFC0u) | ((o[i] >> 4) & 0x3F000u) | ((o[i] >> 6) & 0xFC0000u);
+        dst[g] = make_uint4(t[0] | (t[1] << 24), (t[1] >> 8) | (t[2] << 16), (t[2] >> 16) | (t[3] << 8), 0u);
+      }
+    }
+  } else {
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+  a.sf[blk] = uint8_t(sc);
+  if (a.sf_packed) {
+    // packed atom of (128-row tile, 128-column group): byte (r % 32) * 16 + (r / 32 % 4) * 4 + k
+    const int64_t atom = ((r / 128) * (a.cols / 128) + cb / 4) * 512;
+    a.sf_packed[atom + atom_off(int(r % 128), cb % 4)] = uint8_t(sc);
+  }
+}
+
+// NVFP4 pass 1: the tensor's largest |x| (as fp32 bits) into *tensor_scale.
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(LowpArgs a) {
+  const int64_t n = a.rows * a.cols;
+  uint32_t mx = 0;
+  for (int64_t i = (int64_t(blockIdx.x) * 256 + threadIdx.x) * 8; i < n; i += int64_t(gridDim.x) * 256 * 8) {
+    const uint4 v = ldg16(a.x + i);
+    mx = max(mx, max(max(hmax2(abs2(v.x)), hmax2(abs2(v.y))), max(hmax2(abs2(v.z)), hmax2(abs2(v.w)))));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(a.tensor_scale), mx << 16);
+}
+
+// NVFP4 pass 2: one thread per 1x16 block.
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(LowpArgs a) {
+  const int nb = a.cols / 16;
+  const int64_t blk = int64_t(blockIdx.x) * 256 + threadIdx.x;
+  if (blk >= a.rows * nb) return;
+  const float amax = __ldg(a.tensor_scale);
+  const float st = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;  // 448 * 6
+  const float d6 = __fmul_rn(6.0f, st);
+  const int64_t r = blk / nb;
+  const int cb = int(blk % nb);
+  const uint16_t* src = a.x + r * a.cols + cb * 16;
+  const uint4 v0 = ldg16(src), v1 = ldg16(src + 8);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint32_t mx = 0;
+#pragma unroll
+  for (int e = 0; e < 8; e++) mx = max(mx, hmax2(abs2(w[e])));
+  const float bm = __uint_as_float(mx << 16);
+  const uint32_t sb = cvt_e4m3x2(__fdiv_rn(bm, d6), 0.0f) & 0xFFu;  // E4M3, nearest even, saturating
+  const float sbv = __fmul_rn(e4m3x2_to_float2(sb).x, st);
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    uint32_t lo = 0, hi = 0;
+    if (sbv > 0.0f) {
+      lo = cvt_lowp2<0>(__fdiv_rn(bf_lo(w[2 * i]), sbv), __fdiv_rn(bf_hi(w[2 * i]), sbv));
+      hi = cvt_lowp2<0>(__fdiv_rn(bf_lo(w[2 * i + 1]), sbv), __fdiv_rn(bf_hi(w[2 * i + 1]), sbv));
+    }
+    out[i] = lo | (hi << 16);
+  }
+  *reinterpret_cast<uint4*>(a.q + r * a.cols + cb * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+  a.sf[blk] = uint8_t(sb);
+}
+
+// NVFP4 pass 3: the tensor maximum -> the tensor scale the codes were made with.
+__global__ void nvfp4_finish_kernel(float* tensor_scale) {
+  const float amax = *tensor_scale;
+  *tensor_scale = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+}
+
+cudaError_t launch_lowp_quantize(const LowpArgs& a, cudaStream_t st) {
+  clear_stale_error();
+  if (a.rows == 0) return cudaSuccess;
+  if (a.fmt == 3) {
+    cudaError_t e = cudaMemsetAsync(a.tensor_scale, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    const int64_t n8 = a.rows * a.cols / 8;
+    const int64_t g1w = (n8 + 255) / 256;
+    const unsigned g1 = unsigned(g1w < 4096 ? g1w : 4096);
+    nvfp4_amax_kernel<<<g1, 256, 0, st>>>(a);
+    const int64_t nb = a.rows * (a.cols / 16);
+    nvfp4_quant_kernel<<<unsigned((nb + 255) / 256), 256, 0, st>>>(a);
+    nvfp4_finish_kernel<<<1, 1, 0, st>>>(a.tensor_scale);
+    return cudaGetLastError();
+  }
+  const int64_t nb = a.rows * (a.cols / 32);
+  const unsigned g = unsigned((nb + 255) / 256);
+  switch (a.fmt) {
+    case 0: lowp_mx_kernel<0><<<g, 256, 0, st>>>(a); break;
+    case 1: lowp_mx_kernel<1><<<g, 256, 0, st>>>(a); break;
+    default: lowp_mx_kernel<2><<<g, 256, 0, st>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ sf pack
 // Compact scales -> packed (MMA atom) scales, values unchanged; padding 0x7F.
 // grid (4 * ceil(max_len/128), nseq), block 256.

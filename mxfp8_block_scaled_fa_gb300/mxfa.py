@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
             "mxfa_rmsnorm_quant": (I, [P, P, I64, I64, F, I, I, P, P, P, P]),
             "mxfa_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint)]),
             "mxfa_gemm_quant": (I, [P, P, I64, I64, I64, P, P, P, P]),
+            "mxfa_gemm_quant_fmt": (I, [P, I, P, I, I64, I64, I64, P, P, P, P]),
+            "mxfa_quantize_lowp": (I, [P, I64, I, I, I, P, P, P, P, P]),
             "mxfa_tensor_peak_probe": (I, [I, I, P, P]),
             "mxfa_bwd_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, F, I, I, F, P, P, P, P]),
             "mxfa_bwd_noalloc_scratch_bytes": (S, []),
@@ -536,6 +538,38 @@ def mxfa_gemm_quant(a: MxIn, b: MxIn, M, N, K, y_bf16, y_row: Optional[MxOut],
     ref = lambda m: ctypes.byref(m) if m is not None else None
     _check(lib().mxfa_gemm_quant(ctypes.byref(a), ctypes.byref(b), M, N, K, _p(y_bf16), ref(y_row),
                                  ref(y_col), _stream(stream)), "mxfa_gemm_quant")
+
+
+LOWP_MXFP4, LOWP_MXFP6_E2M3, LOWP_MXFP6_E3M2, LOWP_NVFP4 = 0, 1, 2, 3
+LOWP_CODES, LOWP_MMA = 0, 1
+ELEM_E4M3, ELEM_E2M3, ELEM_E3M2, ELEM_E2M1 = 0, 1, 2, 3
+
+
+def mxfa_quantize_lowp(x, rows, cols, fmt, q_layout, q, sf, sf_packed, tensor_scale, stream=None):
+    _check(lib().mxfa_quantize_lowp(_p(x), rows, cols, fmt, q_layout, _p(q), _p(sf), _p(sf_packed),
+                                    _p(tensor_scale), _stream(stream)), "mxfa_quantize_lowp")
+
+
+def quantize_lowp(x: torch.Tensor, fmt: int, packed: bool = False, mma: bool = False, stream=None):
+    """bf16 [rows, cols] -> dict: 'q' u8 [rows, cols] (codes one per byte, or with
+    mma=True the MMA operand form of the MX formats), 'sf' scales, optional
+    'sf_packed' (MX formats), and 'tensor_scale' (NVFP4, a 1-element fp32 tensor)."""
+    rows, cols = x.shape[0], x.numel() // x.shape[0]
+    dev = x.device
+    u8 = dict(dtype=torch.uint8, device=dev)
+    q = torch.empty((rows, cols), **u8)
+    sf = torch.empty((rows, cols // (16 if fmt == LOWP_NVFP4 else 32)), **u8)
+    sfp = torch.empty((rows // 128) * (cols // 128) * 512, **u8) if packed else None
+    ts = torch.empty(1, dtype=torch.float32, device=dev) if fmt == LOWP_NVFP4 else None
+    mxfa_quantize_lowp(x, rows, cols, fmt, LOWP_MMA if mma else LOWP_CODES, q, sf, sfp, ts, stream)
+    return {"q": q, "sf": sf, "sf_packed": sfp, "tensor_scale": ts}
+
+
+def mxfa_gemm_quant_fmt(a: MxIn, a_fmt, b: MxIn, b_fmt, M, N, K, y_bf16, y_row, y_col, stream=None):
+    ref = lambda m: ctypes.byref(m) if m is not None else None
+    _check(lib().mxfa_gemm_quant_fmt(ctypes.byref(a), a_fmt, ctypes.byref(b), b_fmt, M, N, K,
+                                     _p(y_bf16), ref(y_row), ref(y_col), _stream(stream)),
+           "mxfa_gemm_quant_fmt")
 
 
 def mxfa_tensor_peak_probe(iters, ctas, cycles, stream=None):

@@ -112,6 +112,23 @@ def test_noalloc_argument_checks(lib):
     assert n(*args(m, 128, 0x4000, B=0)) == 1      # empty batch
 
 
+def test_lowp_argument_checks(lib):
+    f = lib.mxfa_quantize_lowp
+    assert f(0x1000, 128, 128, 4, 0, 0x2000, 0x3000, None, None, None) == 1      # format
+    assert f(0x1000, 128, 128, 0, 2, 0x2000, 0x3000, None, None, None) == 1      # q layout
+    assert f(0x1000, 128, 128, 3, 1, 0x2000, 0x3000, None, 0x4000, None) == 2    # NVFP4 has no MMA form
+    assert f(0x1000, 128, 48, 0, 0, 0x2000, 0x3000, None, None, None) == 2       # cols % 32
+    assert f(0x1000, 128, 128, 3, 0, 0x2000, 0x3000, None, None, None) == 1      # NVFP4 tensor scale
+    assert f(0x1000, 100, 128, 0, 1, 0x2000, 0x3000, 0x5000, None, None) == 2    # atoms need rows % 128
+    assert f(0x1008, 128, 128, 0, 1, 0x2000, 0x3000, None, None, None) == 3      # x misaligned
+    from mxfp8_block_scaled_fa_gb300 import mxfa
+    m = mxfa.MxIn(0x1000, 0x2000)
+    g = lib.mxfa_gemm_quant_fmt
+    r = ctypes.byref
+    assert g(r(m), 4, r(m), 0, 128, 128, 128, 0x4000, None, None, None) == 1     # element format
+    assert g(r(m), 3, r(m), 1, 128, 128, 96, 0x4000, None, None, None) == 2      # K % 128
+
+
 def test_attention_options_checks(lib):
     # the *_opts calls validate their options before any launch
     from mxfp8_block_scaled_fa_gb300 import mxfa
