@@ -21,7 +21,8 @@
 //               query row = TMEM lane, the whole 128-key row in registers
 // TMEM (all 512 columns): S_A [0,128) S_B [128,256) O_A [256,384)
 // O_B [384,512).  Once a tile's softmax has loaded S_X(j), the columns of S_X
-// carry P_X(j) [0,32), its scales [32,36), the V scales [36,40) (read by
+// carry P_X(j) [0,32), its scales [32,36) (both stored by the softmax
+// warps), the V scales [36,40) (read by
 // PV_X(j)), and the Q / K scales of the other tile's next S GEMM [40,48).
 // The running max moves only when it grows by more than a threshold (log2
 // units, 8 by default, 0 = at every increase); P~ then stays below
@@ -52,8 +53,7 @@ constexpr int OFF_V = OFF_K + NS * TILE_BYTES;         // NS stages
 constexpr int OFF_SFQ = OFF_V + NS * TILE_BYTES;       // 2 atoms (A, B)
 constexpr int OFF_SFK = OFF_SFQ + 2 * 512;             // NS atoms
 constexpr int OFF_SFV = OFF_SFK + NS * 512;            // NS atoms
-constexpr int OFF_SFP = OFF_SFV + NS * 512;            // 2 atoms (A, B)
-constexpr int OFF_BAR = OFF_SFP + 2 * 512;
+constexpr int OFF_BAR = OFF_SFV + NS * 512;
 enum {
   B_QFULL = 0, B_KVFULL, B_KVEMPTY = B_KVFULL + NS, B_SFULL = B_KVEMPTY + NS,
   B_SLOAD = B_SFULL + 2, B_PFULL = B_SLOAD + 2, B_ODONE = B_PFULL + 2, B_TEAR = B_ODONE + 2, NBAR
@@ -234,7 +234,6 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       auto issue_pv = [&](int x, int j) {
         const int s = j % NS;
         const uint32_t sx = COL_S + 128u * uint32_t(x);
-        cp_sf(sx + SUB_SFP, base + OFF_SFP + 512 * x);
         cp_sf(sx + SUB_SFV, base + OFF_SFV + s * 512);
         const uint64_t dV = smem_desc(base + OFF_V + s * TILE_BYTES, 8192, 1024, 2);
 #pragma unroll
@@ -393,10 +392,12 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       }
       tmem_st16(tmem + lane_base + col_s, pw);
       tmem_st16(tmem + lane_base + col_s + 16, pw + 16);
-      // this row's four P scales: atom word (row % 32) * 4 + row / 32
-      *reinterpret_cast<uint32_t*>(smem + OFF_SFP + 512 * x + (row & 31) * 16 + (row >> 5) * 4) = sfw;
+      // this row's four P scales straight into the P scale slot: the MMA
+      // reads the scales of rows 32q..32q+31 from lane quadrant q, column q of
+      // the slot (the layout a replicated 32x128b copy produces), which is
+      // this thread's own lane
+      tmem_st1(tmem + lane_base + col_s + SUB_SFP + uint32_t(row >> 5), sfw);
       tmem_wait_st();
-      fence_async_smem();
       tc_fence_before();
       fwd_warp_arrive(BAR(B_PFULL + x), lane);
       m = mu;

@@ -250,7 +250,8 @@ __device__ __forceinline__ void tc_cp_sf_w(uint32_t tmem_col, uint64_t sdesc) {
 // fp32 accumulation.  a_mn / b_mn: 1 = operand is MN-major in smem.
 // sfa_id / sfb_id select the byte of each 32-bit scale column.
 // a_fmt / b_fmt: element format codes of the kind (0 E4M3, 3 E2M3, 4 E3M2,
-// 5 E2M1; the sub-byte formats one element per byte in shared memory).
+// 5 E2M1).  The sub-byte formats sit in shared memory as runs of 16 codes
+// packed little-endian and padded to 16 bytes (one byte per element).
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_mn, int b_mn, int sfa_id,
                                                   int sfb_id, int a_fmt = 0, int b_fmt = 0) {
   return (uint32_t(sfb_id & 3) << 4)       // B scale-factor id
