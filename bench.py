@@ -387,6 +387,16 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     pairs = float(np.sum(lq.astype(np.float64) * lk)) * Hj
     res["jagged_fwd"] = {"ms": t_jf, "pflops": 4 * D * pairs / t_jf / 1e12}
     res["jagged_bwd"] = {"ms": t_jb, "pflops": 10 * D * pairs / t_jb / 1e12}
+    # accuracy on the sequence with the most queries, head 0 (outputs of the last timed calls)
+    i = int(np.argmax(lq))
+    a0, a1, k0, k1 = int(cu_q[i]), int(cu_q[i + 1]), int(cu_k[i]), int(cu_k[i + 1])
+    f = lambda x, r0, r1: inputs.bf16_bits_to_f32(x[r0:r1, 0, :]).astype(np.float64)
+    g = lambda t, r0, r1: t[r0:r1, 0, :].float().cpu().numpy()
+    ref = exact_attention(torch, f(qb, a0, a1), f(kb, k0, k1), f(vb, k0, k1), f(dob, a0, a1),
+                          1 / math.sqrt(D), False)
+    res["jagged_bwd"]["sqnr_db"] = sqnr_db([g(o, a0, a1), g(grads[0], a0, a1), g(grads[1], k0, k1),
+                                            g(grads[2], k0, k1)], ref)
+    res["jagged_bwd"]["sqnr_sample"] = f"sequence {i} ({a1 - a0} queries x {k1 - k0} keys), head 0"
     del qR, kR, vC, qS, kS, vR, do_t, doS, o, lse, out, ws, grads
     # the outlier workload: B8 H32 S4096 non-causal, outlier recipe on Q and K
     Bo, Ho, So = 8, 32, 4096
@@ -394,6 +404,7 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     so = mx.Seqs.dense(Bo, So)
     to = lambda b: torch.from_numpy(b.view("int16")).view(torch.bfloat16).reshape(Bo * So, Ho, D).to(dev)
     qo, ko, vo, doo = to(qb), to(kb), to(vb), to(dob)
+    samp = [inputs.bf16_bits_to_f32(x[0, :, 0, :]).astype(np.float64) for x in (qb, kb, vb, dob)]
     del qb, kb, vb, dob
     fq = [mx.quantize(qo, 0, so), mx.quantize(ko, 0, so), mx.quantize(vo, 1, so)]
     bq = [mx.quantize(qo, 2, so), mx.quantize(ko, 2, so), mx.quantize(vo, 0, so),
@@ -409,6 +420,10 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     res["outlier_fwd"] = {"ms": t_of, "pflops": of / t_of / 1e12,
                           "workload": "B8 H32 S4096 D128 non-causal, outlier recipe"}
     res["outlier_bwd"] = {"ms": t_ob, "pflops": 2.5 * of / t_ob / 1e12}
+    ref = exact_attention(torch, *samp, 1 / math.sqrt(D), False)
+    g = lambda t: t[:So, 0, :].float().cpu().numpy()
+    res["outlier_bwd"]["sqnr_db"] = sqnr_db([g(oo)] + [g(t) for t in go], ref)
+    res["outlier_bwd"]["sqnr_sample"] = "(batch 0, head 0), outputs of the last timed calls"
     del qo, ko, vo, doo, fq, bq, oo, lo, wso, go
     # the forward's rescale threshold and the constant P scale mode on the LLM workload
     sweep = {}
@@ -552,23 +567,64 @@ def cpu_baseline(qb, kb, vb, dob, s_len=4096):
                               "PFLOP/s": 14 * D * tiny_pairs / (u2 - u0) / 1e15}}
 
 
+def exact_attention(torch, q, k, v, do, scale, causal, chunk=1024):
+    """fp64 attention without quantization on the host, for one (sequence,
+    head): O = softmax(scale Q K^T) V and its gradients dQ, dK, dV (dS =
+    P * (dP - rowsum(dO * O))), in chunks of query rows.  A measurement
+    reference for the SQNR figures, independent of the GPU path."""
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    q, k, v, do = f(q), f(k), f(v), f(do)
+    lq, lk = q.shape[0], k.shape[0]
+    o = torch.empty_like(q)
+    dq = torch.empty_like(q)
+    dk = torch.zeros_like(k)
+    dv = torch.zeros_like(v)
+    for r0 in range(0, lq, chunk):
+        r1 = min(lq, r0 + chunk)
+        s = (q[r0:r1] @ k.T) * scale
+        if causal:  # query i sees keys j <= i (queries and keys aligned at 0)
+            qi = torch.arange(r0, r1).unsqueeze(1)
+            s = s.masked_fill(torch.arange(lk).unsqueeze(0) > qi, float("-inf"))
+        p = torch.softmax(s, dim=1)
+        oc = p @ v
+        o[r0:r1] = oc
+        dp = do[r0:r1] @ v.T
+        delta = (do[r0:r1] * oc).sum(dim=1, keepdim=True)
+        ds = p * (dp - delta)
+        dq[r0:r1] = (ds @ k) * scale
+        dk += (ds.T @ q[r0:r1]) * scale
+        dv += p.T @ do[r0:r1]
+    return [t.numpy() for t in (o, dq, dk, dv)]
+
+
+def sqnr_db(got, ref):
+    """Signal-to-quantization-noise ratio (dB) of each output against the reference."""
+    out = {}
+    for n, g, r in zip(("O", "dQ", "dK", "dV"), got, ref):
+        if g is None:
+            continue
+        g = np.asarray(g, np.float64).reshape(r.shape)
+        out[n] = float(10 * np.log10(np.sum(r * r) / max(np.sum((g - r) ** 2), 1e-300)))
+    return out
+
+
 def accuracy(torch, st, qb, kb, vb, dob, b=1, h=5):
     """Error of the GPU step's outputs against fp64 attention without any
-    quantization (the oracle with quantization off), on one (batch, head) of
-    the workload: SQNR in dB of O, dQ, dK and dV."""
-    import oracle
+    quantization, on one (batch, head) of the workload: SQNR in dB of O, dQ,
+    dK and dV, with FP32 dQ (the step) and with FP16 (static scale) dQ."""
     from mxfp8_block_scaled_fa_gb300 import inputs
-    take = lambda x: inputs.bf16_bits_to_f32(x[b, :, h:h + 1, :]).astype(np.float64)
-    q, k, v, do = take(qb), take(kb), take(vb), take(dob)
-    scale = 1.0 / math.sqrt(D)
-    o_x, lse_x = oracle.method_fwd(q, k, v, None, None, scale, CAUSAL, False)
-    g_x = oracle.method_bwd(q, k, v, do, o_x, lse_x, None, None, scale, CAUSAL, False)
-    pick = lambda t: t.view(B, S, H, D)[b, :, h:h + 1, :].float().cpu().numpy().astype(np.float64)
-    got = [pick(t) for t in (st.o, st.dq, st.dk, st.dv)]
-    sqnr = lambda g, r: float(10 * np.log10(np.sum(r * r) / max(np.sum((g - r) ** 2), 1e-300)))
-    return {"sample": f"(batch {b}, head {h}) of the workload, outputs of the last timed step",
-            "reference": "fp64 attention without quantization (oracle, quantization off)",
-            "sqnr_db": {n: sqnr(g, r) for n, g, r in zip(("O", "dQ", "dK", "dV"), got, (o_x,) + tuple(g_x))}}
+    take = lambda x: inputs.bf16_bits_to_f32(x[b, :, h, :]).astype(np.float64)
+    ref = exact_attention(torch, take(qb), take(kb), take(vb), take(dob), 1.0 / math.sqrt(D), CAUSAL)
+    pick = lambda t: t.view(B, S, H, D)[b, :, h, :].float().cpu().numpy()
+    res = {"sample": f"(batch {b}, head {h}) of the workload",
+           "reference": "fp64 attention without quantization (host, torch fp64)",
+           "sqnr_db": sqnr_db([pick(t) for t in (st.o, st.dq, st.dk, st.dv)], ref)}
+    st.bwd(1, 1.0)
+    torch.cuda.synchronize()
+    res["sqnr_db_fp16_dq"] = sqnr_db([None, pick(st.dq), pick(st.dk), pick(st.dv)], ref)
+    st.bwd()
+    torch.cuda.synchronize()
+    return res
 
 
 def reference_arm(args):

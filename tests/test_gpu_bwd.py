@@ -201,9 +201,11 @@ def test_fwd_then_bwd_on_gpu(mx):
     check([host(t.float()).astype(np.float64) for t in (dq, dk, dv)], ref, "chained")
 
 
-def test_bwd_llm_config_sampled_head(mx):
-    # the full LLM-shaped causal backward on the GPU; the oracle recomputes one
-    # (batch, head) pair in full from the same O and lse
+@pytest.mark.parametrize("dq_mode,dq_static", [(0, 1.0), (1, 1.0)])
+def test_bwd_llm_config_sampled_head(mx, dq_mode, dq_static):
+    # the full LLM-shaped causal backward on the GPU, with FP32 and with FP16
+    # (static scale) dQ accumulation; the oracle recomputes one (batch, head)
+    # pair in full from the same O and lse
     import torch
     B, H, S, D = 2, 16, 8192, 128
     scale = 1 / math.sqrt(D)
@@ -222,11 +224,11 @@ def test_bwd_llm_config_sampled_head(mx):
     o_bits[b, :, h, :] = o_h_bits.reshape(S, D)
     lse_h32 = torch.from_numpy(lse_h.reshape(S).astype(np.float32)).cuda()  # already fp32 values
     lse.view(B, H, S)[b, h].copy_(lse_h32)
-    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, scale, True)
+    got = gpu_bwd(mx, qb, kb, vb, dob, o_bits, lse, seqs, seqs, scale, True, dq_mode, dq_static)
     got = [g.reshape(B, S, H, D)[b, :, h:h + 1, :] for g in got]
     ref = oracle.method_bwd(sl(qb), sl(kb), sl(vb), sl(dob), o_h_bf, lse_h, None, None, scale, True,
                             True)
-    check(got, ref, "llm")
+    check(got, ref, f"llm dq_mode {dq_mode}")
 
 
 @pytest.mark.parametrize("varlen,dq_mode", [(False, 0), (False, 1), (True, 0)])
