@@ -268,6 +268,48 @@ def time_loop(torch, fn, iters, warmup, flush=None):
     return tot / iters
 
 
+def time_rotating(torch, fns, iters, warmup):
+    """Mean per-call device time (ms) of back-to-back calls that cycle through
+    fns, each on its own input and output buffers (together far larger than
+    L2, so every call reads its input from HBM), with CUDA events around the
+    whole loop: no flush and no per-launch event inside the timed region."""
+    for f in fns:
+        for _ in range(warmup):
+            f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(iters, len(fns))
+    a.record()
+    for i in range(n):
+        fns[i % len(fns)]()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def quant_slots(torch, mx, st, x, blk, dual, k=4):
+    """k copies of x with their own MXFP8 outputs (packed scales, as the step
+    writes them) and one quantize call per copy."""
+    s = st.seqs
+    fns, keep = [], []
+    for _ in range(k):
+        xi = x.clone()
+        if dual:
+            m, r = mx.quantize_dual(xi, blk, s)
+            o1 = mx.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+            o2 = mx.MxOut(r.data.data_ptr(), None, r.sf_packed.data_ptr())
+            fns.append(lambda xi=xi, o1=o1, o2=o2: mx.mxfa_quantize_dual(
+                xi, s.total, H, D, blk, None, s.nseq, s.max_len, s.ptiles, o1, o2))
+            keep += [xi, m, r]
+        else:
+            m = mx.quantize(xi, blk, s)
+            o1 = mx.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+            fns.append(lambda xi=xi, o1=o1: mx.mxfa_quantize(
+                xi, s.total, H, D, blk, None, s.nseq, s.max_len, s.ptiles, o1))
+            keep += [xi, m]
+    return fns, keep
+
+
 def mxfp8_peak(torch, mx, dev, iters=8192):
     """The tensor pipe's dense MXFP8 peak on this GPU: one CTA per SM issuing
     back-to-back block-scaled MMAs (M128 N256 K32) on resident operands."""
@@ -295,8 +337,9 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     from mxfp8_block_scaled_fa_gb300 import inputs
     dev = st.dev
     res = {}
-    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.zero_()
+    res["hbm_timing"] = ("quantizers and RMSNorm+Quantize: back-to-back calls cycling over 4 (2 for "
+                         "RMSNorm) input/output copies larger than L2 together, CUDA events around "
+                         "the loop")
     fp8_peak = 2.0 * bf16_peak
     st.step()
     t_fwd = time_loop(torch, st.fwd, iters, warmup)
@@ -323,11 +366,15 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     t_bwd_mxg = time_loop(torch, bwd_mxg, iters, warmup)
     del gmx
     st.bwd()
-    t_q = time_loop(torch, lambda: st.quant(st.q, "qR"), iters, warmup, flush)
-    t_qs = time_loop(torch, lambda: st.quant(st.q, "qS"), iters, warmup, flush)
-    t_qc = time_loop(torch, lambda: st.quant(st.v, "vC"), iters, warmup, flush)
-    t_dsq = time_loop(torch, lambda: st.quant_dual(st.q, "qS", "qR"), iters, warmup, flush)
-    t_dcr = time_loop(torch, lambda: st.quant_dual(st.v, "vC", "vR"), iters, warmup, flush)
+    # HBM-bound calls: back to back over 4 input / output copies (> 400 MB, past L2)
+    qt = {}
+    for key, x, blk, dual in (("q", st.q, mx.ROW, False), ("qs", st.q, mx.SQ, False),
+                              ("qc", st.v, mx.COL, False), ("dsq", st.q, mx.SQ, True),
+                              ("dcr", st.v, mx.COL, True)):
+        fns, keep = quant_slots(torch, mx, st, x, blk, dual)
+        qt[key] = time_rotating(torch, fns, iters, warmup)
+        del fns, keep
+    t_q, t_qs, t_qc, t_dsq, t_dcr = qt["q"], qt["qs"], qt["qc"], qt["dsq"], qt["dcr"]
     n = B * S * H * D
     res["fwd"] = {"ms": t_fwd, "pflops": FWD_FLOPS / t_fwd / 1e12,
                   "frac_of_4.5": FWD_FLOPS / t_fwd / 1e9 / NOMINAL_FP8_TFLOPS}
@@ -357,7 +404,15 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
                for k, v in outs.items()}
     rms = lambda: mx.mxfa_rmsnorm_quant(xd, gd, 32768, 2048, 1e-6, 8192, 16, structs["row"],
                                          structs["col"], None)
-    t_rms = time_loop(torch, rms, iters, warmup, flush)
+    # a second copy of X and its outputs: the calls alternate between them
+    xd2 = xd.clone()
+    outs2 = mx.rmsnorm_quant(xd2, gd, 1e-6, 8192, 16, outputs=("row", "col"))
+    s2 = {k: mx.MxOut(v.data.data_ptr(), v.sf_compact.data_ptr(), v.sf_packed.data_ptr())
+          for k, v in outs2.items()}
+    rms2 = lambda: mx.mxfa_rmsnorm_quant(xd2, gd, 32768, 2048, 1e-6, 8192, 16, s2["row"], s2["col"],
+                                          None)
+    t_rms = time_rotating(torch, [rms, rms2], iters, warmup)
+    del xd2, outs2
     nb = 32768 * 2048 * (2 + 2 * (1 + 1 / 32))
     res["rmsnorm_quant_row_col"] = {"ms": t_rms, "GB_s": nb / t_rms / 1e6,
                                     "frac_of_hbm": nb / t_rms / 1e6 / hbm_peak}
@@ -503,7 +558,6 @@ def components(torch, mx, st, iters, warmup, bf16_peak, hbm_peak):
     del ag, bg, outs_g, ro, co, yb
     step_q = 2 * t_dsq + t_dcr + t_qs
     res["step_share"] = {"fwd": t_fwd, "bwd": t_bwd, "quantize_4_passes": step_q}
-    del flush_buf
     torch.cuda.synchronize()
     return res
 

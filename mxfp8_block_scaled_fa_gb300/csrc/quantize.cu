@@ -12,10 +12,10 @@
 // paragraph 3), 32x32 squares for the backward operands (andresseo.expert,
 // same section).  The fused producer follows brifing.si item 7.
 //
-// These kernels are HBM-bound.  Column and square blocks: each thread owns an
-// 8-column x 32-row slab in registers (16-byte loads, 8-byte stores).  Row
-// blocks: each thread owns whole 1x32 blocks (64 bytes in, 32 bytes out), so
-// no block maximum crosses threads.  Every input byte is read once.
+// These kernels are HBM-bound.  The quantizer: each thread owns an 8-column x
+// 32-row slab in registers (16-byte loads, 8-byte stores); block maxima that
+// span lanes take butterfly steps; scale atoms are assembled in shared memory
+// and stored whole.  Every input byte is read once.
 #include <cuda_bf16.h>
 
 #include "mx_ptx.cuh"
@@ -36,110 +36,137 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
 
 
 // ------------------------------------------------------------------ quantize
-// grid (ceil(cols/1024), 4 * ceil(max_len/128), nseq), block 128.
-// blockIdx.y indexes 32-row blocks of a sequence, including the padding blocks
-// of its last 128-row tile (which only write padding scale bytes).
-template <int MODE>
-__global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
+// ROW alone (1x32 blocks along D): one thread per (row, 32-column block)
+// with the block's 64 bytes in registers, so the block maximum needs no
+// exchange between threads.  grid (ceil(cols / 1024), 4 * ceil(max_len / 128),
+// nseq), block 128; blockIdx.y indexes 32-row blocks, including the padding
+// blocks of the last 128-row tile (which only write padding scale bytes).
+__global__ void __launch_bounds__(128) quant_row_kernel(QuantArgs a) {
   const int cols = a.H * a.D;
-  const int col0 = blockIdx.x * 1024 + threadIdx.x * 8;
   const int g = blockIdx.z, rb = blockIdx.y;
   int64_t s0;
   int L;
   seq_info(a.seq, g, s0, L);
   const int nrb_real = (L + 31) / 32;
   const int nrb_pad = ((L + 127) / 128) * 4;
-  if (MODE == 0 && rb < nrb_real) {
-    // 1x32 blocks along columns: one thread per (row, 32-column block) with
-    // the block's 64 bytes in registers, so the block maximum needs no
-    // exchange between threads; warp w takes rows w, w + 4, ..., w + 28
-    const int cb = threadIdx.x & 31;
-    const int col = blockIdx.x * 1024 + cb * 32;
-    if (col >= cols) return;
-    const int hd = col / a.D, kb = (col % a.D) / 32;
-    const int kb4 = rb & 3;
-    uint8_t* pbase = nullptr;
-    if (a.sf_packed) {
-      const int64_t tg = seq_units_before(a.seq, g, 128) + (rb >> 2);
-      if (tg >= a.packed_tiles) {
-        atomicOr(&g_status_quant, DEV_BAD_INDEX);
-        return;
-      }
-      pbase = a.sf_packed + (tg * a.H + hd) * 512;
-    }
-    const int64_t r0 = s0 + int64_t(rb) * 32;
-    const int nr = min(32, L - rb * 32);
-    const int rw = threadIdx.x >> 5;
-#pragma unroll 1
-    for (int half = 0; half < 2; half++) {
-      uint4 v[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const int r = rw + 4 * (4 * half + i);
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-          v[i][k] = r < nr ? ldg16(a.x + (r0 + r) * cols + col + 8 * k) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const int r = rw + 4 * (4 * half + i);
-        if (r < nr) {
-          uint32_t w[16];
-#pragma unroll
-          for (int k = 0; k < 4; k++) {
-            w[4 * k] = v[i][k].x;
-            w[4 * k + 1] = v[i][k].y;
-            w[4 * k + 2] = v[i][k].z;
-            w[4 * k + 3] = v[i][k].w;
-          }
-          const uint32_t sc = mx_block_e8m0(w);
-          mx_block_store(a.data + (r0 + r) * cols + col, w, sc);
-          if (a.sf_compact) a.sf_compact[(r0 + r) * (cols / 32) + col / 32] = uint8_t(sc);
-          if (pbase) pbase[atom_off(kb4 * 32 + r, kb)] = uint8_t(sc);
-        } else if (pbase) {
-          pbase[atom_off(kb4 * 32 + r, kb)] = 0x7F;
-        }
-      }
-    }
-    return;
-  }
-  if (rb >= nrb_pad || col0 >= cols) return;
-  const int h = col0 / a.D, dcol = col0 % a.D;
-  const int tile = rb >> 2, kb4 = rb & 3;
-  int64_t tile_g = 0;
-  if (a.sf_packed) tile_g = seq_units_before(a.seq, g, 128) + tile;
-  if (a.sf_packed && tile_g >= a.packed_tiles) {
-    atomicOr(&g_status_quant, DEV_BAD_INDEX);
-    return;
-  }
-  const bool lead = (threadIdx.x & 3) == 0;  // first of the 4 threads of a 32-column block
-
+  if (rb >= nrb_pad) return;
   if (rb >= nrb_real) {  // padding rows of the last tile: scale bytes 0x7F only
     if (!a.sf_packed) return;
-    if (MODE == 0) {
-      uint8_t* base = a.sf_packed + (tile_g * a.H + h) * 512;
-      if (lead)
-        for (int r = 0; r < 32; r++) base[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
-    } else if (MODE == 1) {
-      uint8_t* base = a.sf_packed + (tile_g * a.H + h) * 512;
-      for (int i = 0; i < 8; i++) base[atom_off(dcol + i, kb4)] = 0x7F;
-    } else {
-      if (lead) a.sf_packed[(tile_g * a.H + h) * 16 + kb4 * 4 + dcol / 32] = 0x7F;
+    const int col0 = blockIdx.x * 1024 + threadIdx.x * 8;
+    if (col0 >= cols || (threadIdx.x & 3) != 0) return;
+    const int64_t tile_g = seq_units_before(a.seq, g, 128) + (rb >> 2);
+    if (tile_g >= a.packed_tiles) {
+      atomicOr(&g_status_quant, DEV_BAD_INDEX);
+      return;
     }
-    if (a.row_sfp && lead) {
-      uint8_t* base = a.row_sfp + (tile_g * a.H + h) * 512;
-      for (int r = 0; r < 32; r++) base[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
-    }
+    uint8_t* base = a.sf_packed + (tile_g * a.H + col0 / a.D) * 512;
+    for (int r = 0; r < 32; r++) base[atom_off((rb & 3) * 32 + r, (col0 % a.D) / 32)] = 0x7F;
     return;
   }
-
-  if (MODE == 0) return;  // real row blocks were handled above
+  // 1x32 blocks along columns: one thread per (row, 32-column block) with
+  // the block's 64 bytes in registers, so the block maximum needs no
+  // exchange between threads; warp w takes rows w, w + 4, ..., w + 28
+  const int cb = threadIdx.x & 31;
+  const int col = blockIdx.x * 1024 + cb * 32;
+  if (col >= cols) return;
+  const int hd = col / a.D, kb = (col % a.D) / 32;
+  const int kb4 = rb & 3;
+  uint8_t* pbase = nullptr;
+  if (a.sf_packed) {
+    const int64_t tg = seq_units_before(a.seq, g, 128) + (rb >> 2);
+    if (tg >= a.packed_tiles) {
+      atomicOr(&g_status_quant, DEV_BAD_INDEX);
+      return;
+    }
+    pbase = a.sf_packed + (tg * a.H + hd) * 512;
+  }
   const int64_t r0 = s0 + int64_t(rb) * 32;
   const int nr = min(32, L - rb * 32);
+  const int rw = threadIdx.x >> 5;
+#pragma unroll 1
+  for (int half = 0; half < 2; half++) {
+    uint4 v[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int r = rw + 4 * (4 * half + i);
+#pragma unroll
+      for (int k = 0; k < 4; k++)
+        v[i][k] = r < nr ? ldg16(a.x + (r0 + r) * cols + col + 8 * k) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int r = rw + 4 * (4 * half + i);
+      if (r < nr) {
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          w[4 * k] = v[i][k].x;
+          w[4 * k + 1] = v[i][k].y;
+          w[4 * k + 2] = v[i][k].z;
+          w[4 * k + 3] = v[i][k].w;
+        }
+        const uint32_t sc = mx_block_e8m0(w);
+        mx_block_store(a.data + (r0 + r) * cols + col, w, sc);
+        if (a.sf_compact) a.sf_compact[(r0 + r) * (cols / 32) + col / 32] = uint8_t(sc);
+        if (pbase) pbase[atom_off(kb4 * 32 + r, kb)] = uint8_t(sc);
+      } else if (pbase) {
+        pbase[atom_off(kb4 * 32 + r, kb)] = 0x7F;
+      }
+    }
+  }
+}
+
+// COL and SQ (optionally with ROW from the same read): one CTA = one 128-row tile of one sequence x 256 columns (two heads of
+// D = 128); warp w takes the tile's 32-row block w, each lane 8 adjacent
+// columns of those 32 rows (16-byte loads, coalesced across the warp).
+//   MODE 1 (COL): per-column maxima over the 32 rows, in registers.
+//   MODE 2 (SQ):  the 32x32 block maximum: 8 columns in registers, then the
+//                 four lanes of a quad by two butterfly steps.
+//   ROW (the optional second output): per row, the four lanes of a quad (32
+//                 columns) by two butterfly steps.
+// The packed scale atoms of the tile (512 bytes per head for ROW and COL) are
+// assembled whole in shared memory and written with 16-byte stores; SQ's (16
+// bytes per head) are written a byte per block.  Rows past a sequence end in its last tile carry padding scale
+// bytes 0x7F in the atoms and no payload.
+// grid (ceil(cols / 256), ceil(max_len / 128), nseq), block 128.
+template <int MODE>
+__global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
+  static_assert(MODE == 1 || MODE == 2, "ROW alone runs in quant_row_kernel");
+  __shared__ __align__(16) uint8_t s_blk[2][512];  // COL atoms (MODE 1)
+  __shared__ __align__(16) uint8_t s_row[2][512];  // ROW atoms
+  const int cols = a.H * 128;
+  const int g = blockIdx.z, tile = blockIdx.y;
+  int64_t s0;
+  int L;
+  seq_info(a.seq, g, s0, L);
+  if (tile * 128 >= L) return;  // past this sequence's tiles (whole CTA)
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col0 = blockIdx.x * 256 + lane * 8;
+  const bool cvalid = col0 < cols;      // an odd H leaves the last CTA one head
+  const int hh = lane >> 4;             // head within the CTA
+  const int dcol = col0 & 127;          // column within the head
+  const int rb = tile * 4 + w;          // 32-row block within the sequence
+  const int nr = min(32, L - rb * 32);  // real rows of the block (<= 0: padding block)
+  const int64_t r0 = s0 + int64_t(rb) * 32;
+  const bool lead = (lane & 3) == 0;    // first lane of a 32-column quad
+  const bool row_out = a.row_data != nullptr;
+  uint8_t* row_data = a.row_data;
+  uint8_t* row_sfc = a.row_sfc;
+  uint8_t* row_sfp = a.row_sfp;
+  uint8_t* blk_sfp = a.sf_packed;
+  int64_t tile_g = 0;
+  if (row_sfp || blk_sfp) {
+    tile_g = seq_units_before(a.seq, g, 128) + tile;
+    if (tile_g >= a.packed_tiles) {  // the caller's packed buffer is too small
+      if (threadIdx.x == 0) atomicOr(&g_status_quant, DEV_BAD_INDEX);
+      return;
+    }
+  }
+
   uint4 v[32];
 #pragma unroll
   for (int r = 0; r < 32; r++)
-    v[r] = r < nr ? ldg16(a.x + (r0 + r) * cols + col0) : make_uint4(0, 0, 0, 0);
+    v[r] = (r < nr && cvalid) ? ldg16(a.x + (r0 + r) * cols + col0) : make_uint4(0, 0, 0, 0);
 
   {
     // per-column maxima over the 32 rows (pairs of columns per word)
@@ -151,9 +178,7 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
       cm[2] = __vmaxu2(cm[2], abs2(v[r].z));
       cm[3] = __vmaxu2(cm[3], abs2(v[r].w));
     }
-    const int64_t b32 = seq_units_before(a.seq, g, 32) + rb;
     uint32_t s[8];
-    float inv[8];
     if (MODE == 1) {
 #pragma unroll
       for (int i = 0; i < 4; i++) {
@@ -162,92 +187,110 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
       }
     } else {
       uint32_t m = max(max(hmax2(cm[0]), hmax2(cm[1])), max(hmax2(cm[2]), hmax2(cm[3])));
-      const unsigned quad = __activemask();  // whole lane quads are active together
-      m = max(m, __shfl_xor_sync(quad, m, 1));
-      m = max(m, __shfl_xor_sync(quad, m, 2));
-      uint32_t sb = e8m0_from_bf16abs(m);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const uint32_t sb = e8m0_from_bf16abs(m);
 #pragma unroll
       for (int i = 0; i < 8; i++) s[i] = sb;
     }
-    bool bad[8];
+    if (nr > 0 && cvalid) {
+      bool bad[8];
+      float inv[8];
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      bad[i] = s[i] == 0xFFu;
-      inv[i] = bad[i] ? 0.0f : e8m0_inv_scale(s[i]);
-    }
-#pragma unroll
-    for (int r = 0; r < 32; r++) {
-      if (r < nr) {
-        uint2 out = cvt8(v[r], inv);
-        uint8_t* ob = reinterpret_cast<uint8_t*>(&out);
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-          if (bad[i]) ob[i] = 0x7F;
-        *reinterpret_cast<uint2*>(a.data + (r0 + r) * cols + col0) = out;
+      for (int i = 0; i < 8; i++) {
+        bad[i] = s[i] == 0xFFu;
+        inv[i] = bad[i] ? 0.0f : e8m0_inv_scale(s[i]);
       }
-    }
-    if (MODE == 1) {
+#pragma unroll
+      for (int r = 0; r < 32; r++) {
+        if (r < nr) {
+          uint2 out = cvt8(v[r], inv);
+          uint8_t* ob = reinterpret_cast<uint8_t*>(&out);
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            if (bad[i]) ob[i] = 0x7F;
+          *reinterpret_cast<uint2*>(a.data + (r0 + r) * cols + col0) = out;
+        }
+      }
       if (a.sf_compact) {
-        uint2 sv;
-        sv.x = s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
-        sv.y = s[4] | (s[5] << 8) | (s[6] << 16) | (s[7] << 24);
-        *reinterpret_cast<uint2*>(a.sf_compact + b32 * cols + col0) = sv;
+        const int64_t b32 = seq_units_before(a.seq, g, 32) + rb;
+        if (MODE == 1) {
+          uint2 sv;
+          sv.x = s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
+          sv.y = s[4] | (s[5] << 8) | (s[6] << 16) | (s[7] << 24);
+          *reinterpret_cast<uint2*>(a.sf_compact + b32 * cols + col0) = sv;
+        } else if (lead) {
+          a.sf_compact[b32 * (cols / 32) + col0 / 32] = uint8_t(s[0]);
+        }
       }
-      if (a.sf_packed) {
-        uint8_t* base = a.sf_packed + (tile_g * a.H + h) * 512;
+    }
+    // this block's bytes of the tile's atoms (padding blocks: 0x7F)
+    if (blk_sfp && cvalid) {
+      if (MODE == 1) {
 #pragma unroll
-        for (int i = 0; i < 8; i++) base[atom_off(dcol + i, kb4)] = uint8_t(s[i]);
+        for (int i = 0; i < 8; i++) s_blk[hh][atom_off(dcol + i, w)] = nr > 0 ? uint8_t(s[i]) : uint8_t(0x7F);
+      } else if (lead) {
+        // an SQ atom is 16 bytes per (tile, head): one byte per quad, direct
+        blk_sfp[(tile_g * a.H + blockIdx.x * 2 + hh) * 16 + w * 4 + dcol / 32] =
+            nr > 0 ? uint8_t(s[0]) : uint8_t(0x7F);
       }
-    } else if (lead) {
-      if (a.sf_compact) a.sf_compact[b32 * (cols / 32) + col0 / 32] = uint8_t(s[0]);
-      if (a.sf_packed) a.sf_packed[(tile_g * a.H + h) * 16 + kb4 * 4 + dcol / 32] = uint8_t(s[0]);
     }
   }
-  if (MODE != 0 && a.row_data) {
-    // the same rows in 1x32 blocks along D: a row's 32-column block spans the
-    // four threads of this lane quad (8 columns each), so its maximum takes
-    // two butterfly steps
-    uint8_t* rpk = a.row_sfp ? a.row_sfp + (tile_g * a.H + h) * 512 : nullptr;
-    const unsigned quad = __activemask();  // whole lane quads are active together
+  if (row_out) {
+    // 1x32 blocks along D: a row's 32-column block is the lane quad's
 #pragma unroll
     for (int r = 0; r < 32; r++) {
       uint32_t m = max(max(hmax2(abs2(v[r].x)), hmax2(abs2(v[r].y))), max(hmax2(abs2(v[r].z)), hmax2(abs2(v[r].w))));
-      m = max(m, __shfl_xor_sync(quad, m, 1));
-      m = max(m, __shfl_xor_sync(quad, m, 2));
-      if (r >= nr) continue;
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const uint32_t sc = e8m0_from_bf16abs(m);
-      uint2 out;
-      if (sc == 0xFFu) {
-        out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-      } else {
-        float inv[8];
-        const float f = e8m0_inv_scale(sc);
+      if (r < nr && cvalid) {
+        uint2 out;
+        if (sc == 0xFFu) {
+          out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+          float inv[8];
+          const float f = e8m0_inv_scale(sc);
 #pragma unroll
-        for (int i = 0; i < 8; i++) inv[i] = f;
-        out = cvt8(v[r], inv);
+          for (int i = 0; i < 8; i++) inv[i] = f;
+          out = cvt8(v[r], inv);
+        }
+        *reinterpret_cast<uint2*>(row_data + (r0 + r) * cols + col0) = out;
+        if (lead && row_sfc) row_sfc[(r0 + r) * (cols / 32) + col0 / 32] = uint8_t(sc);
       }
-      *reinterpret_cast<uint2*>(a.row_data + (r0 + r) * cols + col0) = out;
-      if (lead) {
-        if (a.row_sfc) a.row_sfc[(r0 + r) * (cols / 32) + col0 / 32] = uint8_t(sc);
-        if (rpk) rpk[atom_off(kb4 * 32 + r, dcol / 32)] = uint8_t(sc);
-      }
+      if (lead && row_sfp && cvalid) s_row[hh][atom_off(w * 32 + r, dcol / 32)] = r < nr ? uint8_t(sc) : uint8_t(0x7F);
     }
-    // rows past the sequence in this block: padding scales of the packed atom
-    if (rpk && lead)
-      for (int r = nr; r < 32; r++) rpk[atom_off(kb4 * 32 + r, dcol / 32)] = 0x7F;
   }
+  if (!row_sfp && !(MODE == 1 && blk_sfp)) return;
+  __syncthreads();
+  // the tile's atoms, whole, as 16-byte stores: threads 0-63 COL's (2 heads x
+  // 32 chunks), 64-127 ROW's
+  const int t = threadIdx.x;
+  const int head = (t >> 5) & 1, chunk = t & 31;
+  const int hd = blockIdx.x * 2 + head;
+  if (MODE == 1 && blk_sfp && t < 64 && hd < a.H)
+    *reinterpret_cast<uint4*>(blk_sfp + (tile_g * a.H + hd) * 512 + chunk * 16) =
+        *reinterpret_cast<const uint4*>(&s_blk[head][chunk * 16]);
+  if (row_sfp && t >= 64 && hd < a.H)
+    *reinterpret_cast<uint4*>(row_sfp + (tile_g * a.H + hd) * 512 + chunk * 16) =
+        *reinterpret_cast<const uint4*>(&s_row[head][chunk * 16]);
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   clear_stale_error();
   const int cols = a.H * a.D;
-  dim3 grid((cols + 1023) / 1024, 4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
-  if (grid.y == 0 || grid.z == 0) return cudaSuccess;
-  switch (a.mode) {
-    case 0: quant_kernel<0><<<grid, 128, 0, st>>>(a); break;
-    case 1: quant_kernel<1><<<grid, 128, 0, st>>>(a); break;
-    default: quant_kernel<2><<<grid, 128, 0, st>>>(a); break;
+  if (a.mode == 0) {
+    dim3 grid((cols + 1023) / 1024, 4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
+    if (grid.y == 0 || grid.z == 0) return cudaSuccess;
+    quant_row_kernel<<<grid, 128, 0, st>>>(a);
+    return cudaGetLastError();
   }
+  dim3 grid((cols + 255) / 256, (a.seq.seqlen + 127) / 128, a.seq.nseq);
+  if (grid.y == 0 || grid.z == 0) return cudaSuccess;
+  if (a.mode == 1)
+    quant_kernel<1><<<grid, 128, 0, st>>>(a);
+  else
+    quant_kernel<2><<<grid, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 
