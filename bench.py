@@ -9,7 +9,8 @@ keys and 1x32 along D, one read), packed scales -> forward -> quantize dO
 10*D FLOPs per unmasked (query, key) pair, S^2/2 pairs per causal head).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxfa|reference]
-  python bench.py --profile-op fwd|bwd|rmsnorm|quant_row|quant_col|quant_sq [--profile-seq S]
+  python bench.py --profile-op fwd|bwd|rmsnorm|gemm|quant_row|quant_col|quant_sq|quant_dual_sq|
+                   quant_dual_col [--profile-seq S]
                    [--profile-batch B] [--steps K] [--warmup W]
 
 One JSON line on rank 0; at N=1 it also carries "accuracy": the SQNR of the
@@ -64,7 +65,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-components", action="store_true")
     p.add_argument("--no-accuracy", action="store_true")
-    p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm", "quant_row", "quant_col",
+    p.add_argument("--profile-op", choices=["fwd", "bwd", "rmsnorm", "gemm", "quant_dual_sq",
+                                            "quant_dual_col", "quant_row", "quant_col",
                                             "quant_sq"], default=None)
     p.add_argument("--profile-seq", type=int, default=4096)
     p.add_argument("--profile-batch", type=int, default=1)
@@ -740,20 +742,46 @@ def profile_op(args):
                           "ms": ms, "GB_s": nb / ms / 1e6}), flush=True)
         return 0
     b, s = args.profile_batch, args.profile_seq
+    if args.profile_op == "gemm":
+        # the fused workload's QKV projection: X[32768, 2048] x W[6144, 2048]^T, MXFP8 ROW + COL out
+        dev = torch.device("cuda", 0)
+        Mg, Kg, Ng = 32768, 2048, 6144
+        mk = lambda rows, seed: mxfa.quantize(torch.from_numpy(inputs.normal_bf16(
+            (rows, Kg // 128, 128), seed).view("int16")).view(torch.bfloat16).to(dev), mxfa.ROW,
+            mxfa.Seqs.dense(1, rows))
+        ag, bg = mk(Mg, 21), mk(Ng, 22)
+        res = mxfa.gemm_quant(ag, bg, bf16=False)
+        so = [mxfa.MxOut(res[n].data.data_ptr(), res[n].sf_compact.data_ptr(),
+                         res[n].sf_packed.data_ptr()) for n in ("row", "col")]
+        run = lambda: mxfa.mxfa_gemm_quant(ag.mx_in(), bg.mx_in(), Mg, Ng, Kg, None, so[0], so[1])
+        ms = time_loop(torch, run, args.steps, args.warmup)
+        assert mxfa.device_status() == 0, "device status"
+        print(json.dumps({"profile_op": "gemm", "M": Mg, "N": Ng, "K": Kg, "ms": ms,
+                          "pflops": 2.0 * Mg * Ng * Kg / ms / 1e12}), flush=True)
+        return 0
     if args.profile_op.startswith("quant"):
-        blk = {"quant_row": 0, "quant_col": 1, "quant_sq": 2}[args.profile_op]
+        blk = {"quant_row": 0, "quant_col": 1, "quant_sq": 2, "quant_dual_sq": 2,
+               "quant_dual_col": 1}[args.profile_op]
+        dual = args.profile_op.startswith("quant_dual")
         qb = inputs.normal_bf16((B, S, H, D), SEED)
         dev = torch.device("cuda", 0)
         q = torch.from_numpy(qb.view("int16")).view(torch.bfloat16).reshape(B * S, H, D).to(dev)
         seqs = mxfa.Seqs.dense(B, S)
-        m = mxfa.quantize(q, blk, seqs)
-        out = mxfa.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
-        run = lambda: mxfa.mxfa_quantize(q, seqs.total, H, D, blk, None, seqs.nseq, seqs.max_len,
-                                         seqs.ptiles, out)
+        if dual:
+            m, r = mxfa.quantize_dual(q, blk, seqs)
+            o1 = mxfa.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+            o2 = mxfa.MxOut(r.data.data_ptr(), None, r.sf_packed.data_ptr())
+            run = lambda: mxfa.mxfa_quantize_dual(q, seqs.total, H, D, blk, None, seqs.nseq,
+                                                  seqs.max_len, seqs.ptiles, o1, o2)
+        else:
+            m = mxfa.quantize(q, blk, seqs)
+            out = mxfa.MxOut(m.data.data_ptr(), None, m.sf_packed.data_ptr())
+            run = lambda: mxfa.mxfa_quantize(q, seqs.total, H, D, blk, None, seqs.nseq, seqs.max_len,
+                                             seqs.ptiles, out)
         ms = time_loop(torch, run, args.steps, args.warmup)
         assert mxfa.device_status() == 0, "device status"
         n = B * S * H * D
-        nb = n * (2 + 1 + (1 / 1024 if blk == 2 else 1 / 32))
+        nb = n * (2 + 1 + (1 / 1024 if blk == 2 else 1 / 32) + ((1 + 1 / 32) if dual else 0))
         print(json.dumps({"profile_op": args.profile_op, "shape": [B * S, H, D], "ms": ms,
                           "GB_s": nb / ms / 1e6}), flush=True)
         return 0

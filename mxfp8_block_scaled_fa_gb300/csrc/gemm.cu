@@ -6,8 +6,9 @@
 // "Meta's FlashAttention-4 Achieves 2.85 PF/s with MXFP8 on Blackwell GPUs",
 // item 7: GEMM+Quantize emitting FP8 with dual scale-factor layouts):
 //   Y = A B^T with A [M][K] and B [N][K] MXFP8 (E4M3, E8M0 scale per 32
-//   along K) -- or MXFP6 / MXFP4 operands, one code per byte, which the same
-//   MMA kind reads (the pages' next formats) -- fp32 accumulation in tensor
+//   along K) -- or MXFP6 / MXFP4 operands (runs of 16 codes packed and padded
+//   to 16 bytes, one byte per element), which the same MMA kind reads (the
+//   pages' next formats) -- fp32 accumulation in tensor
 //   memory, and an epilogue that writes
 //   Y as bf16 and/or as MXFP8 in two block layouts -- 1x32 along N (ROW: the
 //   next GEMM's K dimension, e.g. Q and K of attention) and 32x1 along M

@@ -62,8 +62,8 @@ struct QuantArgs {
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 
 // Lower-precision quantization (MXFP4, MXFP6, NVFP4) of bf16 x[rows][cols]
-// in 1x32 (MX) or 1x16 (NVFP4) blocks along the columns; codes unpacked, one
-// per byte.
+// in 1x32 (MX) or 1x16 (NVFP4) blocks along the columns; codes one per byte, or
+// (MX formats) in the MMA operand form.
 struct LowpArgs {
   const uint16_t* x;
   int64_t rows;
