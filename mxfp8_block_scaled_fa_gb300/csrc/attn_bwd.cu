@@ -561,8 +561,9 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       }
       const uint8_t* rec = smem + OFF_REC + s * REC_BYTES;
       {
-        const float2* nl2 = reinterpret_cast<const float2*>(rec + REC_NL2) + 16 * hq;
-        const float2* ndl = reinterpret_cast<const float2*>(rec + REC_NDELTA) + 16 * hq;
+        // per query of this half: -lse log2 e and -Delta, four queries per 16-byte load
+        const float4* nl4 = reinterpret_cast<const float4*>(rec + REC_NL2) + 8 * hq;
+        const float4* nd4 = reinterpret_cast<const float4*>(rec + REC_NDELTA) + 8 * hq;
         const int q0 = i * QT + 32 * hq;
         // keys past the sequence and (causal) keys after the query: S = -inf,
         // so that P = 2^-inf = 0 and dS = 0; only tiles on the edge need it
@@ -575,11 +576,16 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
         // exponent arguments t = fl(S * fl(scale * log2 e) - lse * log2 e)
         float tmax = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 t = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, nl2[c / 2]);
-          sv[c] = t.x;
-          sv[c + 1] = t.y;
-          tmax = fmax3(tmax, t.x, t.y);
+        for (int c = 0; c < 32; c += 4) {
+          const float4 n = nl4[c / 4];
+          const float2 t0 = ffma2(make_float2(sv[c], sv[c + 1]), sl2v, make_float2(n.x, n.y));
+          const float2 t1 = ffma2(make_float2(sv[c + 2], sv[c + 3]), sl2v, make_float2(n.z, n.w));
+          sv[c] = t0.x;
+          sv[c + 1] = t0.y;
+          sv[c + 2] = t1.x;
+          sv[c + 3] = t1.y;
+          tmax = fmax3(tmax, t0.x, t0.y);
+          tmax = fmax3(tmax, t1.x, t1.y);
         }
         // P <= 1: exact attention has S * scale <= lse, but S recomputed from
         // the square-block operands can exceed the forward's lse (by hundreds
@@ -593,8 +599,10 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           // P = 2^t, dS = P * (dP - Delta)
+          const float4 nd = nd4[c / 4];
+          const float2 ndc = (c & 2) ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
           const float p0 = bex2(sv[c]), p1 = bex2(sv[c + 1]);
-          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp[c], dp[c + 1]), ndl[c / 2]));
+          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp[c], dp[c + 1]), ndc));
           sv[c] = p0;
           sv[c + 1] = p1;
           dp[c] = ds.x;

@@ -597,8 +597,15 @@ constexpr int NTHREADS = 1024;
 __host__ __device__ constexpr int smem_bytes(int C) { return 32 * C * 2 + 32 * C + C * 4 + C * 4 + C + C / 32; }
 }  // namespace rms
 
-__device__ __forceinline__ float rms_y(uint32_t w, bool hi, float r, float g) {
-  return __fmul_rn(__fmul_rn(hi ? bf_hi(w) : bf_lo(w), r), g);
+// y = (x * r) * g for the two bf16 of a word, as packed f32x2 multiplies
+// (each half rounded exactly as the scalar multiply)
+__device__ __forceinline__ float2 rms_y2(uint32_t w, float r, float g_lo, float g_hi) {
+  return fmul2(fmul2(make_float2(bf_lo(w), bf_hi(w)), make_float2(r, r)), make_float2(g_lo, g_hi));
+}
+// eight y values times their inverse scales -> eight E4M3 bytes
+__device__ __forceinline__ uint2 pack8_scaled(const float2* y, float2 s0, float2 s1, float2 s2, float2 s3) {
+  const float2 a = fmul2(y[0], s0), b = fmul2(y[1], s1), c = fmul2(y[2], s2), d = fmul2(y[3], s3);
+  return make_uint2(pack4_e4m3(a.x, a.y, b.x, b.y), pack4_e4m3(c.x, c.y, d.x, d.y));
 }
 // E8M0 byte from the exponent byte of a block maximum (0xFF: Inf / NaN present).
 __device__ __forceinline__ uint32_t e8m0_from_exp(uint32_t e) {
@@ -663,9 +670,10 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
       const uint32_t wv[4] = {xk.x, xk.y, xk.z, xk.w};
 #pragma unroll
       for (int j = 0; j < 4; j++) {
-        const float lo = bf_lo(wv[j]), hi = bf_hi(wv[j]);
-        ss = __fadd_rn(ss, __fmul_rn(lo, lo));
-        ss = __fadd_rn(ss, __fmul_rn(hi, hi));
+        const float2 x2 = make_float2(bf_lo(wv[j]), bf_hi(wv[j]));
+        const float2 sq = fmul2(x2, x2);
+        ss = __fadd_rn(ss, sq.x);
+        ss = __fadd_rn(ss, sq.y);
       }
     }
 #pragma unroll
@@ -680,12 +688,10 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
       const float4 g0 = *reinterpret_cast<const float4*>(sgm + c0);
       const float4 g1 = *reinterpret_cast<const float4*>(sgm + c0 + 4);
       const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      float y[8];
+      float2 y2[4];
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        y[2 * j] = rms_y(wv[j], false, r, gm[2 * j]);
-        y[2 * j + 1] = rms_y(wv[j], true, r, gm[2 * j + 1]);
-      }
+      for (int j = 0; j < 4; j++) y2[j] = rms_y2(wv[j], r, gm[2 * j], gm[2 * j + 1]);
+      const float y[8] = {y2[0].x, y2[0].y, y2[1].x, y2[1].y, y2[2].x, y2[2].y, y2[3].x, y2[3].y};
       // exponent bytes of |y| (y's bits shifted left by one hold the exponent
       // in their top byte), four per word
       uint32_t u[8];
@@ -701,10 +707,8 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
         e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
         e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 2));
         const uint32_t s = e8m0_from_exp(e);
-        const float f = e8m0_inv_scale(s);
-        uint2 out;
-        out.x = pack4_e4m3(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
-        out.y = pack4_e4m3(y[4] * f, y[5] * f, y[6] * f, y[7] * f);
+        const float2 f2 = make_float2(e8m0_inv_scale(s), e8m0_inv_scale(s));
+        uint2 out = pack8_scaled(y2, f2, f2, f2, f2);
         if (s == 0xFFu) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
         if (valid) {
           *reinterpret_cast<uint2*>(a.row_data + row * C + c0) = out;
@@ -769,18 +773,14 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
       const float4 g0 = *reinterpret_cast<const float4*>(sgm + c0);
       const float4 g1 = *reinterpret_cast<const float4*>(sgm + c0 + 4);
       const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      float y[8];
+      float2 y2[4];
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        y[2 * j] = rms_y(wv[j], false, r, gm[2 * j]);
-        y[2 * j + 1] = rms_y(wv[j], true, r, gm[2 * j + 1]);
-      }
+      for (int j = 0; j < 4; j++) y2[j] = rms_y2(wv[j], r, gm[2 * j], gm[2 * j + 1]);
       if (a.col_data) {
         const float4 i0 = *reinterpret_cast<const float4*>(scinv + c0);
         const float4 i1 = *reinterpret_cast<const float4*>(scinv + c0 + 4);
-        uint2 out;
-        out.x = pack4_e4m3(y[0] * i0.x, y[1] * i0.y, y[2] * i0.z, y[3] * i0.w);
-        out.y = pack4_e4m3(y[4] * i1.x, y[5] * i1.y, y[6] * i1.z, y[7] * i1.w);
+        uint2 out = pack8_scaled(y2, make_float2(i0.x, i0.y), make_float2(i0.z, i0.w), make_float2(i1.x, i1.y),
+                                 make_float2(i1.z, i1.w));
         // columns with Inf / NaN (scale 0xFF) carry 0x7F payloads
         const uint2 sw = *reinterpret_cast<const uint2*>(scol + c0);
         const uint32_t b0 = __vcmpeq4(sw.x, 0xFFFFFFFFu), b1 = __vcmpeq4(sw.y, 0xFFFFFFFFu);
@@ -794,9 +794,8 @@ __global__ void __launch_bounds__(rms::NTHREADS, 1) rms_quant_kernel(RmsArgs a) 
         if (s == 0xFFu) {
           out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
-          const float f = e8m0_inv_scale(s);
-          out.x = pack4_e4m3(y[0] * f, y[1] * f, y[2] * f, y[3] * f);
-          out.y = pack4_e4m3(y[4] * f, y[5] * f, y[6] * f, y[7] * f);
+          const float2 f2 = make_float2(e8m0_inv_scale(s), e8m0_inv_scale(s));
+          out = pack8_scaled(y2, f2, f2, f2, f2);
         }
         *reinterpret_cast<uint2*>(a.sq_data + row * C + c0) = out;
       }
