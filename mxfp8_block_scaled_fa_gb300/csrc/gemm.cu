@@ -15,7 +15,8 @@
 //   (COL: e.g. V of attention, whose MMA K dimension is the token axis) --
 //   with compact and packed scales, one pass over the accumulator.
 //
-// Structure: persistent, one CTA per SM, 128x128 output tiles, 6 warps:
+// Structure: persistent, one CTA per SM, 128x128 output tiles (N tiles
+// fastest, so that a wave of CTAs reads few A panels and B stays in L2), 6 warps:
 //   warp 0      TMA producer: per 128-wide K step, the A and B tiles (128 x
 //               128 E4M3, 128B swizzle) and their 512-byte scale atoms into a
 //               6-stage ring
@@ -23,7 +24,8 @@
 //               tcgen05.cp, four block-scaled MMAs (K = 32 each) per stage;
 //               two accumulators, so one tile's epilogue overlaps the next
 //               tile's MMAs
-//   warps 2-5   epilogue: thread = output row = TMEM lane; each 32-column
+//   warps 2-    epilogue, EQ warps per TMEM lane quadrant (128 / EQ columns each):
+//               thread = output row = TMEM lane; each 32-column
 //               chunk is one ROW block of the thread, and 32 rows of a warp
 //               form the COL blocks (block maximum by a warp reduction)
 // TMEM: accumulators [0,128) and [128,256); per stage s the A / B scale
@@ -49,7 +51,12 @@ constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "GEMM stages exceed the shared memory of one CTA");
 constexpr uint32_t COL_ACC = 0, COL_SF = 256;
-constexpr int NTHREADS = 192;
+#ifndef MXFA_GEMM_EQ
+#define MXFA_GEMM_EQ 2
+#endif
+constexpr int EQ = MXFA_GEMM_EQ;            // epilogue warps per TMEM lane quadrant
+constexpr int CPW = 4 / EQ;                 // 32-column chunks per epilogue warp
+constexpr int NTHREADS = 64 + 128 * EQ;     // producer, MMA issuer, 4 EQ epilogue warps
 }  // namespace gemm
 
 __device__ __forceinline__ bool gemm_wait_raw(uint32_t bar, uint32_t parity) {
@@ -65,6 +72,27 @@ __device__ __forceinline__ uint32_t warp_max_abs_bits(float x) {
   uint32_t r;
   asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(__float_as_uint(x) & 0x7FFFFFFFu));
   return r;
+}
+
+// Largest |x| of a, b, c, NaN if any of them is NaN (Inf stays Inf).
+__device__ __forceinline__ float max3_abs_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+// 32 fp32 values times one inverse scale f -> 32 E4M3 bytes at dst (16-byte
+// aligned); bad (a 0xFF scale: Inf / NaN in the block) gives 0x7F bytes.
+__device__ __forceinline__ void store_e4m3_32_uniform(uint8_t* dst, const float* y, float f, bool bad) {
+  uint32_t w[8];
+  const float2 f2 = make_float2(f, f);
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const float2 a = fmul2(make_float2(y[4 * i], y[4 * i + 1]), f2);
+    const float2 b = fmul2(make_float2(y[4 * i + 2], y[4 * i + 3]), f2);
+    w[i] = bad ? 0x7F7F7F7Fu : (cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16));
+  }
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // 32 fp32 values -> 32 E4M3 bytes at dst (16-byte aligned), each value times
@@ -107,7 +135,7 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(BAR(B_ACCFULL + b), 1);
-      mbar_init(BAR(B_ACCEMPTY + b), 4);  // one arrival per epilogue warp
+      mbar_init(BAR(B_ACCEMPTY + b), 4 * EQ);  // one arrival per epilogue warp
     }
     mbar_init(BAR(B_TEAR), 1);
     fence_mbar_init();
@@ -129,7 +157,7 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        const int mt = t % mt_n, nt = t / mt_n;
+        const int mt = t / nt_n, nt = t % nt_n;  // N tiles fastest: a wave shares few A panels, B stays in L2
         for (int kk = 0; kk < kt_n; kk++, it++) {
           const int s = it % NS;
           if (it >= NS && !mbar_wait(BAR(B_EMPTY + s), ((it / NS) - 1) & 1, abort_flag, &g_status_gemm)) {
@@ -191,7 +219,10 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // EQ warps per TMEM lane quadrant, each taking CPW 32-column chunks of the
+    // tile's 128 columns for the quadrant's 32 rows.
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    const int part = (warp - 2) >> 2;       // columns [32 CPW part, 32 CPW (part + 1))
     const int r = q * 32 + lane;            // row of the tile
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     int lt = 0;
@@ -200,23 +231,25 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(B_ACCFULL + b), (lt >> 1) & 1, abort_flag, &g_status_gemm)))
         break;
       tc_fence_after();
-      float y[128];
+      float y[32 * CPW];
 #pragma unroll
-      for (int c = 0; c < 4; c++)
-        tmem_ld32(tmem + lane_base + COL_ACC + 128u * b + 32 * c, reinterpret_cast<uint32_t*>(y) + 32 * c);
+      for (int c = 0; c < CPW; c++)
+        tmem_ld32(tmem + lane_base + COL_ACC + 128u * b + 32u * (CPW * part + c),
+                  reinterpret_cast<uint32_t*>(y) + 32 * c);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; c++) reg_fence32(reinterpret_cast<uint32_t*>(y) + 32 * c);
+      for (int c = 0; c < CPW; c++) reg_fence32(reinterpret_cast<uint32_t*>(y) + 32 * c);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_ACCEMPTY + b));  // the MMAs may reuse accumulator b
-      const int mt = t % mt_n, nt = t / mt_n;
+      const int mt = t / nt_n, nt = t % nt_n;  // N tiles fastest: a wave shares few A panels, B stays in L2
       const int64_t m = int64_t(mt) * BM + r;
-      uint32_t row_sc = 0;
+      uint32_t row_sc = 0;  // this warp's CPW ROW scale bytes
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
+      for (int c = 0; c < CPW; c++) {
         const float* yc = y + 32 * c;
-        const int64_t n0 = int64_t(nt) * BN + 32 * c;
+        const int cg = CPW * part + c;  // 32-column chunk of the tile
+        const int64_t n0 = int64_t(nt) * BN + 32 * cg;
         if (a.y_bf16) {
           uint32_t w[16];
 #pragma unroll
@@ -229,24 +262,15 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
           for (int v4 = 0; v4 < 4; v4++) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
         if (a.row_data) {
-          // ROW: this thread's 32 values are one 1x32 block along N
-          float mx = 0.0f;
+          // ROW: this thread's 32 values are one 1x32 block along N; the
+          // NaN-propagating maximum also flags Inf / NaN (exponent field 0xFF)
+          float mx = max3_abs_nan(yc[0], yc[1], yc[2]);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) mx = fmax3(mx, fabsf(yc[i]), fabsf(yc[i + 1]));
-          bool bad = false;
-#pragma unroll
-          for (int i = 0; i < 32; i++) bad |= !(fabsf(yc[i]) <= 3.402823466e38f);
-          const uint32_t sc = bad ? 0xFFu : e8m0_from_amax(mx);
+          for (int i = 3; i < 31; i += 2) mx = max3_abs_nan(mx, yc[i], yc[i + 1]);
+          mx = max3_abs_nan(mx, yc[31], 0.0f);
+          const uint32_t sc = e8m0_from_amax(mx);
           row_sc |= sc << (8 * c);
-          float inv[32];
-          uint32_t scs[32];
-          const float f = sc == 0xFFu ? 1.0f : e8m0_inv_scale(sc);
-#pragma unroll
-          for (int i = 0; i < 32; i++) {
-            inv[i] = f;
-            scs[i] = sc;
-          }
-          store_e4m3_32(a.row_data + m * a.N + n0, yc, inv, scs);
+          store_e4m3_32_uniform(a.row_data + m * a.N + n0, yc, sc == 0xFFu ? 1.0f : e8m0_inv_scale(sc), sc == 0xFFu);
         }
         if (a.col_data) {
           // COL: the warp's 32 rows form one 32x1 block per column
@@ -267,14 +291,17 @@ __global__ void __launch_bounds__(gemm::NTHREADS, 1) gemm_quant_kernel(const __g
           if (a.col_sfc) a.col_sfc[rb * a.N + n0 + lane] = uint8_t(my_sc);
           // packed COL atom of (row tile mt, column group nt): byte (d % 32) * 16 + (d / 32) * 4 + k
           if (a.col_sfp)
-            a.col_sfp[(int64_t(mt) * nt_n + nt) * 512 + atom_off(32 * c + lane, q)] = uint8_t(my_sc);
+            a.col_sfp[(int64_t(mt) * nt_n + nt) * 512 + atom_off(32 * cg + lane, q)] = uint8_t(my_sc);
         }
       }
       if (a.row_data) {
-        if (a.row_sfc) *reinterpret_cast<uint32_t*>(a.row_sfc + m * (a.N / 32) + int64_t(nt) * 4) = row_sc;
-        if (a.row_sfp)
-          *reinterpret_cast<uint32_t*>(a.row_sfp + (int64_t(mt) * nt_n + nt) * 512 + (r & 31) * 16 + (r >> 5) * 4) =
-              row_sc;
+#pragma unroll
+        for (int c = 0; c < CPW; c++) {
+          const uint8_t v = uint8_t(row_sc >> (8 * c));
+          if (a.row_sfc) a.row_sfc[m * (a.N / 32) + int64_t(nt) * 4 + CPW * part + c] = v;
+          if (a.row_sfp)
+            a.row_sfp[(int64_t(mt) * nt_n + nt) * 512 + (r & 31) * 16 + (r >> 5) * 4 + CPW * part + c] = v;
+        }
       }
     }
   }
