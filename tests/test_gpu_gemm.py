@@ -116,3 +116,25 @@ def test_tensor_peak_probe(mx):
     assert np.all(c > 0)
     rate = 256 * 4 * 128 * 256 * 32 / c
     assert np.all(rate <= 8192 * 1.01) and np.all(rate >= 2048), rate.min()
+
+
+def test_gemm_quant_nan_rows(mx):
+    # a NaN in one element of A makes its quantized block NaN (scale 0xFF), so
+    # that row of Y is NaN: its ROW blocks and the COL blocks holding it carry
+    # scale 0xFF and 0x7F payloads; every other row is exact
+    M, N, K = 256, 256, 256
+    rng = np.random.default_rng(77)
+    a = rng.integers(-8, 9, size=(M, K)).astype(np.float32)
+    b = rng.integers(-8, 9, size=(N, K)).astype(np.float32)
+    a[37, 5] = np.nan
+    res = _run(mx, _bf16(a), _bf16(b))
+    ad = a.astype(np.float64)
+    ad[37, :32] = np.nan  # the whole quantized block of A reads as NaN
+    y, (q_row, s_row), (q_col, s_col) = oracle.method_gemm_quant(ad, b.astype(np.float64))
+    assert np.isnan(y[37]).all() and not np.isnan(np.delete(y, 37, axis=0)).any()
+    np.testing.assert_array_equal(host(res["row"].sf_compact), s_row)
+    np.testing.assert_array_equal(host(res["row"].data), q_row)
+    np.testing.assert_array_equal(host(res["col"].sf_compact), s_col)
+    np.testing.assert_array_equal(host(res["col"].data), q_col)
+    assert np.all(host(res["row"].sf_compact)[37] == 0xFF) and np.all(host(res["col"].sf_compact)[1] == 0xFF)
+    _check_packed(res, M, N, s_row, s_col)
