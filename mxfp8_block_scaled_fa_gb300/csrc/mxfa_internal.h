@@ -124,6 +124,7 @@ struct FwdArgs {
   float* lse;
   int64_t lse_hstride;  // dense: S, varlen: total_q
   int dense_lse;        // 1: lse[(b*H + h) * S + s]; 0: lse[h * total_q + token]
+  int sched_slot;       // work-counter slot of this launch (set by launch_fwd)
 };
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 
