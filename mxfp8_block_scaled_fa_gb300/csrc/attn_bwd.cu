@@ -348,6 +348,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
   if (bad) {
     // nothing issued; fall through to teardown
   } else if (warp == 0) {
+    warp_converged();
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_q);
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       bwait_raw(BAR(B_KVFULL), 0);
     }
   } else if (warp == 2 || warp == 3) {
+    warp_converged();
     // ------------------------------------------------ key-tile scale atoms
     // Atom word w (bytes 4w..4w+3) holds row r = (w & 3) * 32 + (w >> 2),
     // k-blocks 0..3 in its bytes.  Square scale entry: byte 4 * tb + db.
@@ -400,6 +402,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
     }
     warp_arrive(BAR(B_KCONST), lane);
     if (warp == 2) {
+      warp_converged();
       // -------------------------------------- MMA issuer: dV, dK, dQ^T
       // The whole warp walks the schedule; every tcgen05 operation is issued
       // through a lane elected inside the instruction.
@@ -467,6 +470,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       __syncwarp();
     }
   } else if (warp == 1) {
+    warp_converged();
     // ------------------------------------------------ MMA issuer: S^T, dP^T
     // The whole warp walks the schedule (descriptors and TMEM addresses are
     // warp-uniform) and issues every tcgen05 operation through a lane elected
@@ -522,6 +526,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       __syncwarp();
     }
   } else if (warp >= 4 && warp < 12) {
+    warp_converged();
     // ------------------------------------------------------------ P / dS
     // Load S^T and dP^T of the tile from TMEM, free their columns, form and
     // quantize P and dS, store P^T / dS^T (shared memory, the gradient GEMMs'
@@ -697,6 +702,7 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       }
     }
   } else if (warp >= 12) {
+    warp_converged();
     // ------------------------------------------------------------ dQ drain
     // dQ^T of each tile: TMEM -> shared staging -> one tiled TMA reduce-add
     // into the global accumulator.
