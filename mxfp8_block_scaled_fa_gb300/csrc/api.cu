@@ -82,6 +82,21 @@ bool make_map_acc(CUtensorMap* m, const void* ptr, int64_t tokens, int H, bool h
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor [tokens][H][128] as a 3-D map for stores, box 64 x 1 x 32 (128-byte rows),
+// 128B swizzle.
+bool make_map_bf16_store(CUtensorMap* m, void* ptr, int64_t tokens, int H) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, cuuint64_t(H), cuuint64_t(tokens)};
+  cuuint64_t strides[2] = {256, cuuint64_t(H) * 256};
+  cuuint32_t box[3] = {64, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -151,7 +166,7 @@ mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seq
   FwdArgs a;
   memset(&a, 0, sizeof(a));
   if (!make_map_u8(&a.tm_q, q->data, total_q, H, 128) || !make_map_u8(&a.tm_k, k->data, total_k, H, 128) ||
-      !make_map_u8(&a.tm_v, v->data, total_k, H, 128))
+      !make_map_u8(&a.tm_v, v->data, total_k, H, 128) || !make_map_bf16_store(&a.tm_o, o, total_q, H))
     return MXFA_ERR_CUDA;
   a.sfq = q->sf;
   a.sfk = k->sf;
@@ -176,6 +191,10 @@ mxfa_status fwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, Seq
   a.lse = lse;
   a.dense_lse = dense ? 1 : 0;
   a.lse_hstride = dense ? sq.seqlen : total_q;
+  // Staged TMA stores of O (and one K/V stage fewer) pay off when items are
+  // short, the epilogue being a large share of each item, and cost 1-2% on
+  // long ones: mean key length up to 2048.
+  a.stage_o = total_k <= int64_t(sk.nseq) * 2048 ? 1 : 0;
   return from_cuda(launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -59,31 +59,44 @@ constexpr int kFwdSchedSlots = 64;
 static __device__ unsigned g_fwd_sched[kFwdSchedSlots][2];
 
 namespace fwd {
-constexpr int NS = 4;  // K/V pipeline stages
 constexpr int TILE = 128;
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows x 128 E4M3
+constexpr int NS_MAX = 4;               // K/V pipeline stages at most
 
 // Q_A, Q_B of two work items (slot = item parity), so that the next item's Q
 // lands while this item runs
 constexpr int OFF_Q = 0;                               // [slot][tile]
 constexpr int OFF_K = OFF_Q + 4 * TILE_BYTES;          // NS stages
-constexpr int OFF_V = OFF_K + NS * TILE_BYTES;         // NS stages
-constexpr int OFF_SFQ = OFF_V + NS * TILE_BYTES;       // 4 atoms [slot][tile]
-constexpr int OFF_SFK = OFF_SFQ + 4 * 512;             // NS atoms
-constexpr int OFF_SFV = OFF_SFK + NS * 512;            // NS atoms
-constexpr int OFF_BAR = OFF_SFV + NS * 512;
 enum {
-  B_QFULL = 0, B_QEMPTY = B_QFULL + 2, B_KVFULL = B_QEMPTY + 2, B_KVEMPTY = B_KVFULL + NS,
-  B_SFULL = B_KVEMPTY + NS, B_SLOAD = B_SFULL + 2, B_PFULL = B_SLOAD + 2, B_ODONE = B_PFULL + 2,
-  B_TEAR = B_ODONE + 2, B_IFULL = B_TEAR + 1, B_IEMPTY = B_IFULL + 2, NBAR = B_IEMPTY + 2
+  B_QFULL = 0, B_QEMPTY = B_QFULL + 2, B_SFULL = B_QEMPTY + 2, B_SLOAD = B_SFULL + 2, B_PFULL = B_SLOAD + 2,
+  B_ODONE = B_PFULL + 2, B_TEAR = B_ODONE + 2, B_IFULL = B_TEAR + 1, B_IEMPTY = B_IFULL + 2,
+  B_KVFULL = B_IEMPTY + 2, B_KVEMPTY = B_KVFULL + NS_MAX, NBAR = B_KVEMPTY + NS_MAX
 };
 // item ring (2 entries): the producer publishes each claimed item, the MMA
 // warp and the eight softmax warps release it
 constexpr int ITEM_READERS = 9;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int OFF_ITEMS = OFF_MISC + 16;            // int[2]: claimed item per ring entry (-1: none left)
-constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "forward tiles exceed the shared memory of one CTA");
+// O staging for TMA stores: one area of 32 rows x 64 bf16 columns (128B-swizzled)
+// per softmax warp
+constexpr int OST_BYTES = 32 * 128;
+
+// Shared-memory layout.  STAGE: O leaves through TMA stores staged in shared
+// memory, paid for with one K/V stage (for short items, where the epilogue is
+// a large share of the work); otherwise every thread stores its own O row.
+template <bool STAGE>
+struct Layout {
+  static constexpr int NS = STAGE ? 3 : 4;                 // K/V pipeline stages
+  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;    // NS stages
+  static constexpr int OFF_OST = OFF_V + NS * TILE_BYTES;  // 8 staging areas (STAGE)
+  static constexpr int OFF_SFQ = OFF_OST + (STAGE ? 8 * OST_BYTES : 0);  // 4 atoms [slot][tile]
+  static constexpr int OFF_SFK = OFF_SFQ + 4 * 512;        // NS atoms
+  static constexpr int OFF_SFV = OFF_SFK + NS * 512;       // NS atoms
+  static constexpr int OFF_BAR = OFF_SFV + NS * 512;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_ITEMS = OFF_MISC + 16;          // int[2]: claimed item per ring entry (-1: none left)
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 227 * 1024, "forward tiles exceed the shared memory of one CTA");
+  static_assert(OFF_OST % 1024 == 0, "a 128B-swizzled staging area starts on a 1024-byte boundary");
+};
 
 constexpr uint32_t COL_S = 0, COL_O = 256;                       // + 128 * tile
 constexpr uint32_t SUB_SFP = 32, SUB_SFV = 36, SUB_SFQ = 40, SUB_SFK = 44;  // inside an S region
@@ -171,10 +184,14 @@ __device__ __forceinline__ int64_t tiles_before(const Seqs& s, int g) {
   return acc;
 }
 
-// PCONST: every P block takes the scale a.p_sc_const (the constant-scale mode)
-template <bool PCONST>
+// PCONST: every P block takes the scale a.p_sc_const (the constant-scale mode);
+// STAGE: the shared-memory layout with O staging (see Layout)
+template <bool PCONST, bool STAGE>
 __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using namespace fwd;
+  using L = Layout<STAGE>;
+  constexpr int NS = L::NS, OFF_V = L::OFF_V, OFF_SFQ = L::OFF_SFQ, OFF_SFK = L::OFF_SFK, OFF_SFV = L::OFF_SFV,
+                OFF_BAR = L::OFF_BAR, OFF_MISC = L::OFF_MISC, OFF_ITEMS = L::OFF_ITEMS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -562,6 +579,14 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         const int64_t tok = sq0 + qpos;
         uint16_t* orow = a.o + (tok * a.H + h) * 128;
         uint32_t sfw = 0;  // E8M0 scales of the MXFP8 O row, one byte per 32 columns
+        // STAGE: a warp whose 32 rows all lie inside the sequence sends O out
+        // by TMA stores of 32-row x 64-column halves staged in shared memory
+        // (128B-swizzled rows); one thread per row storing its own 256 bytes
+        // touches 32 rows 2H KB apart per instruction, which makes the
+        // epilogue about as long as two key-tile steps.  Other warps store
+        // row by row.
+        const bool staged = STAGE && __all_sync(0xFFFFFFFFu, valid);
+        const uint32_t ost = base + L::OFF_OST + uint32_t(warp - 4) * OST_BYTES;
   #pragma unroll
         for (int c = 0; c < 4; c++) {
           uint32_t o[32];
@@ -580,7 +605,27 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
                                                       __uint_as_float(o[2 * e + 1]) * r);
             w[e] = *reinterpret_cast<uint32_t*>(&p2);
           }
-          if (valid) {
+          if (staged) {
+            // the previous store from this area has read it
+            if ((c & 1) == 0) {
+              if (lane == 0) bulk_wait_read0();
+              __syncwarp();
+            }
+  #pragma unroll
+            for (int v4 = 0; v4 < 4; v4++) {
+              const uint32_t chunk = uint32_t((c & 1) * 4 + v4) ^ uint32_t(lane & 7);
+              st_shared_v4(ost + uint32_t(lane) * 128u + (chunk << 4), w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                           w[4 * v4 + 3]);
+            }
+            if (c & 1) {
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&a.tm_o, ost, 64 * (c >> 1), h, int(sq0 + qpos - lane));
+                bulk_commit();
+              }
+            }
+          } else if (valid) {
   #pragma unroll
             for (int v4 = 0; v4 < 4; v4++)
               *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v4) =
@@ -614,6 +659,9 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
       }
       st += nkv_x;
     }
+    // every O store of this warp has completed before the CTA exits
+    if (STAGE && lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -635,11 +683,15 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> attr{0};
   clear_stale_error();
   cudaError_t e = once_per_device(attr, [] {
-    cudaError_t r = cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         fwd::SMEM_BYTES);
-    if (r != cudaSuccess) return r;
-    return cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fwd::SMEM_BYTES);
+    const cudaFuncAttribute smem = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t r = cudaFuncSetAttribute(attn_fwd_kernel<false, false>, smem, fwd::Layout<false>::SMEM_BYTES);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_fwd_kernel<true, false>, smem, fwd::Layout<false>::SMEM_BYTES);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_fwd_kernel<false, true>, smem, fwd::Layout<true>::SMEM_BYTES);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_fwd_kernel<true, true>, smem, fwd::Layout<true>::SMEM_BYTES);
+    return r;
   });
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (fewer when there are fewer items); each CTA
@@ -654,10 +706,15 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   static std::atomic<unsigned> launches{0};
   FwdArgs b = a;
   b.sched_slot = int(launches.fetch_add(1u) % unsigned(kFwdSchedSlots));
-  if (b.p_sc_const)
-    attn_fwd_kernel<true><<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(b);
+  const int sb = b.stage_o ? fwd::Layout<true>::SMEM_BYTES : fwd::Layout<false>::SMEM_BYTES;
+  if (b.p_sc_const && b.stage_o)
+    attn_fwd_kernel<true, true><<<grid, fwd::NTHREADS, sb, st>>>(b);
+  else if (b.p_sc_const)
+    attn_fwd_kernel<true, false><<<grid, fwd::NTHREADS, sb, st>>>(b);
+  else if (b.stage_o)
+    attn_fwd_kernel<false, true><<<grid, fwd::NTHREADS, sb, st>>>(b);
   else
-    attn_fwd_kernel<false><<<grid, fwd::NTHREADS, fwd::SMEM_BYTES, st>>>(b);
+    attn_fwd_kernel<false, false><<<grid, fwd::NTHREADS, sb, st>>>(b);
   return cudaGetLastError();
 }
 

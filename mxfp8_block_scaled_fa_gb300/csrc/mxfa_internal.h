@@ -106,6 +106,7 @@ cudaError_t launch_rmsnorm_quant(const RmsArgs& a, cudaStream_t s);
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // u8 [tokens][H][128], box 128 x 1 x 128, 128B swizzle
+  CUtensorMap tm_o;              // bf16 O [tokens][H][128], box 64 x 1 x 32, 128B swizzle (stores)
   const uint8_t* sfq;  // packed ROW atoms
   const uint8_t* sfk;  // packed ROW atoms
   const uint8_t* sfv;  // packed COL atoms
@@ -125,6 +126,7 @@ struct FwdArgs {
   int64_t lse_hstride;  // dense: S, varlen: total_q
   int dense_lse;        // 1: lse[(b*H + h) * S + s]; 0: lse[h * total_q + token]
   int sched_slot;       // work-counter slot of this launch (set by launch_fwd)
+  int stage_o;          // 1: O leaves through TMA stores staged in the item's Q tiles (short items)
 };
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 
