@@ -239,7 +239,8 @@ mxfa_status bwd_common(const mxfa_mx* q, const mxfa_mx* k, const mxfa_mx* v, con
   BwdArgs a;
   memset(&a, 0, sizeof(a));
   if (!make_map_u8(&a.tm_q, q->data, total_q, H, 64) || !make_map_u8(&a.tm_do, dmx->data, total_q, H, 64) ||
-      !make_map_u8(&a.tm_k, k->data, total_k, H, 128) || !make_map_u8(&a.tm_v, v->data, total_k, H, 128))
+      !make_map_u8(&a.tm_k, k->data, total_k, H, 128) || !make_map_u8(&a.tm_v, v->data, total_k, H, 128) ||
+      !make_map_bf16_store(&a.tm_dk, dk, total_k, H) || !make_map_bf16_store(&a.tm_dv, dv, total_k, H))
     return MXFA_ERR_CUDA;
   a.sfq = q->sf;
   a.sfk = k->sf;

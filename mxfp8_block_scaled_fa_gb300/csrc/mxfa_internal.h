@@ -133,6 +133,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // u8 payloads; q/do boxes 128 x 1 x 64
   CUtensorMap tm_dqacc;                 // dQ accumulator (fp32 / fp16), box 128 x 1 x 64
+  CUtensorMap tm_dk, tm_dv;             // bf16 dK, dV [tokens][H][128], box 64 x 1 x 32, 128B swizzle (stores)
   const uint8_t* sfq;   // packed SQ (16 B per tile and head)
   const uint8_t* sfk;   // packed SQ
   const uint8_t* sfv;   // packed ROW atoms
