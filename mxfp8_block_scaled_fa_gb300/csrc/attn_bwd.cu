@@ -103,6 +103,20 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   int64_t s0;
   int L;
   seq_info(a.sq, g, s0, L);
+  const int esz = a.dq_mode == 1 ? 2 : 4;
+  // zero dQ accumulator rows [r0, r1) of head h (16-byte chunks)
+  auto zero_rows = [&](int64_t r0, int64_t r1) {
+    const int chunks = 128 * esz / 16;
+    for (int64_t i = threadIdx.x; i < (r1 - r0) * chunks; i += 256) {
+      uint8_t* row = reinterpret_cast<uint8_t*>(a.dq_acc) + ((r0 + i / chunks) * a.H + h) * 128 * esz;
+      *reinterpret_cast<uint4*>(row + 16 * (i % chunks)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  // tokens outside every sequence (before the first, after the last) get dQ = 0
+  if (a.sq.cu != nullptr && t == 0) {
+    if (g == 0) zero_rows(0, __ldg(a.sq.cu));
+    if (g == a.sq.nseq - 1) zero_rows(__ldg(a.sq.cu + a.sq.nseq), a.total_q);
+  }
   if (t * QT >= L) return;
   const int64_t t128 = seq_units_before_warp(a.sq, g, 128, threadIdx.x & 31) + t / 2;
   if (t128 >= a.ptiles_q) {
@@ -116,26 +130,40 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a) {
   auto pick = [](uint4 e, int tb) { return tb == 0 ? e.x : tb == 1 ? e.y : tb == 2 ? e.z : e.w; };
   const int tb0 = (t & 1) * 2;
   float* ndelta = reinterpret_cast<float*>(rec + REC_NDELTA);
-  for (int r = warp * 8; r < warp * 8 + 8; r++) {
-    const int q = t * QT + r;
-    float d = 0.0f;
+  // the warp's eight rows: every load in flight first, then the dot products
+  uint2 ov[8];
+  uint32_t dq4[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int q = t * QT + warp * 8 + i;
+    ov[i] = make_uint2(0u, 0u);
+    dq4[i] = 0u;
     if (q < L) {
       const int64_t off = ((s0 + q) * a.H + h) * 128 + lane * 4;
-      const uint2 ov = *reinterpret_cast<const uint2*>(a.o + off);
-      // dO^ of these four columns: E4M3 codes times the 32x32 block scale of
-      // (query block tb0 + r / 32, d block lane / 8)
-      const uint32_t dq4 = *reinterpret_cast<const uint32_t*>(a.do_q + off);
-      const uint32_t sb = (pick(d4, tb0 + (r >> 5)) >> (8 * (lane >> 3))) & 0xFFu;
-      const float f = e8m0_value(sb);
-      const float2 d01 = e4m3x2_to_float2(dq4 & 0xFFFFu), d23 = e4m3x2_to_float2(dq4 >> 16);
-      auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
-      auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-      d = lo(ov.x) * (d01.x * f) + hi(ov.x) * (d01.y * f) + lo(ov.y) * (d23.x * f) + hi(ov.y) * (d23.y * f);
-#pragma unroll
-      for (int off2 = 16; off2 >= 1; off2 >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off2);
+      ov[i] = *reinterpret_cast<const uint2*>(a.o + off);
+      dq4[i] = *reinterpret_cast<const uint32_t*>(a.do_q + off);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int r = warp * 8 + i;
+    // dO^ of these four columns: E4M3 codes times the 32x32 block scale of
+    // (query block tb0 + r / 32, d block lane / 8); rows past the sequence
+    // hold zeros
+    const uint32_t sb = (pick(d4, tb0 + (r >> 5)) >> (8 * (lane >> 3))) & 0xFFu;
+    const float f = e8m0_value(sb);
+    const float2 d01 = e4m3x2_to_float2(dq4[i] & 0xFFFFu), d23 = e4m3x2_to_float2(dq4[i] >> 16);
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+    float d = lo(ov[i].x) * (d01.x * f) + hi(ov[i].x) * (d01.y * f) + lo(ov[i].y) * (d23.x * f) +
+              hi(ov[i].y) * (d23.y * f);
+#pragma unroll
+    for (int off2 = 16; off2 >= 1; off2 >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off2);
     if (lane == 0) ndelta[r] = -d;
   }
+  // the dQ accumulator rows of this tile start at zero (each token row of a
+  // sequence belongs to exactly one (64-query tile, head))
+  zero_rows(s0 + t * QT, s0 + t * QT + min(QT, L - t * QT));
   if (tid < QT) {
     const int q = t * QT + tid;
     float nl2 = -INFINITY;  // rows past the sequence: P = 2^-inf = 0
@@ -804,12 +832,11 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
                                 bwd::SMEM_BYTES);
   });
   if (e != cudaSuccess) return e;
-  const int64_t rows = a.total_q * a.H;
-  const size_t esz = a.dq_mode == 1 ? 2 : 4;
-  e = cudaMemsetAsync(a.dq_acc, 0, size_t(rows) * 128 * esz, st);
-  if (e != cudaSuccess) return e;
   {
-    dim3 pg(unsigned((a.sq.seqlen + bwd::QT - 1) / bwd::QT), unsigned(a.H), unsigned(a.sq.nseq));
+    // the preparation kernel also zeroes the dQ accumulator
+    // at least one tile per (head, sequence): tile 0 of the first and last
+    // sequences also zeroes the rows outside every sequence
+    dim3 pg(unsigned(max(1, (a.sq.seqlen + bwd::QT - 1) / bwd::QT)), unsigned(a.H), unsigned(a.sq.nseq));
     if (pg.x > 0) bwd_prep_kernel<<<pg, 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -835,7 +862,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     attn_bwd_kernel<<<grid, bwd::NTHREADS, bwd::SMEM_BYTES, st>>>(args);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  const int64_t n = rows * 128;
+  const int64_t n = a.total_q * a.H * 128;
   const float mult = a.dq_mode == 1 ? 1.0f / a.dq_static_scale : a.scale;
   if (a.dqmx == nullptr) {
     bwd_post_kernel<<<unsigned((n + 2047) / 2048), 256, 0, st>>>(a.dq_acc, a.dq, n, a.dq_mode, mult);
@@ -846,7 +873,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       PackArgs p;
       p.sf_compact = a.dqmx_sfc;
-      p.tokens = rows / a.H;
+      p.tokens = a.total_q;
       p.H = a.H;
       p.D = 128;
       p.mode = 0;
