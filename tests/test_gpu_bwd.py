@@ -131,6 +131,44 @@ def test_bwd_varlen_empty_sequences(mx):
     check(got, ref)
 
 
+def test_bwd_rows_outside_sequences(mx):
+    # query tokens after the last sequence (total_q > cu_seqlens_q[nseq]) belong
+    # to no sequence: their dQ rows are 0 whatever the workspace held before,
+    # and the other rows are unchanged
+    import dataclasses
+    import torch
+    H, D, extra = 2, 128, 24
+    lq, lk = [70, 130], [90, 40]
+    qb, kb, vb, dob, cu_q, cu_k = inputs.varlen_attn(lq, lk, H, D, seed=35)
+    scale = 1 / math.sqrt(D)
+    o_bits, o_bf, lse = oracle_fwd_out(f64(qb), f64(kb), f64(vb), cu_q, cu_k, scale, False)
+    ref = oracle.method_bwd(f64(qb), f64(kb), f64(vb), f64(dob), o_bf, lse, cu_q, cu_k, scale,
+                            False, True)
+    total = sum(lq)
+    sq = mx.Seqs.varlen(lq, "cuda")
+    sk = mx.Seqs.varlen(lk, "cuda")
+    sq_pad = dataclasses.replace(sq, total=total + extra)
+    pad = lambda t: torch.cat([t, torch.zeros((extra,) + tuple(t.shape[1:]), dtype=t.dtype, device=t.device)])
+    q = mx.quantize(to_dev(qb), mx.SQ, sq)
+    dmx = mx.quantize(to_dev(dob), mx.SQ, sq)
+    q = mx.Mx(pad(q.data), q.sf_compact, q.sf_packed, q.blk)
+    dmx = mx.Mx(pad(dmx.data), dmx.sf_compact, dmx.sf_packed, dmx.blk)
+    k = mx.quantize(to_dev(kb), mx.SQ, sk)
+    v = mx.quantize(to_dev(vb), mx.ROW, sk)
+    o_t = pad(to_dev(o_bits).reshape(-1, H, D))
+    do_t = pad(to_dev(dob).reshape(-1, H, D))
+    lse_pad = np.concatenate([lse.reshape(H, total), np.zeros((H, extra))], axis=1).astype(np.float32)
+    wsb = mx.mxfa_bwd_workspace_size(total + extra, sq.nseq, H, D, 0)
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN bytes
+    dq, dk, dv = mx.attention_bwd(q, k, v, dmx, o_t, do_t, torch.from_numpy(lse_pad).cuda(), sq_pad, sk,
+                                  scale, False, ws=ws)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    got = [host(t.float()).astype(np.float64) for t in (dq, dk, dv)]
+    assert np.all(got[0][total:] == 0)
+    check([got[0][:total], got[1], got[2]], ref, "rows outside sequences")
+
+
 @pytest.mark.parametrize("varlen", [False, True])
 def test_bwd_constant_p_scale(mx, varlen):
     # P^T quantized with the constant scale 2^-8 instead of each block's own,
