@@ -245,6 +245,33 @@ class GpuStep:
         return t0.elapsed_time(t1) / steps
 
 
+def host_link_probe(torch, st, iters=10):
+    """The host link's ceiling for the end-to-end figure: the same pinned
+    host <-> device copies as one end-to-end step (Q, K, V, dO in; O, dQ, dK,
+    dV out), both directions at once on their own streams and nothing else on
+    the GPU.  Returns (ms per step, GB/s per direction)."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    dev_in = [torch.empty_like(t, device=st.dev) for t in st.host_in]
+    dev_out = [st.o, st.dq, st.dk, st.dv]
+    cur = torch.cuda.current_stream()
+
+    def once():
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            for d, h in zip(dev_in, st.host_in):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in zip(st.host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    ms = time_loop(torch, once, iters, 2)
+    nbytes = sum(t.numel() * t.element_size() for t in st.host_in)
+    return ms, nbytes / ms / 1e6
+
+
 def time_loop(torch, fn, iters, warmup, flush=None):
     """Mean per-call device time (ms) with CUDA events on the current stream."""
     for _ in range(warmup):
@@ -891,6 +918,8 @@ def main():
     barrier()
     ms_e2e = st.e2e(args.steps)
     barrier()
+    ms_link, link_gbs = host_link_probe(torch, st)
+    barrier()
     if world > 1:
         ms, ms_e2e = slowest_rank(torch, dist, [ms, ms_e2e], dev)
     assert mxfa.device_status() == 0, "device status after timing"
@@ -922,7 +951,11 @@ def main():
                     "ms_per_step": ms_e2e, "h2d_bytes_per_step": bytes_io,
                     "overlap": "copy-in of step i+1 and copy-out of step i-1 on their own "
                                "streams during step i (double-buffered device tensors)",
-                    "d2h_bytes_per_step": bytes_io},
+                    "d2h_bytes_per_step": bytes_io,
+                    "host_link": {"ms_per_step": ms_link, "GB_s_per_direction": link_gbs,
+                                  "frac": ms_link / ms_e2e,
+                                  "how": "the same pinned copies in and out of one step, both "
+                                         "directions at once, nothing else on the GPU"}},
             "gpu_launches": st.launches_per_step * args.steps,
             "clocks": clk,
             "sustained": {"steps": n_sus, "ms_per_step": ms_sus,

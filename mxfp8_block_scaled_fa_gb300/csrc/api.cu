@@ -97,6 +97,22 @@ bool make_map_bf16_store(CUtensorMap* m, void* ptr, int64_t tokens, int H) {
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor [tokens][H][128] as a 3-D map for loads, box 128 x heads x 32
+// (32 rows of `heads` adjacent heads), no swizzle; rows and heads past the
+// tensor read 0.
+bool make_map_bf16_rows(CUtensorMap* m, const void* ptr, int64_t tokens, int H, int heads) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, cuuint64_t(H), cuuint64_t(tokens)};
+  cuuint64_t strides[2] = {256, cuuint64_t(H) * 256};
+  cuuint32_t box[3] = {128, cuuint32_t(heads), 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -378,6 +394,8 @@ mxfa_status mxfa_quantize_dual(const void* x, int64_t tokens, int H, int D, mxfa
   a.row_sfc = out_row->sf_compact;
   a.row_sfp = out_row->sf_packed;
   if (tokens == 0) return MXFA_OK;
+  // dense batches of at least one unit's heads take the streaming kernel
+  a.has_map = (!cu && H >= kQuantHeadsPerUnit && make_map_bf16_rows(&a.tm_x, x, tokens, H, kQuantHeadsPerUnit)) ? 1 : 0;
   return from_cuda(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -58,7 +58,13 @@ struct QuantArgs {
   uint8_t* row_data;
   uint8_t* row_sfc;
   uint8_t* row_sfp;
+  // dense batches (seq.cu == nullptr) with two outputs: x as bf16
+  // [tokens][H][128], box 128 x kQuantHeadsPerUnit x 32, no swizzle, for the
+  // streaming kernel; has_map = 0 selects the register-staged kernels
+  CUtensorMap tm_x;
+  int has_map;
 };
+constexpr int kQuantHeadsPerUnit = 2;
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 
 // Lower-precision quantization (MXFP4, MXFP6, NVFP4) of bf16 x[rows][cols]

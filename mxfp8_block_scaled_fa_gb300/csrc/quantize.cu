@@ -35,6 +35,22 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
 }
 
 
+// The eight bf16 of a 16-byte word group as four fp32 pairs (exact).
+__device__ __forceinline__ void unpack8(uint4 v, float2* p) {
+  p[0] = make_float2(bf_lo(v.x), bf_hi(v.x));
+  p[1] = make_float2(bf_lo(v.y), bf_hi(v.y));
+  p[2] = make_float2(bf_lo(v.z), bf_hi(v.z));
+  p[3] = make_float2(bf_lo(v.w), bf_hi(v.w));
+}
+// Four fp32 pairs times power-of-two inverse scales (packed multiplies, exact
+// unless the product leaves the fp32 range) -> eight E4M3 bytes, first
+// element in the low byte.
+__device__ __forceinline__ uint2 conv8(const float2* p, const float2* inv) {
+  const float2 a = fmul2(p[0], inv[0]), b = fmul2(p[1], inv[1]);
+  const float2 c = fmul2(p[2], inv[2]), d = fmul2(p[3], inv[3]);
+  return make_uint2(pack4_e4m3(a.x, a.y, b.x, b.y), pack4_e4m3(c.x, c.y, d.x, d.y));
+}
+
 // ------------------------------------------------------------------ quantize
 // ROW alone (1x32 blocks along D): one thread per (row, 32-column block)
 // with the block's 64 bytes in registers, so the block maximum needs no
@@ -129,8 +145,8 @@ __global__ void __launch_bounds__(128) quant_row_kernel(QuantArgs a) {
 // bytes per head) are written a byte per block.  Rows past a sequence end in its last tile carry padding scale
 // bytes 0x7F in the atoms and no payload.
 // grid (ceil(cols / 256), ceil(max_len / 128), nseq), block 128.
-template <int MODE>
-__global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
+template <int MODE, bool ROWOUT>
+__global__ void __launch_bounds__(128, 3) quant_kernel(QuantArgs a) {
   static_assert(MODE == 1 || MODE == 2, "ROW alone runs in quant_row_kernel");
   __shared__ __align__(16) uint8_t s_blk[2][512];  // COL atoms (MODE 1)
   __shared__ __align__(16) uint8_t s_row[2][512];  // ROW atoms
@@ -149,8 +165,6 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
   const int nr = min(32, L - rb * 32);  // real rows of the block (<= 0: padding block)
   const int64_t r0 = s0 + int64_t(rb) * 32;
   const bool lead = (lane & 3) == 0;    // first lane of a 32-column quad
-  const bool row_out = a.row_data != nullptr;
-  uint8_t* row_data = a.row_data;
   uint8_t* row_sfc = a.row_sfc;
   uint8_t* row_sfp = a.row_sfp;
   uint8_t* blk_sfp = a.sf_packed;
@@ -168,100 +182,114 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
   for (int r = 0; r < 32; r++)
     v[r] = (r < nr && cvalid) ? ldg16(a.x + (r0 + r) * cols + col0) : make_uint4(0, 0, 0, 0);
 
-  {
-    // per-column maxima over the 32 rows (pairs of columns per word)
-    uint32_t cm[4] = {0, 0, 0, 0};
+  // ---- first pass, row by row as the loads land.  COL / SQ: per-column
+  // maxima over the 32 rows (pairs of columns per word).  ROW (ROWOUT): the
+  // row's 1x32 block is the lane quad's 32 columns (two butterfly steps); its
+  // payload is written at once and its scale byte goes into the tile's ROW
+  // atom (rows past the sequence: padding 0x7F).
+  uint32_t cm[4] = {0, 0, 0, 0};
+  uint8_t* rdst = ROWOUT ? a.row_data + r0 * cols + col0 : nullptr;
 #pragma unroll
-    for (int r = 0; r < 32; r++) {
-      cm[0] = __vmaxu2(cm[0], abs2(v[r].x));
-      cm[1] = __vmaxu2(cm[1], abs2(v[r].y));
-      cm[2] = __vmaxu2(cm[2], abs2(v[r].z));
-      cm[3] = __vmaxu2(cm[3], abs2(v[r].w));
+  for (int r = 0; r < 32; r++) {
+    const uint32_t ax = abs2(v[r].x), ay = abs2(v[r].y), az = abs2(v[r].z), aw = abs2(v[r].w);
+    cm[0] = __vmaxu2(cm[0], ax);
+    cm[1] = __vmaxu2(cm[1], ay);
+    cm[2] = __vmaxu2(cm[2], az);
+    cm[3] = __vmaxu2(cm[3], aw);
+    if (ROWOUT) {
+      uint32_t t = __vmaxu2(__vmaxu2(ax, ay), __vmaxu2(az, aw));
+      t = __vmaxu2(t, __shfl_xor_sync(0xFFFFFFFFu, t, 1));
+      t = __vmaxu2(t, __shfl_xor_sync(0xFFFFFFFFu, t, 2));
+      const uint32_t sc = e8m0_from_bf16abs(hmax2(t));
+      if (r < nr && cvalid) {
+        float2 p[4];
+        unpack8(v[r], p);
+        const float f = e8m0_inv_scale(sc);
+        const float2 fi[4] = {make_float2(f, f), make_float2(f, f), make_float2(f, f), make_float2(f, f)};
+        uint2 o = conv8(p, fi);
+        if (sc == 0xFFu) o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        *reinterpret_cast<uint2*>(rdst + int64_t(r) * cols) = o;
+      }
+      if (lead && cvalid) s_row[hh][atom_off(w * 32 + r, dcol / 32)] = r < nr ? uint8_t(sc) : uint8_t(0x7F);
     }
-    uint32_t s[8];
+  }
+  uint32_t s[8];
+  if (MODE == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      s[2 * i] = e8m0_from_bf16abs(cm[i] & 0xFFFFu);
+      s[2 * i + 1] = e8m0_from_bf16abs(cm[i] >> 16);
+    }
+  } else {
+    uint32_t m = max(max(hmax2(cm[0]), hmax2(cm[1])), max(hmax2(cm[2]), hmax2(cm[3])));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    const uint32_t sb = e8m0_from_bf16abs(m);
+#pragma unroll
+    for (int i = 0; i < 8; i++) s[i] = sb;
+  }
+  // inverse scales per column pair, and a byte mask of the columns whose
+  // block holds Inf / NaN (their bytes are written 0x7F)
+  float2 inv2[4];
+  uint2 badm = make_uint2(0, 0);
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const bool bad = s[i] == 0xFFu;
+    const float f = bad ? 0.0f : e8m0_inv_scale(s[i]);
+    if (i & 1) inv2[i >> 1].y = f; else inv2[i >> 1].x = f;
+    if (bad) {
+      if (i < 4) badm.x |= 0xFFu << (8 * i); else badm.y |= 0xFFu << (8 * (i - 4));
+    }
+  }
+  if (nr > 0 && cvalid && a.sf_compact) {
+    const int64_t b32 = seq_units_before(a.seq, g, 32) + rb;
+    if (MODE == 1) {
+      uint2 sv;
+      sv.x = s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
+      sv.y = s[4] | (s[5] << 8) | (s[6] << 16) | (s[7] << 24);
+      *reinterpret_cast<uint2*>(a.sf_compact + b32 * cols + col0) = sv;
+    } else if (lead) {
+      a.sf_compact[b32 * (cols / 32) + col0 / 32] = uint8_t(s[0]);
+    }
+  }
+  // this block's bytes of the tile's COL / SQ atoms (padding blocks: 0x7F)
+  if (blk_sfp && cvalid) {
     if (MODE == 1) {
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        s[2 * i] = e8m0_from_bf16abs(cm[i] & 0xFFFFu);
-        s[2 * i + 1] = e8m0_from_bf16abs(cm[i] >> 16);
-      }
-    } else {
-      uint32_t m = max(max(hmax2(cm[0]), hmax2(cm[1])), max(hmax2(cm[2]), hmax2(cm[3])));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const uint32_t sb = e8m0_from_bf16abs(m);
-#pragma unroll
-      for (int i = 0; i < 8; i++) s[i] = sb;
-    }
-    if (nr > 0 && cvalid) {
-      bool bad[8];
-      float inv[8];
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        bad[i] = s[i] == 0xFFu;
-        inv[i] = bad[i] ? 0.0f : e8m0_inv_scale(s[i]);
-      }
-#pragma unroll
-      for (int r = 0; r < 32; r++) {
-        if (r < nr) {
-          uint2 out = cvt8(v[r], inv);
-          uint8_t* ob = reinterpret_cast<uint8_t*>(&out);
-#pragma unroll
-          for (int i = 0; i < 8; i++)
-            if (bad[i]) ob[i] = 0x7F;
-          *reinterpret_cast<uint2*>(a.data + (r0 + r) * cols + col0) = out;
-        }
-      }
-      if (a.sf_compact) {
-        const int64_t b32 = seq_units_before(a.seq, g, 32) + rb;
-        if (MODE == 1) {
-          uint2 sv;
-          sv.x = s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
-          sv.y = s[4] | (s[5] << 8) | (s[6] << 16) | (s[7] << 24);
-          *reinterpret_cast<uint2*>(a.sf_compact + b32 * cols + col0) = sv;
-        } else if (lead) {
-          a.sf_compact[b32 * (cols / 32) + col0 / 32] = uint8_t(s[0]);
-        }
-      }
-    }
-    // this block's bytes of the tile's atoms (padding blocks: 0x7F)
-    if (blk_sfp && cvalid) {
-      if (MODE == 1) {
-#pragma unroll
-        for (int i = 0; i < 8; i++) s_blk[hh][atom_off(dcol + i, w)] = nr > 0 ? uint8_t(s[i]) : uint8_t(0x7F);
-      } else if (lead) {
-        // an SQ atom is 16 bytes per (tile, head): one byte per quad, direct
-        blk_sfp[(tile_g * a.H + blockIdx.x * 2 + hh) * 16 + w * 4 + dcol / 32] =
-            nr > 0 ? uint8_t(s[0]) : uint8_t(0x7F);
-      }
+      for (int i = 0; i < 8; i++) s_blk[hh][atom_off(dcol + i, w)] = nr > 0 ? uint8_t(s[i]) : uint8_t(0x7F);
+    } else if (lead) {
+      // an SQ atom is 16 bytes per (tile, head): one byte per quad, direct
+      blk_sfp[(tile_g * a.H + blockIdx.x * 2 + hh) * 16 + w * 4 + dcol / 32] = nr > 0 ? uint8_t(s[0]) : uint8_t(0x7F);
     }
   }
-  if (row_out) {
-    // 1x32 blocks along D: a row's 32-column block is the lane quad's
+  // ---- second pass: the block layout's payload
+  uint8_t* dst = a.data + r0 * cols + col0;
+  const bool anybad = (badm.x | badm.y) != 0u;
 #pragma unroll
-    for (int r = 0; r < 32; r++) {
-      uint32_t m = max(max(hmax2(abs2(v[r].x)), hmax2(abs2(v[r].y))), max(hmax2(abs2(v[r].z)), hmax2(abs2(v[r].w))));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      const uint32_t sc = e8m0_from_bf16abs(m);
-      if (r < nr && cvalid) {
-        uint2 out;
-        if (sc == 0xFFu) {
-          out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-          float inv[8];
-          const float f = e8m0_inv_scale(sc);
-#pragma unroll
-          for (int i = 0; i < 8; i++) inv[i] = f;
-          out = cvt8(v[r], inv);
-        }
-        *reinterpret_cast<uint2*>(row_data + (r0 + r) * cols + col0) = out;
-        if (lead && row_sfc) row_sfc[(r0 + r) * (cols / 32) + col0 / 32] = uint8_t(sc);
+  for (int r = 0; r < 32; r++) {
+    if (r < nr && cvalid) {
+      float2 p[4];
+      unpack8(v[r], p);
+      uint2 o = conv8(p, inv2);
+      if (anybad) {
+        o.x = (o.x & ~badm.x) | (0x7F7F7F7Fu & badm.x);
+        o.y = (o.y & ~badm.y) | (0x7F7F7F7Fu & badm.y);
       }
-      if (lead && row_sfp && cvalid) s_row[hh][atom_off(w * 32 + r, dcol / 32)] = r < nr ? uint8_t(sc) : uint8_t(0x7F);
+      *reinterpret_cast<uint2*>(dst + int64_t(r) * cols) = o;
     }
   }
-  if (!row_sfp && !(MODE == 1 && blk_sfp)) return;
+  if (ROWOUT && row_sfc) {
+    // compact ROW scales: lane = row of this warp's block; the row's four
+    // k-block bytes of a head are one word of the head's atom
+    __syncwarp();
+    if (lane < nr) {
+      uint8_t* cdst = row_sfc + (r0 + lane) * (cols / 32) + blockIdx.x * 8;
+      *reinterpret_cast<uint32_t*>(cdst) = *reinterpret_cast<const uint32_t*>(&s_row[0][atom_off(w * 32 + lane, 0)]);
+      if (blockIdx.x * 256 + 128 < cols)
+        *reinterpret_cast<uint32_t*>(cdst + 4) = *reinterpret_cast<const uint32_t*>(&s_row[1][atom_off(w * 32 + lane, 0)]);
+    }
+  }
+  if (!(ROWOUT && row_sfp) && !(MODE == 1 && blk_sfp)) return;
   __syncthreads();
   // the tile's atoms, whole, as 16-byte stores: threads 0-63 COL's (2 heads x
   // 32 chunks), 64-127 ROW's
@@ -271,14 +299,259 @@ __global__ void __launch_bounds__(128) quant_kernel(QuantArgs a) {
   if (MODE == 1 && blk_sfp && t < 64 && hd < a.H)
     *reinterpret_cast<uint4*>(blk_sfp + (tile_g * a.H + hd) * 512 + chunk * 16) =
         *reinterpret_cast<const uint4*>(&s_blk[head][chunk * 16]);
-  if (row_sfp && t >= 64 && hd < a.H)
+  if (ROWOUT && row_sfp && t >= 64 && hd < a.H)
     *reinterpret_cast<uint4*>(row_sfp + (tile_g * a.H + hd) * 512 + chunk * 16) =
         *reinterpret_cast<const uint4*>(&s_row[head][chunk * 16]);
+}
+
+// --------------------------------------------- streaming quantizer (dense)
+// The one-read, two-output quantization (COL or SQ, plus ROW) of dense batches
+// (every sequence seqlen rows, back to back: the training step's Q, K, V).
+// One CTA per SM walks units of 32 rows x HPU heads: a 32-row block of one
+// sequence, the padding blocks of a sequence's last 128-row tile included
+// (those write padding scale bytes only).  A producer thread brings each unit
+// into a ring of shared-memory stages with one TMA copy; twelve consumer
+// warps, HPU to a unit (one head each), read their head from shared memory
+// twice -- first pass: the COL / SQ maxima, and the ROW output whole (its
+// blocks lie within a row); second pass: the COL / SQ payload -- and hand the
+// stage back.  The copies of later units stay in flight while earlier ones are
+// converted.  The register-staged kernel above holds a block in registers for
+// its whole life, which caps it at three CTAs per SM, mostly waiting on their
+// loads, and two outputs per read double its arithmetic; with one output it
+// keeps up with this one and serves that case.  Lane l of a consumer takes
+// rows 16 (l / 16) .. +15 of the unit and columns 8 (l % 16) .. +7 of its
+// head: a 32-column block is a lane quad, a column's 32 rows two lanes 16
+// apart.
+// Consumer group c (HPU warps) takes units j = c, c + NCG, ... and owns
+// stages 2c and 2c + 1, which its units alternate: stage(j) = 2 (j % NCG) +
+// (j / NCG) % 2, the k-th unit of a stage being j / NST.  Every waiter on a
+// stage therefore finished the previous unit of that stage itself, so its
+// parity wait can never be met by the phase before the one it wants (which
+// a stage shared round-robin among more waiters than the ring is deep
+// allows).
+namespace qst {
+constexpr int HPU = kQuantHeadsPerUnit;  // heads per unit (TMA box 128 x HPU x 32)
+constexpr int NCG = 12 / HPU;             // consumer groups
+constexpr int NCW = NCG * HPU;            // consumer warps
+constexpr int NTHREADS = 32 * (NCW + 1);  // + the producer warp
+constexpr int NST = 2 * NCG;              // stages, two per group
+constexpr int ROW_BYTES = 256 * HPU;      // HPU heads of 128 bf16
+constexpr int STAGE_BYTES = 32 * ROW_BYTES;
+constexpr int OFF_BAR = NST * STAGE_BYTES;  // full[NST], empty[NST]
+constexpr int SMEM_BYTES = OFF_BAR + 2 * NST * 8;
+}  // namespace qst
+
+// MODE 1: COL, MODE 2: SQ (into data / sf_compact / sf_packed), each with ROW
+// (into row_data / row_sfc / row_sfp).
+template <int MODE>
+__global__ void __launch_bounds__(qst::NTHREADS, 1) quant_stream_kernel(const __grid_constant__ QuantArgs a) {
+  static_assert(MODE == 1 || MODE == 2, "COL or SQ, with ROW");
+  extern __shared__ __align__(128) uint8_t qs_smem[];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, cols = H * 128;
+  const int L = a.seq.seqlen;
+  const int ntile = (L + 127) / 128;
+  const int nrb = 4 * ntile;  // 32-row blocks per sequence, padding blocks included
+  const int NHU = (H + qst::HPU - 1) / qst::HPU;  // units per 32-row block
+  const int64_t units = int64_t(a.seq.nseq) * nrb * NHU;
+  const uint32_t base = smem_u32(qs_smem);
+  const uint32_t bar0 = base + qst::OFF_BAR;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < qst::NST; s++) {
+      mbar_init(bar0 + 8u * s, 1);                         // full: the producer
+      mbar_init(bar0 + 8u * (qst::NST + s), qst::HPU);     // empty: the group's warps
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto stage = [](int64_t j) { return int(2 * (j % qst::NCG) + ((j / qst::NCG) & 1)); };
+  if (warp == 0) {
+    // ---- producer (lane 0): heads fastest, so that consecutive units cover
+    // whole rows
+    if (lane != 0) return;
+    tma_prefetch_desc(&a.tm_x);
+    int64_t j = 0;  // units issued
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, j++) {
+      const int s = stage(j);
+      if (j >= qst::NST &&
+          !mbar_wait(bar0 + 8u * (qst::NST + s), uint32_t((j / qst::NST - 1) & 1), &abort_flag, &g_status_quant))
+        break;
+      const int hd = qst::HPU * int(u % NHU);
+      const int64_t rbg = u / NHU;
+      const int g = int(rbg / nrb), rb = int(rbg % nrb);
+      const bool load = 32 * rb < L;  // padding blocks bring nothing
+      mbar_arrive_expect_tx(bar0 + 8u * s, load ? uint32_t(qst::STAGE_BYTES) : 0u);
+      if (load) tma_load_3d(base + uint32_t(s * qst::STAGE_BYTES), &a.tm_x, bar0 + 8u * s, 0, hd, int(int64_t(g) * L + 32 * rb));
+    }
+    // no copy may still be writing shared memory when the CTA exits: wait
+    // (bounded) for the last phase of every stage used
+    for (int64_t k = j > qst::NST ? j - qst::NST : 0; k < j; k++) {
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait_sleep(bar0 + 8u * stage(k), uint32_t((k / qst::NST) & 1)))
+        if (global_ns() - t0 > kWaitLimitNs) break;
+    }
+    return;
+  }
+  // ---- consumers
+  uint8_t* rdata = a.row_data;
+  uint8_t* rsfc = a.row_sfc;
+  uint8_t* rsfp = a.row_sfp;
+  uint8_t* blk_sfp = a.sf_packed;
+  const int half = lane >> 4, c8 = (lane & 15) * 8, q = (lane & 15) >> 2;
+  const bool lead = (lane & 3) == 0;
+  const int cg = (warp - 1) / qst::HPU, hh = (warp - 1) % qst::HPU;
+  int64_t j = cg;
+  for (int64_t u = blockIdx.x + int64_t(cg) * gridDim.x; u < units;
+       u += int64_t(qst::NCG) * gridDim.x, j += qst::NCG) {
+    const int s = stage(j);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8u * s, uint32_t((j / qst::NST) & 1), &abort_flag, &g_status_quant)))
+      break;
+    const int hd = qst::HPU * int(u % NHU) + hh;
+    const int64_t rbg = u / NHU;
+    const int g = int(rbg / nrb), rb = int(rbg % nrb);
+    const int nr = min(32, L - 32 * rb);  // <= 0: padding block
+    if (hd < H) {  // the last unit of a block may hold fewer than HPU heads
+    const int w = rb & 3;                 // block within its 128-row tile
+    const int64_t r0 = int64_t(g) * L + 32 * rb;
+    const int64_t tile_g = int64_t(g) * ntile + (rb >> 2);
+    const bool pk = tile_g < a.packed_tiles;
+    if ((rsfp || blk_sfp) && !pk && lane == 0) atomicOr(&g_status_quant, DEV_BAD_INDEX);
+    const uint8_t* srow = qs_smem + s * qst::STAGE_BYTES + (half * 16) * qst::ROW_BYTES + hh * 256 + (lane & 15) * 16;
+    const int64_t col = int64_t(hd) * 128 + c8;
+    // ---- first pass
+    uint32_t cm[4] = {0, 0, 0, 0};
+    uint8_t* ratom = (rsfp && pk) ? rsfp + (tile_g * H + hd) * 512 : nullptr;
+#pragma unroll 4
+    for (int i = 0; i < 16; i++) {
+      const int r = half * 16 + i;
+      const uint4 v = nr > 0 ? *reinterpret_cast<const uint4*>(srow + i * qst::ROW_BYTES) : make_uint4(0, 0, 0, 0);
+      const uint32_t ax = abs2(v.x), ay = abs2(v.y), az = abs2(v.z), aw = abs2(v.w);
+      if (r < nr) {
+        cm[0] = __vmaxu2(cm[0], ax);
+        cm[1] = __vmaxu2(cm[1], ay);
+        cm[2] = __vmaxu2(cm[2], az);
+        cm[3] = __vmaxu2(cm[3], aw);
+      }
+      {
+        uint32_t t = __vmaxu2(__vmaxu2(ax, ay), __vmaxu2(az, aw));
+        t = __vmaxu2(t, __shfl_xor_sync(0xFFFFFFFFu, t, 1));
+        t = __vmaxu2(t, __shfl_xor_sync(0xFFFFFFFFu, t, 2));
+        const uint32_t sc = e8m0_from_bf16abs(hmax2(t));
+        if (r < nr) {
+          float2 p[4];
+          unpack8(v, p);
+          const float f = e8m0_inv_scale(sc);
+          const float2 fi[4] = {make_float2(f, f), make_float2(f, f), make_float2(f, f), make_float2(f, f)};
+          uint2 o = conv8(p, fi);
+          if (sc == 0xFFu) o = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          *reinterpret_cast<uint2*>(rdata + (r0 + r) * cols + col) = o;
+          if (lead && rsfc) rsfc[(r0 + r) * (cols / 32) + hd * 4 + q] = uint8_t(sc);
+        }
+        if (lead && ratom) ratom[atom_off(w * 32 + r, q)] = r < nr ? uint8_t(sc) : uint8_t(0x7F);
+      }
+    }
+    {
+      // the column maxima of the two half-blocks of rows
+#pragma unroll
+      for (int k = 0; k < 4; k++) cm[k] = __vmaxu2(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 16));
+      uint32_t sc[8];
+      if (MODE == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          sc[2 * i] = e8m0_from_bf16abs(cm[i] & 0xFFFFu);
+          sc[2 * i + 1] = e8m0_from_bf16abs(cm[i] >> 16);
+        }
+      } else {
+        uint32_t m = max(max(hmax2(cm[0]), hmax2(cm[1])), max(hmax2(cm[2]), hmax2(cm[3])));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const uint32_t sb = e8m0_from_bf16abs(m);
+#pragma unroll
+        for (int i = 0; i < 8; i++) sc[i] = sb;
+      }
+      float2 inv2[4];
+      uint2 badm = make_uint2(0, 0);
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const bool bad = sc[i] == 0xFFu;
+        const float f = bad ? 0.0f : e8m0_inv_scale(sc[i]);
+        if (i & 1) inv2[i >> 1].y = f; else inv2[i >> 1].x = f;
+        if (bad) {
+          if (i < 4) badm.x |= 0xFFu << (8 * i); else badm.y |= 0xFFu << (8 * (i - 4));
+        }
+      }
+      // the block's scales (from the lanes of the first row half)
+      if (half == 0) {
+        if (nr > 0 && a.sf_compact) {
+          const int64_t b32 = int64_t(g) * ((L + 31) / 32) + rb;
+          if (MODE == 1) {
+            uint2 sv;
+            sv.x = sc[0] | (sc[1] << 8) | (sc[2] << 16) | (sc[3] << 24);
+            sv.y = sc[4] | (sc[5] << 8) | (sc[6] << 16) | (sc[7] << 24);
+            *reinterpret_cast<uint2*>(a.sf_compact + b32 * cols + col) = sv;
+          } else if (lead) {
+            a.sf_compact[b32 * (cols / 32) + hd * 4 + q] = uint8_t(sc[0]);
+          }
+        }
+        if (blk_sfp && pk) {
+          if (MODE == 1) {
+            uint8_t* at = blk_sfp + (tile_g * H + hd) * 512;
+#pragma unroll
+            for (int i = 0; i < 8; i++) at[atom_off(c8 + i, w)] = nr > 0 ? uint8_t(sc[i]) : uint8_t(0x7F);
+          } else if (lead) {
+            blk_sfp[(tile_g * H + hd) * 16 + w * 4 + q] = nr > 0 ? uint8_t(sc[0]) : uint8_t(0x7F);
+          }
+        }
+      }
+      // ---- second pass: the block layout's payload
+#pragma unroll 4
+      for (int i = 0; i < 16; i++) {
+        const int r = half * 16 + i;
+        if (r < nr) {
+          const uint4 v = *reinterpret_cast<const uint4*>(srow + i * qst::ROW_BYTES);
+          float2 p[4];
+          unpack8(v, p);
+          uint2 o = conv8(p, inv2);
+          o.x = (o.x & ~badm.x) | (0x7F7F7F7Fu & badm.x);
+          o.y = (o.y & ~badm.y) | (0x7F7F7F7Fu & badm.y);
+          *reinterpret_cast<uint2*>(a.data + (r0 + r) * cols + col) = o;
+        }
+      }
+    }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar0 + 8u * (qst::NST + s));  // this warp is done with the stage
+  }
+}
+
+template <int MODE>
+cudaError_t launch_quant_stream(const QuantArgs& a, cudaStream_t st) {
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(quant_stream_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                qst::SMEM_BYTES);
+  });
+  if (e != cudaSuccess) return e;
+  const int nsm = sm_count_current_device();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  const int64_t units = int64_t(a.seq.nseq) * 4 * ((a.seq.seqlen + 127) / 128) * ((a.H + qst::HPU - 1) / qst::HPU);
+  if (units == 0) return cudaSuccess;
+  const unsigned grid = unsigned(units < nsm ? units : int64_t(nsm));
+  quant_stream_kernel<MODE><<<grid, qst::NTHREADS, qst::SMEM_BYTES, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   clear_stale_error();
   const int cols = a.H * a.D;
+  if (a.has_map && a.row_data) {
+    // dense, two outputs: the streaming kernel (one output: the register-staged
+    // kernels below keep up with the copy rate there)
+    if (a.mode == 1) return launch_quant_stream<1>(a, st);
+    if (a.mode == 2) return launch_quant_stream<2>(a, st);
+  }
   if (a.mode == 0) {
     dim3 grid((cols + 1023) / 1024, 4 * ((a.seq.seqlen + 127) / 128), a.seq.nseq);
     if (grid.y == 0 || grid.z == 0) return cudaSuccess;
@@ -287,10 +560,14 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
   }
   dim3 grid((cols + 255) / 256, (a.seq.seqlen + 127) / 128, a.seq.nseq);
   if (grid.y == 0 || grid.z == 0) return cudaSuccess;
-  if (a.mode == 1)
-    quant_kernel<1><<<grid, 128, 0, st>>>(a);
-  else
-    quant_kernel<2><<<grid, 128, 0, st>>>(a);
+  const bool row = a.row_data != nullptr;
+  if (a.mode == 1) {
+    if (row) quant_kernel<1, true><<<grid, 128, 0, st>>>(a);
+    else quant_kernel<1, false><<<grid, 128, 0, st>>>(a);
+  } else {
+    if (row) quant_kernel<2, true><<<grid, 128, 0, st>>>(a);
+    else quant_kernel<2, false><<<grid, 128, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -89,6 +89,43 @@ def test_quantize_dual(mx, blk, case):
         _check_dual(mx, q.reshape(160, 5, 128), None, 5, blk)
 
 
+@pytest.mark.parametrize("B,S,H", [(3, 200, 3), (2, 96, 4), (4, 128, 1)])
+def test_quantize_dense_batches(mx, B, S, H):
+    # dense batches of several sequences whose length is not a multiple of the
+    # 128-row tile (padding blocks inside each sequence's last tile), odd head
+    # counts (a half-used column chunk): every kind, single and dual output
+    import torch
+    q, _, _, _ = inputs.dense_attn(B, H, S, 128, seed=12 + S)
+    bits3 = q.reshape(B * S, H, 128)
+    tokens = B * S
+    seqs = mx.Seqs.dense(B, S)
+    lens = [S] * B
+    cu = np.arange(B + 1, dtype=np.int32) * S
+    x64 = f64(bits3).reshape(tokens, -1)
+    ref = {b: oracle.quantize(x64, b, cu) for b in (0, 1, 2)}
+
+    def check(m, b):
+        q_ref, s_ref = ref[b]
+        np.testing.assert_array_equal(host(m.data).reshape(tokens, -1), q_ref, err_msg=str(b))
+        np.testing.assert_array_equal(host(m.sf_compact), s_ref, err_msg=str(b))
+        comp, pad = unpack_packed(host(m.sf_packed), b, lens, H)
+        np.testing.assert_array_equal(comp, s_ref, err_msg=str(b))
+        assert np.all(pad == 0x7F), b
+
+    dev = to_dev(bits3)
+    for b in (0, 1, 2):
+        m = mx.quantize(dev, b, seqs)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        check(m, b)
+    for b in (1, 2):
+        first, row = mx.quantize_dual(dev, b, seqs)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        check(first, b)
+        check(row, 0)
+
+
 @pytest.mark.parametrize("blk,name", MODES)
 def test_quantize_tiny_dense(mx, blk, name):
     q, _, _, _ = inputs.dense_attn(1, 2, 256, 128, seed=0)
@@ -143,6 +180,7 @@ def test_quantize_full_llm_tensor(mx):
     seqs = mx.Seqs.dense(B, S)
     x64 = f64(q).reshape(B * S, H * D)
     cu = np.array([0, S, 2 * S], np.int32)
+    refs = {}
     for blk in (0, 1, 2):
         m = mx.quantize(dev, blk, seqs)
         torch.cuda.synchronize()
@@ -150,6 +188,15 @@ def test_quantize_full_llm_tensor(mx):
         q_ref, s_ref = oracle.quantize(x64, blk, cu)
         np.testing.assert_array_equal(host(m.data).reshape(B * S, -1), q_ref)
         np.testing.assert_array_equal(host(m.sf_compact), s_ref)
+        refs[blk] = (q_ref, s_ref)
+    # the one-read dual outputs, as the training step uses them
+    for blk in (1, 2):
+        first, row = mx.quantize_dual(dev, blk, seqs)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        for m, b in ((first, blk), (row, 0)):
+            np.testing.assert_array_equal(host(m.data).reshape(B * S, -1), refs[b][0], err_msg=str(b))
+            np.testing.assert_array_equal(host(m.sf_compact), refs[b][1], err_msg=str(b))
 
 
 @pytest.mark.parametrize("T,C,H,seg", [(256, 2048, 16, 128), (96, 256, 2, 32), (384, 512, 4, 128)])
