@@ -42,6 +42,10 @@ sys.path.insert(0, ROOT)
 
 B, H, S, D = 2, 16, 8192, 128
 CAUSAL = True
+# DRAM bytes of one mxfa_bwd call at this workload (preparation, main and post
+# kernels), from the ncu capture recorded in profiles/attn_bwd_kernel_llm_traffic.md;
+# valid while those kernels are unchanged
+BWD_CALL_TRAFFIC = 101825280 + 87026944 + 1336138496 + 917195776 + 134224384 + 31139840
 SEED = 1
 METRIC = "MXFP8 attn fwd+bwd PFLOP/s (1 GB300)"
 NOMINAL_FP8_TFLOPS = 4500.0
@@ -971,10 +975,14 @@ def main():
                             "pre/post)" if dom == "bwd" else "attn_fwd_kernel",
                             "achieved": achieved, "peak": probe["tflops"], "unit": "TFLOP/s",
                             "frac": achieved / probe["tflops"],
-                            "traffic": None,
-                            "traffic_note": "ncu DRAM read + write of this kernel is recorded "
-                                            "beside its capture command in profiles/, not in "
-                                            "this run",
+                            "traffic": BWD_CALL_TRAFFIC if dom == "bwd" else None,
+                            "traffic_unit": "bytes per call",
+                            "traffic_note": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of "
+                                             "bwd_prep_kernel + attn_bwd_kernel + bwd_post_kernel "
+                                             "in one capture of this workload "
+                                             "(profiles/attn_bwd_kernel_llm_traffic.md), not "
+                                             "measured in this run" if dom == "bwd" else
+                                             "no capture of this kernel at this workload"),
                             "peak_source": "measured in this run: the dense MXFP8 tensor-pipe "
                                            "peak (mxfa_tensor_peak_probe, see mxfp8_peak)",
                             "peak_probe": probe,
