@@ -394,8 +394,12 @@ mxfa_status mxfa_quantize_dual(const void* x, int64_t tokens, int H, int D, mxfa
   a.row_sfc = out_row->sf_compact;
   a.row_sfp = out_row->sf_packed;
   if (tokens == 0) return MXFA_OK;
-  // dense batches of at least one unit's heads take the streaming kernel
-  a.has_map = (!cu && H >= kQuantHeadsPerUnit && make_map_bf16_rows(&a.tm_x, x, tokens, H, kQuantHeadsPerUnit)) ? 1 : 0;
+  // dense batches of at least one unit's heads take the streaming kernel (its
+  // TMA row coordinate is a 32-bit integer)
+  a.has_map = (!cu && H >= kQuantHeadsPerUnit && tokens < (int64_t(1) << 31) &&
+               make_map_bf16_rows(&a.tm_x, x, tokens, H, kQuantHeadsPerUnit))
+                  ? 1
+                  : 0;
   return from_cuda(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
