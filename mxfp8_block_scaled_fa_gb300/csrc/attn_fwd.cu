@@ -587,16 +587,21 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
         // row by row.
         const bool staged = STAGE && __all_sync(0xFFFFFFFFu, valid);
         const uint32_t ost = base + L::OFF_OST + uint32_t(warp - 4) * OST_BYTES;
+        // the row's 128 accumulator columns, all four loads in flight at once
+        uint32_t oa[128];
+        if (any_key) {
+  #pragma unroll
+          for (int c = 0; c < 4; c++) tmem_ld32(tmem + lane_base + col_o + 32 * c, oa + 32 * c);
+          tmem_wait_ld();
+  #pragma unroll
+          for (int c = 0; c < 4; c++) reg_fence32(oa + 32 * c);
+        } else {
+  #pragma unroll
+          for (int e = 0; e < 128; e++) oa[e] = 0u;
+        }
   #pragma unroll
         for (int c = 0; c < 4; c++) {
-          uint32_t o[32];
-          if (any_key) {
-            tmem_ld32(tmem + lane_base + col_o + 32 * c, o);
-            tmem_wait_ld();
-          } else {
-  #pragma unroll
-            for (int e = 0; e < 32; e++) o[e] = 0u;
-          }
+          const uint32_t* o = oa + 32 * c;
           const float r = any_key ? rl : 0.0f;
           uint32_t w[16];
   #pragma unroll
