@@ -78,7 +78,8 @@ constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "backward tile exceeds the shared memory of one CTA");
 // the dK / dV epilogue stages 8 x 4 KB of 128B-swizzled rows in the Q ring
-static_assert(OFF_Q % 1024 == 0 && NSQ * QD_BYTES >= 8 * 4096, "dK / dV staging does not fit the Q ring");
+static_assert(OFF_Q % 1024 == 0 && OFF_DO == OFF_Q + NSQ * QD_BYTES && 2 * NSQ * QD_BYTES >= 8 * 8192,
+              "dK / dV staging does not fit the Q and dO rings");
 
 constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 256, COL_DP = 320, COL_DQ = 384;
 constexpr uint32_t COL_SFK = 448, COL_SFV = 452, COL_SFKT = 456, COL_SFQ = 460, COL_SFDO = 464,
@@ -693,18 +694,25 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
       uint8_t* mxd = hq == 0 ? a.dvmx : a.dkmx;
       uint32_t sfw = 0;  // E8M0 scales of the MXFP8 gradient row, one byte per 32 columns
       // A warp whose 32 key rows all lie inside the sequence sends its rows out
-      // by TMA stores of 32-row x 64-column halves staged in shared memory (the
-      // Q ring, idle now that every GEMM has completed; 128B-swizzled rows):
-      // a thread storing its own 256-byte row touches 32 rows 2H KB apart per
-      // instruction.  Other warps store row by row.
+      // by TMA stores of 32-row x 64-column halves staged in shared memory (8 KB
+      // per warp in the Q and dO rings, idle now that every GEMM has completed,
+      // so both halves are staged without waiting for the first one's store;
+      // 128B-swizzled rows): a thread storing its own 256-byte row touches 32
+      // rows 2H KB apart per instruction.  Other warps store row by row.
       const bool staged = __all_sync(0xFFFFFFFFu, kvalid);
-      const uint32_t stg = base + OFF_Q + uint32_t(warp - 4) * 4096u;
+      const uint32_t stg = base + OFF_Q + uint32_t(warp - 4) * 8192u;
       const CUtensorMap* tmo = hq == 0 ? &a.tm_dv : &a.tm_dk;
+      uint32_t vv[64];  // two 32-column loads per wait
 #pragma unroll
       for (int c = 0; c < 4; c++) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + col + 32 * c, v);
-        tmem_wait_ld();
+        if ((c & 1) == 0) {
+          tmem_ld32(tmem + lane_base + col + 32 * c, vv);
+          tmem_ld32(tmem + lane_base + col + 32 * c + 32, vv + 32);
+          tmem_wait_ld();
+          reg_fence32(vv);
+          reg_fence32(vv + 32);
+        }
+        const uint32_t* v = vv + 32 * (c & 1);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
@@ -714,22 +722,18 @@ __global__ void __launch_bounds__(bwd::NTHREADS, 1) attn_bwd_kernel(const __grid
           w[e] = *reinterpret_cast<uint32_t*>(&p2);
         }
         if (staged) {
-          // the first half's store has read the area before the second half
-          if (c == 2) {
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-          }
+          const uint32_t half = stg + uint32_t(c >> 1) * 4096u;
 #pragma unroll
           for (int v4 = 0; v4 < 4; v4++) {
             const uint32_t chunk = uint32_t((c & 1) * 4 + v4) ^ uint32_t(lane & 7);
-            st_shared_v4(stg + uint32_t(lane) * 128u + (chunk << 4), w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+            st_shared_v4(half + uint32_t(lane) * 128u + (chunk << 4), w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
                          w[4 * v4 + 3]);
           }
           if (c & 1) {
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(tmo, stg, 64 * (c >> 1), h, int(tok - lane));
+              tma_store_3d(tmo, half, 64 * (c >> 1), h, int(tok - lane));
               bulk_commit();
             }
           }
