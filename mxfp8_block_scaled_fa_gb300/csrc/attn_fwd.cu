@@ -267,11 +267,18 @@ __global__ void __launch_bounds__(fwd::NTHREADS, 1) attn_fwd_kernel(const __grid
           // every reader has released entry r - 2
           if (r >= 2 && !mbar_wait(BAR(B_IEMPTY + (r & 1)), ((r >> 1) - 1) & 1, abort_flag, &g_status_fwd)) break;
           int it = r == 0 ? int(blockIdx.x) : int(gridDim.x + atomicAdd(&g_fwd_sched[a.sched_slot][0], 1u));
+          FwdItem w = fwd_item(a, ok && it < nitems ? it : 0);
+          // a varlen item whose query pair lies past its sequence is skipped
+          // here rather than passed through the ring to every reader (dense
+          // items are never empty)
+          while (a.sq.cu != nullptr && ok && it < nitems && !w.valid) {
+            it = int(gridDim.x + atomicAdd(&g_fwd_sched[a.sched_slot][0], 1u));
+            if (it < nitems) w = fwd_item(a, it);
+          }
           if (!ok || it >= nitems) it = -1;
           s_items[r & 1] = it;
           mbar_arrive(BAR(B_IFULL + (r & 1)));
           if (it < 0) break;
-          const FwdItem w = fwd_item(a, it);
           if (!w.valid) continue;
           const int64_t tq_g = tiles_before(a.sq, w.g) + 2 * w.qp;  // packed tile of Q_A
           const int64_t tk_g0 = tiles_before(a.sk, w.g);            // packed tile of key tile 0
