@@ -89,11 +89,12 @@ def test_quantize_dual(mx, blk, case):
         _check_dual(mx, q.reshape(160, 5, 128), None, 5, blk)
 
 
-@pytest.mark.parametrize("B,S,H", [(3, 200, 3), (2, 96, 4), (4, 128, 1)])
+@pytest.mark.parametrize("B,S,H", [(3, 200, 3), (2, 96, 4), (4, 128, 1), (3, 5, 2)])
 def test_quantize_dense_batches(mx, B, S, H):
     # dense batches of several sequences whose length is not a multiple of the
     # 128-row tile (padding blocks inside each sequence's last tile), odd head
-    # counts (a half-used column chunk): every kind, single and dual output
+    # counts (a half-used column chunk), a tensor shorter than one 32-row
+    # block: every kind, single and dual output
     import torch
     q, _, _, _ = inputs.dense_attn(B, H, S, 128, seed=12 + S)
     bits3 = q.reshape(B * S, H, 128)
